@@ -1,0 +1,344 @@
+"""Benchmark of one EAGLE speculative step on libeaglespec (GB300).
+
+A step is the whole hot path over one batch: FC fuse of the auxiliary hidden
+states, K draft passes (draft layer + LM head), verification of the drafts
+against target logits.  Default workload: the Llama-3.1-8B-shaped EAGLE-3 chain
+(H 4096, 32/8 heads, MLP 14336, vocab 128256, bf16, batch 4, context 256,
+K 5, greedy verification) with synthetic random-init weights and inputs.
+
+Prints one JSON line.  `--impl reference` times the CPU oracle instead on a
+bounded sample of the same workload.  Under torchrun every rank runs its own
+replica (requests are independent: weak scaling, no data-path collective).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from eagle_speculative_decoding_step_gb300 import configs, synth  # noqa: E402
+
+METRIC = "spec steps/s"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def step_bytes(w):
+    """Algorithmic HBM bytes of one chain step (weights once per pass, allowed K/V,
+    target logits once) and the LM head's bytes per launch."""
+    es = 2 if w.dtype == "bf16" else 4
+    H, nq, nkv, hd, I, V = w.H, w.nq, w.nkv, w.hd, w.I, w.V
+    layer = (2 * H * (nq + 2 * nkv) * hd + nq * hd * H + 3 * H * I) * es
+    fc = 3 * H * H * es
+    head = V * H * es
+    kv_per_pass = w.B * (w.max_ctx + w.K) * 2 * nkv * hd * es
+    verify = w.B * (w.K + 1) * V * 4
+    total = fc + w.K * (layer + head + kv_per_pass) + verify
+    lm_launch = head + w.B * H * es
+    return total, lm_launch
+
+
+def run_gpu(args, w):
+    import torch
+    from eagle_speculative_decoding_step_gb300 import binding as lib, engine
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = "cuda:%d" % local
+    lib.load()
+
+    t0 = time.time()
+    W = synth.make_weights(w)
+    ctx = synth.context_lengths(w)
+    kv = synth.make_kv(w, ctx)
+    aux = synth.make_aux(w)
+    root = synth.root_tokens(w)
+    dm = engine.DeviceModel(w, W, kv, ctx, device=device)
+    del W
+    gen_s = time.time() - t0
+
+    aux_d = engine.to_device(aux, w.dtype, device)
+    root_d = torch.from_numpy(root).to(device)
+    # target logits = the draft's own logits over K+1 chained passes + N(0, sigma)
+    # (built once, untimed, with the library's debug full-logits LM head)
+    B, K, V = w.B, w.K, w.V
+    target = torch.empty(B, K + 1, V, dtype=torch.float32, device=device)
+    h0 = dm.hidden(B)
+    pre = [dm.hidden(B), dm.hidden(B)]
+    hn = dm.hidden(B)
+    ids = torch.zeros(B, K + 1, dtype=torch.int32, device=device)
+    lp = torch.zeros(B, K + 1, dtype=torch.float32, device=device)
+    logits = torch.empty(B, V, dtype=torch.float32, device=device)
+    lib.spec_fc_fuse(dm.desc, dm.weights, aux_d, h0, B, dm.ws)
+    hid = h0
+    for i in range(K + 1):
+        tok = root_d if i == 0 else ids.data_ptr() + 4 * (i - 1)
+        rows = lib.make_rows(B, B, 1, dm.ctx_len, tok, step=i, tok_stride=1 if i == 0 else K + 1)
+        lib.spec_draft_layer(dm.desc, dm.weights, rows, hid, pre[i % 2], hn, dm.kv, dm.ws)
+        if w.rank > 0:
+            lib.spec_lowrank_candidates(dm.desc, dm.weights, hn, B, 1, ids.data_ptr() + 4 * i, ws=dm.ws,
+                                        out_ld=K + 1)
+            lib.spec_lm_head(dm.desc, dm.weights, hn, B, 1, torch.zeros(B, 1, dtype=torch.int32, device=device),
+                             torch.zeros(B, 1, device=device), None, logits, ws=dm.ws)
+        else:
+            lib.spec_lm_head(dm.desc, dm.weights, hn, B, 1, ids.data_ptr() + 4 * i, lp.data_ptr() + 4 * i, None,
+                             logits, ws=dm.ws, ids_ld=K + 1)
+        target[:, i].copy_(logits)
+        hid = pre[i % 2]
+    noise = torch.from_numpy(synth.noise(w, (B, K + 1, V))).to(device)
+    target.add_(noise)
+    del noise
+    torch.cuda.synchronize()
+
+    temp = torch.full((B,), w.temperature, dtype=torch.float32, device=device)
+    st = engine.ChainStep(dm, aux_d, root_d, target, temperature=temp, seed=w.philox_seed)
+    # warm-up (also builds tensor maps / sets kernel attributes), then capture one step
+    for _ in range(max(1, args.warmup)):
+        st.run()
+    torch.cuda.synchronize()
+    assert dm.device_error() == 0, "device error after warm-up"
+    stream = torch.cuda.Stream(device=device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            st.run()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    acc = st.acc.cpu().numpy()
+    verified = float((acc + 1).sum())
+
+    # dominant kernel (LM head GEMM with fused top-k / lse epilogue), timed alone
+    lm_ids = torch.zeros(B, 1, dtype=torch.int32, device=device)
+    lm_lp = torch.zeros(B, 1, dtype=torch.float32, device=device)
+    n_lm = 20
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            lib.spec_lm_head(dm.desc, dm.weights, st.hn, B, 1, lm_ids, lm_lp, ws=dm.ws)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_lm):
+            lib.spec_lm_head(dm.desc, dm.weights, st.hn, B, 1, lm_ids, lm_lp, ws=dm.ws)
+        a1.record(stream)
+    torch.cuda.synchronize()
+    lm_ms = a0.elapsed_time(a1) / n_lm
+
+    # end to end through the public API with host buffers: inputs H2D from pinned
+    # memory, step, result D2H, every step
+    aux_h = aux_d.cpu().pin_memory()
+    root_h = root_d.cpu().pin_memory()
+    tgt_h = target.cpu().pin_memory()
+    out_h = torch.empty(B, K + 1, dtype=torch.int32).pin_memory()
+    acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    n_e2e = max(3, args.steps // 2)
+    with torch.cuda.stream(stream):
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(n_e2e):
+            aux_d.copy_(aux_h, non_blocking=True)
+            root_d.copy_(root_h, non_blocking=True)
+            target.copy_(tgt_h, non_blocking=True)
+            graph.replay()
+            out_h.copy_(st.out, non_blocking=True)
+            acc_h.copy_(st.acc, non_blocking=True)
+        b1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = b0.elapsed_time(b1) / n_e2e
+    h2d = aux_h.numel() * aux_h.element_size() + root_h.numel() * 4 + tgt_h.numel() * 4
+    d2h = out_h.numel() * 4 + acc_h.numel() * 4
+    assert dm.device_error() == 0, "device error in the timed region"
+
+    hbm, tf, kind = _peaks()
+    total_bytes, lm_bytes = step_bytes(w)
+    lm_gbs = lm_bytes / (lm_ms * 1e-3) / 1e9
+    launches_per_step = 2 + K * 13 + 2
+    res = {
+        "metric": METRIC, "value": world * 1000.0 / ms_step, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded random-init weights, N(0,1) aux states and context K/V)",
+        "config": {"workload": w.name, "H": w.H, "heads": [w.nq, w.nkv], "head_dim": w.hd, "I": w.I, "V": w.V,
+                   "batch": w.B, "ctx": w.ctx, "K": K, "verify": w.verify,
+                   "l2": "inputs larger than L2 (weights %.2f GB streamed per step)" % (total_bytes / 1e9),
+                   "graph": "one CUDA graph per step"},
+        "draft_tokens_per_s": world * B * K * 1000.0 / ms_step,
+        "verified_tokens_per_s": world * verified * 1000.0 / ms_step,
+        "step_roofline": {"bytes": total_bytes, "t_roof_ms": total_bytes / (hbm * 1e9) * 1e3,
+                          "frac": (total_bytes / (hbm * 1e9) * 1e3) / ms_step},
+        "roofline": {"kernel": "tc_kernel<SchedRows, EpiStats> (LM head, fused top-k/lse)", "bound": "hbm",
+                     "achieved": lm_gbs, "peak": hbm, "unit": "GB/s", "frac": lm_gbs / hbm, "traffic": None,
+                     "peak_kind": kind + " (burst copy)", "ms_per_launch": lm_ms},
+        "e2e": {"value": world * 1000.0 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "setup_s": gen_s,
+    }
+    return res, rank
+
+
+def run_cpu_baseline(w, budget_s=20.0):
+    """The oracle (fp64 numpy) on a bounded sample: one draft pass of the whole
+    batch plus verification; steps/s extrapolated to K passes."""
+    import copy
+    from oracle import draft as od, verify as ov
+    import threadpoolctl  # noqa: F401  (optional)
+
+    t0 = time.time()
+    W = synth.make_weights(w)
+    ctx = synth.context_lengths(w)
+    kv = synth.make_kv(w, ctx)
+    aux = synth.make_aux(w)
+    root = synth.root_tokens(w)
+    gen = time.time() - t0
+    t1 = time.time()
+    h0 = od.fc_fuse(w, W, aux)
+    rows = {"M": w.B, "B": w.B, "R": 1, "step": 0, "ctx_len": ctx, "tok": root}
+    pre, hn = od.draft_layer(w, W, rows, h0, kv)
+    ids, lp, lse, logits = od.lm_head(w, W, hn, 1)
+    t_pass = time.time() - t1
+    target = np.repeat(logits[:, None, :], w.K + 1, axis=1).astype(np.float32)
+    t2 = time.time()
+    ov.verify_greedy_chain(target, np.repeat(ids, w.K, axis=1))
+    t_ver = time.time() - t2
+    step_s = w.K * t_pass + t_ver
+    return {"value": 1.0 / step_s, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "one draft pass (FC + layer + LM head) over the full batch, timed once, x K passes + "
+                      "one greedy verification; generation %.1fs excluded" % gen}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="llama8b_chain")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = configs.WORKLOADS[args.config]
+    if w.mode != "chain":
+        raise SystemExit("bench.py times chain workloads; tree steps are timed by the tests")
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        t0 = time.time()
+        vals = []
+        for _ in range(args.warmup + args.steps if args.steps <= 3 else 3):
+            vals.append(run_cpu_baseline(w)["value"])
+        v = statistics.median(vals)
+        cb = run_cpu_baseline(w) if False else {"kind": "oracle", "cores": os.cpu_count(),
+                                                "sample": "one draft pass over the full batch x K + verify"}
+        cb["value"] = v
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": 1,
+                          "steps": len(vals), "warmup": 0, "higher_is_better": True, "scaling": "weak",
+                          "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": {"workload": w.name}, "cpu_baseline": cb,
+                          "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                          "wall_s": time.time() - t0}))
+        return
+    res, rank = run_gpu(args, w)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = run_cpu_baseline(w)
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

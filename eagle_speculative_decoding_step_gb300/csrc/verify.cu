@@ -1,0 +1,344 @@
+// Verification of drafts against target logits.
+//
+// [NEURON] "Speculative Decoding (EAGLE3) in the vLLM Neuron Framework",
+// section "Rejection Sampling": the on-device greedy sampler (match mask,
+// first mismatch, accept through the mismatch emitting the target token, bonus
+// token when all match, -1 padding) and the CPU probabilistic sampler
+// (arXiv:2211.17192: accept when u <= p(draft) with draft prob 1; recovered
+// token by Gumbel-max over the target distribution with the draft token
+// removed; bonus token sampled from the target at the last position).
+// Tree verification ([EAGLET] introduction: the target verifies the tree in one
+// pass): a node is accepted when its parent is and its token equals the
+// target's argmax at the parent; the deepest accepted node's path is emitted,
+// then its K/V is compacted to contiguous cache indices.
+//
+// Both verifiers are one streaming read of the fp32 target logits (HBM-bound):
+// kernel 1 splits every row into chunks and reduces each chunk (argmax, or
+// max / sum-exp / Gumbel key for the stochastic sampler); kernel 2 runs one
+// CTA per request over the chunk partials and makes the sequential accept
+// decisions, writes the outputs and moves the accepted K/V.
+#include "common.cuh"
+#include "internal.h"
+
+namespace spec {
+
+struct ArgPart { float v; int i; };
+struct RejPart { float m, s, key; int idx; };
+
+static int verify_chunks(int rows, int V) {
+  int want = (640 + rows - 1) / rows;
+  int cap = V / 4096;
+  if (cap < 1) cap = 1;
+  if (want > cap) want = cap;
+  if (want > 64) want = 64;
+  return want < 1 ? 1 : want;
+}
+static int chunk_len(int V, int nch) { int L = (V + nch - 1) / nch; return (L + 3) & ~3; }
+
+// ---------------------------------------------------------------- greedy argmax
+template <bool VEC>
+__global__ void __launch_bounds__(256) argmax_chunks_kernel(const float* __restrict__ logits, int V,
+                                                           int nch, int L, ArgPart* __restrict__ part) {
+  __shared__ float rv[32];
+  __shared__ int ri[32];
+  const int row = blockIdx.y, c = blockIdx.x;
+  const float* x = logits + (size_t)row * V;
+  const int lo = c * L, hi = min(V, lo + L);
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  if (VEC) {
+    for (int j = lo + 4 * threadIdx.x; j < hi; j += 4 * blockDim.x) {
+      float4 q = *reinterpret_cast<const float4*>(x + j);
+      if (better(q.x, j, bv, bi)) { bv = q.x; bi = j; }
+      if (j + 1 < hi && better(q.y, j + 1, bv, bi)) { bv = q.y; bi = j + 1; }
+      if (j + 2 < hi && better(q.z, j + 2, bv, bi)) { bv = q.z; bi = j + 2; }
+      if (j + 3 < hi && better(q.w, j + 3, bv, bi)) { bv = q.w; bi = j + 3; }
+    }
+  } else {
+    for (int j = lo + threadIdx.x; j < hi; j += blockDim.x) {
+      float q = x[j];
+      if (better(q, j, bv, bi)) { bv = q; bi = j; }
+    }
+  }
+  block_argmax(bv, bi, rv, ri);
+  if (threadIdx.x == 0) part[(size_t)row * nch + c] = ArgPart{bv, bi};
+}
+
+__device__ int merged_argmax(const ArgPart* part, int row, int nch) {
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int c = 0; c < nch; ++c) {
+    ArgPart p = part[(size_t)row * nch + c];
+    if (better(p.v, p.i, bv, bi)) { bv = p.v; bi = p.i; }
+  }
+  return bi;
+}
+
+// Moves the accepted path's K/V from cache index ctx + src[d] to ctx + d,
+// d = 1 .. a, in increasing d (a source index is never below its destination
+// and sources increase along the path, so no source is overwritten first).
+template <typename T>
+__device__ void compact_path(const spec_kv& kv, int b, int ctx, const int* src, int a, int row_elems,
+                             void* ws) {
+  for (int d = 1; d <= a; ++d) {
+    long long s = slot_of(kv, b, ctx + src[d]);
+    long long t = slot_of(kv, b, ctx + d);
+    if (s < 0 || t < 0) {
+      if (threadIdx.x == 0) report(ws, SPEC_ERR_DEVICE, b, d);
+    } else if (s != t) {
+      T* K = reinterpret_cast<T*>(kv.k);
+      T* Vv = reinterpret_cast<T*>(kv.v);
+      for (int e = threadIdx.x; e < row_elems; e += blockDim.x) {
+        K[t * row_elems + e] = K[s * row_elems + e];
+        Vv[t * row_elems + e] = Vv[s * row_elems + e];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(128) verify_greedy_finalize_kernel(
+    int R, int nch, const ArgPart* __restrict__ part, const int32_t* __restrict__ draft,
+    const int32_t* __restrict__ parent, int max_depth, int32_t* __restrict__ out,
+    int32_t* __restrict__ acc_out, int32_t* __restrict__ kv_src, spec_kv kv, int has_kv,
+    int row_elems, int elem_bytes, const int32_t* __restrict__ ctx_len, void* ws) {
+  __shared__ int t[64];
+  __shared__ int path[65];
+  __shared__ int s_a;
+  const int b = blockIdx.x;
+  for (int n = threadIdx.x; n < R; n += blockDim.x) t[n] = merged_argmax(part, b * R + n, nch);
+  __syncthreads();
+  const int W = (parent == nullptr) ? R : max_depth + 1;
+  if (threadIdx.x == 0) {
+    int a = 0;
+    if (parent == nullptr) {
+      const int K = R - 1;
+      const int32_t* d = draft + (size_t)b * K;
+      while (a < K && d[a] == t[a]) ++a;
+      for (int i = 0; i < W; ++i) {
+        out[(size_t)b * W + i] = i < a ? d[i] : (i == a ? t[a] : -1);
+        if (kv_src) kv_src[(size_t)b * W + i] = i <= a ? i : -1;
+      }
+      path[0] = 0;
+    } else {
+      const int32_t* tok = draft + (size_t)b * R;
+      const int32_t* par = parent + (size_t)b * R;
+      unsigned long long accepted = 1ull;   // R <= 64
+      int depth[64];
+      depth[0] = 0;
+      int best = 0;
+      for (int n = 1; n < R; ++n) {
+        int p = par[n];
+        if (p < 0 || p >= n) {
+          report(ws, SPEC_ERR_DEVICE, b, n);
+          depth[n] = 0;
+          continue;
+        }
+        depth[n] = depth[p] + 1;
+        if (((accepted >> p) & 1ull) && tok[n] == t[p]) {
+          accepted |= 1ull << n;
+          if (depth[n] > depth[best]) best = n;
+        }
+      }
+      a = depth[best];
+      if (a > max_depth) {
+        report(ws, SPEC_ERR_DEVICE, b, a);
+        a = max_depth;
+      }
+      int n = best;
+      for (int dd = depth[best]; dd > 0; --dd) {
+        if (dd <= a) path[dd] = n;
+        n = par[n];
+      }
+      path[0] = 0;
+      for (int i = 0; i < W; ++i) {
+        int o = -1;
+        if (i < a) o = tok[path[i + 1]];
+        else if (i == a) o = t[best];
+        out[(size_t)b * W + i] = o;
+        if (kv_src) kv_src[(size_t)b * W + i] = i <= a ? path[i] : -1;
+      }
+    }
+    acc_out[b] = a;
+    s_a = a;
+  }
+  __syncthreads();
+  if (parent != nullptr && has_kv) {
+    const int ctx = ctx_len[b];
+    if (elem_bytes == 2)
+      compact_path<__nv_bfloat16>(kv, b, ctx, path, s_a, row_elems, ws);
+    else
+      compact_path<float>(kv, b, ctx, path, s_a, row_elems, ws);
+  }
+}
+
+// ---------------------------------------------------------------- rejection
+template <bool VEC>
+__global__ void __launch_bounds__(256) rejection_chunks_kernel(
+    const float* __restrict__ logits, int K, int V, int nch, int L, const int32_t* __restrict__ draft,
+    const float* __restrict__ temperature, uint2 key, uint32_t ctr_w, RejPart* __restrict__ part) {
+  __shared__ float red[32];
+  __shared__ int redi[32];
+  const int row = blockIdx.y, c = blockIdx.x;
+  const int b = row / (K + 1), i = row % (K + 1);
+  const float T = temperature[b];
+  const bool greedy = !(T > 0.f);
+  const int excl = (!greedy && i < K) ? draft[(size_t)b * K + i] : -1;
+  const float* x = logits + (size_t)row * V;
+  const int lo = c * L, hi = min(V, lo + L);
+  float m = -INFINITY, s = 0.f, bk = -INFINITY;
+  int bi = 0x7fffffff;
+  // every thread handles aligned groups of 4 vocabulary ids = one Philox block
+  for (int j = lo + 4 * threadIdx.x; j < hi; j += 4 * blockDim.x) {
+    float v[4];
+    if (VEC) {
+      float4 q = *reinterpret_cast<const float4*>(x + j);
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+#pragma unroll
+      for (int l = 0; l < 4; ++l) v[l] = (j + l < hi) ? x[j + l] : -INFINITY;
+    }
+    if (greedy) {
+#pragma unroll
+      for (int l = 0; l < 4; ++l)
+        if (j + l < hi && better(v[l], j + l, bk, bi)) { bk = v[l]; bi = j + l; }
+      continue;
+    }
+    uint4 r = philox4x32_10(make_uint4((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b, ctr_w), key);
+    uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      if (j + l >= hi) break;
+      float y = v[l] / T;
+      if (y > m) { s = s * expf(m - y) + 1.f; m = y; }
+      else s += expf(y - m);
+      if (j + l == excl) continue;
+      float u = word_to_uniform(w[l]);
+      float g = y - logf(-logf(u));
+      if (better(g, j + l, bk, bi)) { bk = g; bi = j + l; }
+    }
+  }
+  // reduce (m, s)
+  float bm = block_max(m, red);
+  float contrib = (m == -INFINITY) ? 0.f : s * expf(m - bm);
+  float bs = block_sum(contrib, red);
+  block_argmax(bk, bi, red, redi);
+  if (threadIdx.x == 0) part[(size_t)row * nch + c] = RejPart{bm, bs, bk, bi};
+}
+
+__global__ void __launch_bounds__(32) rejection_finalize_kernel(
+    const float* __restrict__ logits, int K, int V, int nch, const RejPart* __restrict__ part,
+    const int32_t* __restrict__ draft, const float* __restrict__ temperature, uint2 key, uint32_t ctr_w0,
+    int32_t* __restrict__ out, int32_t* __restrict__ acc_out, int32_t* __restrict__ kv_src) {
+  const int b = blockIdx.x;
+  if (threadIdx.x != 0) return;
+  const float T = temperature[b];
+  const bool greedy = !(T > 0.f);
+  int a = 0, emitted = -1;
+  for (int i = 0; i <= K; ++i) {
+    const size_t row = (size_t)b * (K + 1) + i;
+    float M = -INFINITY, S = 0.f, bk = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int c = 0; c < nch; ++c) {
+      RejPart p = part[row * nch + c];
+      if (p.m > M) { S = S * expf(M - p.m) + p.s; M = p.m; }
+      else if (p.m > -INFINITY) S += p.s * expf(p.m - M);
+      if (better(p.key, p.idx, bk, bi)) { bk = p.key; bi = p.idx; }
+    }
+    if (i == K) { emitted = bi; break; }
+    const int d = draft[(size_t)b * K + i];
+    bool ok;
+    if (greedy) {
+      ok = (d == bi);
+    } else {
+      float lse = M + logf(S);
+      float pd = (d >= 0 && d < V) ? expf(logits[row * V + d] / T - lse) : 0.f;
+      uint4 r = philox4x32_10(make_uint4(0u, (uint32_t)i, (uint32_t)b, ctr_w0), key);
+      ok = word_to_uniform(r.x) <= pd;
+    }
+    if (!ok) { emitted = bi; break; }
+    ++a;
+  }
+  for (int i = 0; i <= K; ++i) {
+    out[(size_t)b * (K + 1) + i] = i < a ? draft[(size_t)b * K + i] : (i == a ? emitted : -1);
+    if (kv_src) kv_src[(size_t)b * (K + 1) + i] = i <= a ? i : -1;
+  }
+  acc_out[b] = a;
+}
+
+}  // namespace spec
+
+using namespace spec;
+
+extern "C" size_t spec_verify_workspace_bytes(int32_t B, int32_t R, int32_t V) {
+  if (B <= 0 || R <= 0 || V <= 0) return 0;
+  int rows = B * R;
+  int nch = verify_chunks(rows, V);
+  return kWsHeader + align_up((size_t)rows * nch * sizeof(RejPart), 256);
+}
+
+extern "C" spec_status spec_verify_greedy(int32_t B, int32_t R, int32_t V, const float* target_logits,
+                                          const int32_t* draft_tok, const int32_t* parent,
+                                          int32_t max_depth, int32_t* out_tok, int32_t* accept_len,
+                                          int32_t* kv_src, const spec_model_desc* desc,
+                                          const spec_kv* kv, const int32_t* ctx_len, void* ws,
+                                          size_t ws_bytes, spec_stream_t stream) {
+  if (B <= 0 || R <= 0 || V <= 0) return SPEC_ERR_SHAPE;
+  if (!target_logits || !draft_tok || !out_tok || !accept_len) return SPEC_ERR_ARG;
+  if (R > 64) return SPEC_ERR_CAPACITY;
+  if (parent == nullptr && R < 2) return SPEC_ERR_SHAPE;
+  if (parent != nullptr && (max_depth < 0 || max_depth >= 64)) return SPEC_ERR_SHAPE;
+  if (!ws || !aligned(ws, 256) || ws_bytes < spec_verify_workspace_bytes(B, R, V)) return SPEC_ERR_WORKSPACE;
+  int has_kv = 0, row_elems = 0, elem_bytes = 4;
+  spec_kv kvv{};
+  if (parent != nullptr && kv != nullptr) {
+    if (!desc || !ctx_len || !kv->k || !kv->v || !kv->block_table) return SPEC_ERR_ARG;
+    if (kv->block_size <= 0 || kv->max_blocks <= 0 || kv->num_slots <= 0) return SPEC_ERR_SHAPE;
+    has_kv = 1;
+    kvv = *kv;
+    row_elems = desc->n_kv_heads * desc->head_dim;
+    elem_bytes = desc->dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  }
+  const int rows = B * R;
+  const int nch = verify_chunks(rows, V);
+  const int L = chunk_len(V, nch);
+  ArgPart* part = reinterpret_cast<ArgPart*>(static_cast<char*>(ws) + kWsHeader);
+  dim3 grid(nch, rows);
+  const bool vec = (V % 4 == 0) && aligned(target_logits, 16);
+  if (vec)
+    argmax_chunks_kernel<true><<<grid, 256, 0, stream>>>(target_logits, V, nch, L, part);
+  else
+    argmax_chunks_kernel<false><<<grid, 256, 0, stream>>>(target_logits, V, nch, L, part);
+  verify_greedy_finalize_kernel<<<B, 128, 0, stream>>>(R, nch, part, draft_tok, parent, max_depth, out_tok,
+                                                       accept_len, kv_src, kvv, has_kv, row_elems, elem_bytes,
+                                                       ctx_len, ws);
+  return last_launch();
+}
+
+extern "C" spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, const float* target_logits,
+                                             const int32_t* draft_tok, const float* temperature,
+                                             uint64_t seed, uint64_t step_offset, int32_t* out_tok,
+                                             int32_t* accept_len, int32_t* kv_src, void* ws,
+                                             size_t ws_bytes, spec_stream_t stream) {
+  if (B <= 0 || K <= 0 || V <= 0) return SPEC_ERR_SHAPE;
+  if (!target_logits || !draft_tok || !temperature || !out_tok || !accept_len) return SPEC_ERR_ARG;
+  const int R = K + 1;
+  if (!ws || !aligned(ws, 256) || ws_bytes < spec_verify_workspace_bytes(B, R, V)) return SPEC_ERR_WORKSPACE;
+  const int rows = B * R;
+  const int nch = verify_chunks(rows, V);
+  const int L = chunk_len(V, nch);
+  RejPart* part = reinterpret_cast<RejPart*>(static_cast<char*>(ws) + kWsHeader);
+  uint2 key = make_uint2((uint32_t)(seed & 0xffffffffull), (uint32_t)(seed >> 32));
+  uint32_t w0 = (uint32_t)((2ull * step_offset) & 0xffffffffull);
+  dim3 grid(nch, rows);
+  const bool vec = (V % 4 == 0) && aligned(target_logits, 16);
+  if (vec)
+    rejection_chunks_kernel<true><<<grid, 256, 0, stream>>>(target_logits, K, V, nch, L, draft_tok, temperature,
+                                                            key, w0 + 1u, part);
+  else
+    rejection_chunks_kernel<false><<<grid, 256, 0, stream>>>(target_logits, K, V, nch, L, draft_tok, temperature,
+                                                             key, w0 + 1u, part);
+  rejection_finalize_kernel<<<B, 32, 0, stream>>>(target_logits, K, V, nch, part, draft_tok, temperature, key, w0,
+                                                  out_tok, accept_len, kv_src);
+  return last_launch();
+}

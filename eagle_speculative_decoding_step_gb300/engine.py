@@ -1,0 +1,183 @@
+"""Device-resident draft model and the whole speculative step, on libeaglespec.
+
+``DeviceModel`` uploads a workload's weights and paged K/V cache to the GPU and
+owns the workspaces.  ``ChainStep`` and ``TreeStep`` hold the per-step device
+buffers and issue one speculative step as a fixed sequence of library calls on
+the current stream (no host synchronisation, so a step can be captured into a
+CUDA graph and replayed):
+
+* chain ([NEURON] "Speculative Decoding (EAGLE3) in the vLLM Neuron
+  Framework", "EagleProposer" ``propose()``): fc_fuse, then K x (draft_layer,
+  LM head or low-rank candidate head), then greedy or rejection verification;
+* tree ([EAGLET] draft_top_k / draft_depth / total_draft_tokens): fc_fuse,
+  root pass + LM head top-k + tree_expand, (depth-1) x (frontier pass + LM head
+  top-k + tree_expand), then greedy tree verification with K/V compaction.
+
+Every computation is a library kernel; torch only allocates device memory and
+provides the stream.
+"""
+import numpy as np
+import torch
+
+from . import binding as lib
+from . import synth
+
+
+def to_device(x: np.ndarray, dtype: str, device) -> torch.Tensor:
+    """Upload a float32 array holding values of ``dtype`` ("bf16" or "f32")."""
+    if dtype == "bf16":
+        bits = torch.from_numpy(synth.bf16_bits(x))
+        return bits.view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+
+
+def from_device(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy()
+
+
+class DeviceModel:
+    def __init__(self, w, W: dict, kv: dict, ctx_len: np.ndarray, device="cuda", max_rows=None):
+        self.w = w
+        self.device = device
+        self.desc = lib.make_desc(w)
+        self.tW = {k: to_device(v, w.dtype, device) for k, v in W.items()}
+        self.weights = lib.make_weights(self.tW)
+        self.tkv = {
+            "k": to_device(kv["k"], w.dtype, device),
+            "v": to_device(kv["v"], w.dtype, device),
+            "block_table": torch.from_numpy(kv["block_table"]).to(device),
+            "block_size": kv["block_size"], "max_blocks": kv["max_blocks"], "num_slots": kv["num_slots"],
+        }
+        self.kv = lib.make_kv(self.tkv)
+        self.ctx_len = torch.from_numpy(np.asarray(ctx_len, dtype=np.int32)).to(device)
+        self.max_rows = max_rows or max(w.rows_max, w.B)
+        nb = lib.spec_workspace_bytes(self.desc, self.max_rows, w.max_ctx)
+        self.ws = torch.zeros(nb, dtype=torch.uint8, device=device)
+        self.tdtype = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def hidden(self, rows):
+        return torch.zeros(rows, self.w.H, dtype=self.tdtype, device=self.device)
+
+    def device_error(self):
+        return lib.spec_get_device_error(self.ws)
+
+
+class ChainStep:
+    """Buffers and call sequence of one chain speculative step."""
+
+    def __init__(self, dm: DeviceModel, aux: torch.Tensor, root_tok: torch.Tensor, target: torch.Tensor,
+                 temperature=None, seed=0, step_offset=0):
+        w = dm.w
+        self.dm = dm
+        B, K, V = w.B, w.K, w.V
+        self.B, self.K, self.V = B, K, V
+        dev = dm.device
+        self.aux = aux
+        self.root = root_tok
+        self.target = target
+        self.h0 = dm.hidden(B)
+        self.pre = [dm.hidden(B), dm.hidden(B)]
+        self.hn = dm.hidden(B)
+        self.drafts = torch.zeros(B, K, dtype=torch.int32, device=dev)
+        self.lp = torch.zeros(B, K, dtype=torch.float32, device=dev)
+        self.out = torch.zeros(B, K + 1, dtype=torch.int32, device=dev)
+        self.acc = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.kv_src = torch.zeros(B, K + 1, dtype=torch.int32, device=dev)
+        self.temperature = temperature if temperature is not None else torch.full((B,), w.temperature,
+                                                                                     device=dev)
+        self.seed, self.step_offset = seed, step_offset
+        self.vws = torch.zeros(lib.spec_verify_workspace_bytes(B, K + 1, V), dtype=torch.uint8, device=dev)
+
+    def draft(self):
+        dm, w, B, K = self.dm, self.dm.w, self.B, self.K
+        lib.spec_fc_fuse(dm.desc, dm.weights, self.aux, self.h0, B, dm.ws)
+        hid = self.h0
+        for i in range(K):
+            if i == 0:
+                rows = lib.make_rows(B, B, 1, dm.ctx_len, self.root, step=0)
+            else:
+                rows = lib.make_rows(B, B, 1, dm.ctx_len, self.drafts.data_ptr() + 4 * (i - 1), step=i,
+                                     tok_stride=K)
+            out = self.pre[i % 2]
+            lib.spec_draft_layer(dm.desc, dm.weights, rows, hid, out, self.hn, dm.kv, dm.ws)
+            ids = self.drafts.data_ptr() + 4 * i
+            if w.rank > 0:
+                lib.spec_lowrank_candidates(dm.desc, dm.weights, self.hn, B, 1, ids, ws=dm.ws, out_ld=K)
+            else:
+                lib.spec_lm_head(dm.desc, dm.weights, self.hn, B, 1, ids, self.lp.data_ptr() + 4 * i, ws=dm.ws,
+                                 ids_ld=K)
+            hid = out
+
+    def verify(self):
+        w = self.dm.w
+        if w.verify == "rejection":
+            lib.spec_verify_rejection(self.B, self.K, self.V, self.target, self.drafts, self.temperature, self.seed,
+                                      self.step_offset, self.out, self.acc, self.kv_src, ws=self.vws)
+        else:
+            lib.spec_verify_greedy(self.B, self.K + 1, self.V, self.target, self.drafts, self.out, self.acc,
+                                   self.kv_src, ws=self.vws)
+
+    def run(self):
+        self.draft()
+        self.verify()
+
+
+class TreeStep:
+    """Buffers and call sequence of one tree speculative step."""
+
+    def __init__(self, dm: DeviceModel, aux: torch.Tensor, root_tok: torch.Tensor, target: torch.Tensor = None):
+        w = dm.w
+        self.dm = dm
+        B, k, D, N, V = w.B, w.top_k, w.depth, w.total, w.V
+        self.B, self.k, self.D, self.N, self.V = B, k, D, N, V
+        dev = dm.device
+        self.aux, self.root, self.target = aux, root_tok, target
+        self.h0 = dm.hidden(B)
+        self.pre = [dm.hidden(B * k), dm.hidden(B * k)]
+        self.hn = dm.hidden(B * k)
+        self.ids = torch.zeros(B * k, k, dtype=torch.int32, device=dev)
+        self.lp = torch.zeros(B * k, k, dtype=torch.float32, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.f_tok = torch.zeros(B * k, **i32)
+        self.f_pos = torch.zeros(B * k, **i32)
+        self.f_kv = torch.zeros(B * k, **i32)
+        self.f_mask = torch.zeros(B * k, dtype=torch.int64, device=dev)
+        self.f_src = torch.zeros(B * k, **i32)
+        self.t_tok = torch.zeros(B, N + 1, **i32)
+        self.t_par = torch.zeros(B, N + 1, **i32)
+        self.t_dep = torch.zeros(B, N + 1, **i32)
+        self.t_pos = torch.zeros(B, N + 1, **i32)
+        self.t_score = torch.zeros(B, N + 1, dtype=torch.float32, device=dev)
+        self.t_mask = torch.zeros(B, N + 1, dtype=torch.int64, device=dev)
+        self.io = lib.make_tree_io(self.f_tok, self.f_pos, self.f_kv, self.f_mask, self.f_src, self.t_tok, self.t_par,
+                                   self.t_dep, self.t_pos, self.t_score, self.t_mask)
+        self.state = torch.zeros(lib.spec_tree_state_bytes(B, k, D, N), dtype=torch.uint8, device=dev)
+        self.out = torch.zeros(B, D + 1, **i32)
+        self.acc = torch.zeros(B, **i32)
+        self.kv_src = torch.zeros(B, D + 1, **i32)
+        self.vws = torch.zeros(lib.spec_verify_workspace_bytes(B, N + 1, V), dtype=torch.uint8, device=dev)
+
+    def draft(self):
+        dm, B, k, D, N = self.dm, self.B, self.k, self.D, self.N
+        lib.spec_fc_fuse(dm.desc, dm.weights, self.aux, self.h0, B, dm.ws)
+        rows = lib.make_rows(B, B, 1, dm.ctx_len, self.root, step=0)
+        lib.spec_draft_layer(dm.desc, dm.weights, rows, self.h0, self.pre[0], self.hn, dm.kv, dm.ws)
+        lib.spec_lm_head(dm.desc, dm.weights, self.hn, B, k, self.ids, self.lp, ws=dm.ws)
+        lib.spec_tree_expand(B, k, 1, D, N, dm.ctx_len, self.root, self.ids, self.lp, self.state, self.io)
+        for d in range(2, D + 1):
+            rows = lib.make_rows(B * k, B, k, dm.ctx_len, self.f_tok, pos=self.f_pos, kv_idx=self.f_kv,
+                                 mask=self.f_mask, hid_src=self.f_src)
+            src, dst = self.pre[d % 2], self.pre[(d + 1) % 2]
+            lib.spec_draft_layer(dm.desc, dm.weights, rows, src, dst, self.hn, dm.kv, dm.ws)
+            lib.spec_lm_head(dm.desc, dm.weights, self.hn, B * k, k, self.ids, self.lp, ws=dm.ws)
+            lib.spec_tree_expand(B, k, d, D, N, dm.ctx_len, self.root, self.ids, self.lp, self.state, self.io)
+
+    def verify(self, compact=True):
+        dm = self.dm
+        lib.spec_verify_greedy(self.B, self.N + 1, self.V, self.target, self.t_tok, self.out, self.acc, self.kv_src,
+                               parent=self.t_par, max_depth=self.D, desc=dm.desc if compact else None,
+                               kv=dm.kv if compact else None, ctx_len=dm.ctx_len, ws=self.vws)
+
+    def run(self):
+        self.draft()
+        self.verify()
