@@ -83,6 +83,8 @@ EXPORTS = {
                                    ctypes.POINTER(ModelDesc), ctypes.POINTER(KV), c_vp, c_vp, c_size, c_vp]),
     "spec_verify_rejection": (c_i32, [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_u64, c_u64, c_vp, c_vp, c_vp, c_vp,
                                       c_size, c_vp]),
+    "spec_verify_greedy_static": (c_i32, [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp,
+                                          ctypes.POINTER(ModelDesc), ctypes.POINTER(KV), c_vp, c_vp]),
 }
 
 _LIB = None
@@ -224,3 +226,13 @@ def spec_verify_rejection(B, K, V, target_logits, draft_tok, temperature, seed, 
     _check(_lib().spec_verify_rejection(B, K, V, _p(target_logits), _p(draft_tok), _p(temperature), seed,
                                         step_offset, _p(out_tok), _p(accept_len), _p(kv_src), _p(ws),
                                         ws.numel() * ws.element_size(), _stream()), "spec_verify_rejection")
+
+
+def spec_verify_greedy_static(B, R, V, target_logits, draft_tok, out_tok, accept_len, kv_src=None, parent=None,
+                              max_depth=0, desc=None, kv=None, ctx_len=None):
+    """Greedy verification with the library's fixed scratch array (no workspace)."""
+    _check(_lib().spec_verify_greedy_static(B, R, V, _p(target_logits), _p(draft_tok), _p(parent), max_depth,
+                                            _p(out_tok), _p(accept_len), _p(kv_src),
+                                            ctypes.byref(desc) if desc is not None else None,
+                                            ctypes.byref(kv) if kv is not None else None, _p(ctx_len), _stream()),
+           "spec_verify_greedy_static")

@@ -17,6 +17,8 @@
 // max / sum-exp / Gumbel key for the stochastic sampler); kernel 2 runs one
 // CTA per request over the chunk partials and makes the sequential accept
 // decisions, writes the outputs and moves the accepted K/V.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -340,5 +342,78 @@ extern "C" spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, co
                                                              key, w0 + 1u, part);
   rejection_finalize_kernel<<<B, 32, 0, stream>>>(target_logits, K, V, nch, part, draft_tok, temperature, key, w0,
                                                   out_tok, accept_len, kv_src);
+  return last_launch();
+}
+
+// ---------------------------------------------------------------- no-allocation variant
+// Some callers cannot allocate device memory at all: a host framework that owns
+// every device buffer and hands the verifier only its inputs and outputs, code
+// that runs where cudaMalloc is forbidden because it synchronises the device
+// (latency-critical serving loops), or plugins that see no allocator.  For them
+// spec_verify_greedy_static keeps its scratch in a fixed array in device memory
+// that is part of the loaded library (every GPU that loads the library holds it
+// until the process exits).
+namespace spec {
+constexpr size_t kStaticVerifyScratch = 256 * 1024;     // header + chunk partials
+static __device__ __align__(256) unsigned char g_verify_scratch[kStaticVerifyScratch];
+constexpr int kStaticMaxDevices = 64;
+static void* g_verify_scratch_addr[kStaticMaxDevices];
+static std::mutex g_verify_scratch_mu;
+
+// Device address of the scratch array on the current device (looked up once per
+// device, with that device current).  nullptr if the lookup fails.
+static void* static_verify_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStaticMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_verify_scratch_mu);
+  if (g_verify_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess) return nullptr;
+    g_verify_scratch_addr[dev] = p;
+  }
+  return g_verify_scratch_addr[dev];
+}
+}  // namespace spec
+
+extern "C" spec_status spec_verify_greedy_static(int32_t B, int32_t R, int32_t V, const float* target_logits,
+                                                 const int32_t* draft_tok, const int32_t* parent,
+                                                 int32_t max_depth, int32_t* out_tok, int32_t* accept_len,
+                                                 int32_t* kv_src, const spec_model_desc* desc, const spec_kv* kv,
+                                                 const int32_t* ctx_len, spec_stream_t stream) {
+  if (B <= 0 || R <= 0 || V <= 0) return SPEC_ERR_SHAPE;
+  if (!target_logits || !draft_tok || !out_tok || !accept_len) return SPEC_ERR_ARG;
+  if (R > 64) return SPEC_ERR_CAPACITY;
+  if (parent == nullptr && R < 2) return SPEC_ERR_SHAPE;
+  if (parent != nullptr && (max_depth < 0 || max_depth >= 64)) return SPEC_ERR_SHAPE;
+  // the same scratch layout as the workspace version must fit the fixed array
+  if (spec_verify_workspace_bytes(B, R, V) > kStaticVerifyScratch) return SPEC_ERR_CAPACITY;
+  int has_kv = 0, row_elems = 0, elem_bytes = 4;
+  spec_kv kvv{};
+  if (parent != nullptr && kv != nullptr) {
+    if (!desc || !ctx_len || !kv->k || !kv->v || !kv->block_table) return SPEC_ERR_ARG;
+    if (kv->block_size <= 0 || kv->max_blocks <= 0 || kv->num_slots <= 0) return SPEC_ERR_SHAPE;
+    has_kv = 1;
+    kvv = *kv;
+    row_elems = desc->n_kv_heads * desc->head_dim;
+    elem_bytes = desc->dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  }
+  void* ws = static_verify_scratch();
+  if (ws == nullptr) return SPEC_ERR_CUDA;
+  // the array keeps the previous call's contents: the error header starts at zero;
+  // every chunk partial is rewritten before it is read
+  if (cudaMemsetAsync(ws, 0, kWsHeader, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  const int rows = B * R;
+  const int nch = verify_chunks(rows, V);
+  const int L = chunk_len(V, nch);
+  ArgPart* part = reinterpret_cast<ArgPart*>(static_cast<char*>(ws) + kWsHeader);
+  dim3 grid(nch, rows);
+  const bool vec = (V % 4 == 0) && aligned(target_logits, 16);
+  if (vec)
+    argmax_chunks_kernel<true><<<grid, 256, 0, stream>>>(target_logits, V, nch, L, part);
+  else
+    argmax_chunks_kernel<false><<<grid, 256, 0, stream>>>(target_logits, V, nch, L, part);
+  verify_greedy_finalize_kernel<<<B, 128, 0, stream>>>(R, nch, part, draft_tok, parent, max_depth, out_tok,
+                                                       accept_len, kv_src, kvv, has_kv, row_elems, elem_bytes,
+                                                       ctx_len, ws);
   return last_launch();
 }

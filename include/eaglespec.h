@@ -312,6 +312,28 @@ spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, const float *
                                   int32_t *accept_len, int32_t *kv_src,
                                   void *ws, size_t ws_bytes, spec_stream_t stream);
 
+/* Greedy verification without caller-provided scratch.  The paper has no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory -- a host framework that owns every device buffer and passes only
+ * inputs and outputs, a latency-critical loop where cudaMalloc (which
+ * synchronises the device) is not allowed, or a plugin without access to an
+ * allocator.  Same arguments, results and checks as spec_verify_greedy, minus
+ * ws / ws_bytes.  Its scratch is a fixed 256 KiB array of device memory inside
+ * the library (held on every GPU that loads the library until the process
+ * exits); requests whose scratch (spec_verify_workspace_bytes(B, R, V)) exceeds
+ * it return SPEC_ERR_CAPACITY without launching.  The first call on a device
+ * looks up the array's device address with that device current; make that first
+ * call before any stream capture.  All calls share the one array, so calls that
+ * overlap on the GPU (different streams, no ordering) race; calls ordered on
+ * one stream are safe.  Each call clears the array's error header; device-side
+ * index errors of this variant are not reported back (offending accesses are
+ * skipped as in the workspace version).  It allocates nothing. */
+spec_status spec_verify_greedy_static(int32_t B, int32_t R, int32_t V, const float *target_logits,
+                                      const int32_t *draft_tok, const int32_t *parent,
+                                      int32_t max_depth, int32_t *out_tok, int32_t *accept_len,
+                                      int32_t *kv_src, const spec_model_desc *desc,
+                                      const spec_kv *kv, const int32_t *ctx_len, spec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
