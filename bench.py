@@ -91,18 +91,98 @@ class ClockSampler:
 
 
 def step_bytes(w):
-    """Algorithmic HBM bytes of one chain step (weights once per pass, allowed K/V,
-    target logits once) and the LM head's bytes per launch."""
+    """Algorithmic HBM bytes of one step (every weight read once per draft pass, the
+    allowed context K/V once per pass and request, target logits once) and the
+    dominant kernel's (LM head) bytes per launch."""
     es = 2 if w.dtype == "bf16" else 4
     H, nq, nkv, hd, I, V = w.H, w.nq, w.nkv, w.hd, w.I, w.V
     layer = (2 * H * (nq + 2 * nkv) * hd + nq * hd * H + 3 * H * I) * es
     fc = 3 * H * H * es
-    head = V * H * es
-    kv_per_pass = w.B * (w.max_ctx + w.K) * 2 * nkv * hd * es
-    verify = w.B * (w.K + 1) * V * 4
-    total = fc + w.K * (layer + head + kv_per_pass) + verify
-    lm_launch = head + w.B * H * es
+    head = V * H * es if w.rank == 0 else (H * w.rank + V * w.rank) * es + w.B * w.num_candidates * H * es
+    keys = min(w.max_ctx, w.window) if w.window > 0 else w.max_ctx
+    kv_per_pass = w.B * (keys + w.draft_region) * 2 * nkv * hd * es
+    passes = w.K if w.mode == "chain" else w.depth
+    verify = w.B * w.verify_rows * V * 4
+    total = fc + passes * (layer + head + kv_per_pass) + verify
+    rows = w.B if w.mode == "chain" else w.B * w.top_k
+    lm_launch = V * H * es + rows * H * es
     return total, lm_launch
+
+
+def launches_per_step(w):
+    layer = 11                                   # prologue, 4 GEMMs, 4 epilogues, attention + combine
+    head = 6 if w.rank > 0 else 2                # fused LM head + merge, or the candidate head's 6
+    if w.mode == "chain":
+        return 2 + w.K * (layer + head) + 2
+    return 2 + w.depth * (layer + head + 1) + 2  # + tree expansion per depth
+
+
+def build_chain_step(w, dm, aux_d, root_d, device):
+    """Chain step whose target logits are the draft's own logits over K+1 chained
+    passes plus N(0, sigma) noise (built once, untimed, with the library's
+    full-logits LM head)."""
+    import torch
+    from eagle_speculative_decoding_step_gb300 import binding as lib, engine
+    B, K, V = w.B, w.K, w.V
+    target = torch.empty(B, K + 1, V, dtype=torch.float32, device=device)
+    h0 = dm.hidden(B)
+    pre = [dm.hidden(B), dm.hidden(B)]
+    hn = dm.hidden(B)
+    ids = torch.zeros(B, K + 1, dtype=torch.int32, device=device)
+    lp = torch.zeros(B, K + 1, dtype=torch.float32, device=device)
+    logits = torch.empty(B, V, dtype=torch.float32, device=device)
+    scratch_ids = torch.zeros(B, 1, dtype=torch.int32, device=device)
+    scratch_lp = torch.zeros(B, 1, dtype=torch.float32, device=device)
+    lib.spec_fc_fuse(dm.desc, dm.weights, aux_d, h0, B, dm.ws)
+    hid = h0
+    for i in range(K + 1):
+        tok = root_d if i == 0 else ids.data_ptr() + 4 * (i - 1)
+        rows = lib.make_rows(B, B, 1, dm.ctx_len, tok, step=i, tok_stride=1 if i == 0 else K + 1,
+                             max_ctx=w.max_ctx)
+        lib.spec_draft_layer(dm.desc, dm.weights, rows, hid, pre[i % 2], hn, dm.kv, dm.ws)
+        if w.rank > 0:
+            lib.spec_lowrank_candidates(dm.desc, dm.weights, hn, B, 1, ids.data_ptr() + 4 * i, ws=dm.ws,
+                                        out_ld=K + 1)
+            lib.spec_lm_head(dm.desc, dm.weights, hn, B, 1, scratch_ids, scratch_lp, None, logits, ws=dm.ws)
+        else:
+            lib.spec_lm_head(dm.desc, dm.weights, hn, B, 1, ids.data_ptr() + 4 * i, lp.data_ptr() + 4 * i, None,
+                             logits, ws=dm.ws, ids_ld=K + 1)
+        target[:, i].copy_(logits)
+        hid = pre[i % 2]
+    target.add_(torch.from_numpy(synth.noise(w, (B, K + 1, V))).to(device))
+    torch.cuda.synchronize()
+    temp = torch.full((B,), w.temperature, dtype=torch.float32, device=device)
+    return engine.ChainStep(dm, aux_d, root_d, target, temperature=temp, seed=w.philox_seed)
+
+
+def build_tree_step(w, dm, aux_d, root_d, device):
+    """Tree step whose target logits are one draft pass over the root and all tree
+    nodes (tree mask, root FC feature as every node's hidden input) plus noise."""
+    import torch
+    from eagle_speculative_decoding_step_gb300 import binding as lib, engine
+    B, N, V = w.B, w.total, w.V
+    st = engine.TreeStep(dm, aux_d, root_d, None)
+    st.draft()
+    M = B * (N + 1)
+    big = engine.DeviceModel.__new__(engine.DeviceModel)
+    big.__dict__.update(dm.__dict__)
+    nb = lib.spec_workspace_bytes(dm.desc, M, w.max_ctx)
+    big.ws = torch.zeros(nb, dtype=torch.uint8, device=device)
+    kv_idx = torch.arange(N + 1, dtype=torch.int32, device=device).repeat(B)
+    hid_src = torch.arange(B, dtype=torch.int32, device=device).repeat_interleave(N + 1)
+    rows = lib.make_rows(M, B, N + 1, dm.ctx_len, st.t_tok.reshape(-1), pos=st.t_pos.reshape(-1), kv_idx=kv_idx,
+                         mask=st.t_mask.reshape(-1), hid_src=hid_src, max_ctx=w.max_ctx)
+    pre, hn = big.hidden(M), big.hidden(M)
+    lib.spec_draft_layer(dm.desc, dm.weights, rows, st.h0, pre, hn, dm.kv, big.ws)
+    target = torch.empty(B, N + 1, V, dtype=torch.float32, device=device)
+    for b in range(B):
+        lib.spec_lm_head(dm.desc, dm.weights, hn[b * (N + 1):(b + 1) * (N + 1)], N + 1, 1,
+                         torch.zeros(N + 1, 1, dtype=torch.int32, device=device),
+                         torch.zeros(N + 1, 1, device=device), None, target[b], ws=big.ws)
+    target.add_(torch.from_numpy(synth.noise(w, (B, N + 1, V))).to(device))
+    torch.cuda.synchronize()
+    st.target = target
+    return st
 
 
 def run_gpu(args, w):
@@ -132,39 +212,12 @@ def run_gpu(args, w):
 
     aux_d = engine.to_device(aux, w.dtype, device)
     root_d = torch.from_numpy(root).to(device)
-    # target logits = the draft's own logits over K+1 chained passes + N(0, sigma)
-    # (built once, untimed, with the library's debug full-logits LM head)
-    B, K, V = w.B, w.K, w.V
-    target = torch.empty(B, K + 1, V, dtype=torch.float32, device=device)
-    h0 = dm.hidden(B)
-    pre = [dm.hidden(B), dm.hidden(B)]
-    hn = dm.hidden(B)
-    ids = torch.zeros(B, K + 1, dtype=torch.int32, device=device)
-    lp = torch.zeros(B, K + 1, dtype=torch.float32, device=device)
-    logits = torch.empty(B, V, dtype=torch.float32, device=device)
-    lib.spec_fc_fuse(dm.desc, dm.weights, aux_d, h0, B, dm.ws)
-    hid = h0
-    for i in range(K + 1):
-        tok = root_d if i == 0 else ids.data_ptr() + 4 * (i - 1)
-        rows = lib.make_rows(B, B, 1, dm.ctx_len, tok, step=i, tok_stride=1 if i == 0 else K + 1)
-        lib.spec_draft_layer(dm.desc, dm.weights, rows, hid, pre[i % 2], hn, dm.kv, dm.ws)
-        if w.rank > 0:
-            lib.spec_lowrank_candidates(dm.desc, dm.weights, hn, B, 1, ids.data_ptr() + 4 * i, ws=dm.ws,
-                                        out_ld=K + 1)
-            lib.spec_lm_head(dm.desc, dm.weights, hn, B, 1, torch.zeros(B, 1, dtype=torch.int32, device=device),
-                             torch.zeros(B, 1, device=device), None, logits, ws=dm.ws)
-        else:
-            lib.spec_lm_head(dm.desc, dm.weights, hn, B, 1, ids.data_ptr() + 4 * i, lp.data_ptr() + 4 * i, None,
-                             logits, ws=dm.ws, ids_ld=K + 1)
-        target[:, i].copy_(logits)
-        hid = pre[i % 2]
-    noise = torch.from_numpy(synth.noise(w, (B, K + 1, V))).to(device)
-    target.add_(noise)
-    del noise
-    torch.cuda.synchronize()
-
-    temp = torch.full((B,), w.temperature, dtype=torch.float32, device=device)
-    st = engine.ChainStep(dm, aux_d, root_d, target, temperature=temp, seed=w.philox_seed)
+    B, V = w.B, w.V
+    if w.mode == "tree":
+        st = build_tree_step(w, dm, aux_d, root_d, device)
+    else:
+        st = build_chain_step(w, dm, aux_d, root_d, device)
+    target = st.target
     # warm-up (also builds tensor maps / sets kernel attributes), then capture one step
     for _ in range(max(1, args.warmup)):
         st.run()
@@ -203,18 +256,21 @@ def run_gpu(args, w):
     ms_step = ms / args.steps
     acc = st.acc.cpu().numpy()
     verified = float((acc + 1).sum())
+    proposed = B * (w.K if w.mode == "chain" else w.total)
+    lm_rows = B if w.mode == "chain" else B * w.top_k
+    lm_k = 1 if w.mode == "chain" else w.top_k
 
     # dominant kernel (LM head GEMM with fused top-k / lse epilogue), timed alone
-    lm_ids = torch.zeros(B, 1, dtype=torch.int32, device=device)
-    lm_lp = torch.zeros(B, 1, dtype=torch.float32, device=device)
+    lm_ids = torch.zeros(lm_rows, lm_k, dtype=torch.int32, device=device)
+    lm_lp = torch.zeros(lm_rows, lm_k, dtype=torch.float32, device=device)
     n_lm = 20
     with torch.cuda.stream(stream):
         for _ in range(3):
-            lib.spec_lm_head(dm.desc, dm.weights, st.hn, B, 1, lm_ids, lm_lp, ws=dm.ws)
+            lib.spec_lm_head(dm.desc, dm.weights, st.hn, lm_rows, lm_k, lm_ids, lm_lp, ws=dm.ws)
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
         for _ in range(n_lm):
-            lib.spec_lm_head(dm.desc, dm.weights, st.hn, B, 1, lm_ids, lm_lp, ws=dm.ws)
+            lib.spec_lm_head(dm.desc, dm.weights, st.hn, lm_rows, lm_k, lm_ids, lm_lp, ws=dm.ws)
         a1.record(stream)
     torch.cuda.synchronize()
     lm_ms = a0.elapsed_time(a1) / n_lm
@@ -224,7 +280,7 @@ def run_gpu(args, w):
     aux_h = aux_d.cpu().pin_memory()
     root_h = root_d.cpu().pin_memory()
     tgt_h = target.cpu().pin_memory()
-    out_h = torch.empty(B, K + 1, dtype=torch.int32).pin_memory()
+    out_h = torch.empty(tuple(st.out.shape), dtype=torch.int32).pin_memory()
     acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
     n_e2e = max(3, args.steps // 2)
     with torch.cuda.stream(stream):
@@ -247,16 +303,18 @@ def run_gpu(args, w):
     hbm, tf, kind = _peaks()
     total_bytes, lm_bytes = step_bytes(w)
     lm_gbs = lm_bytes / (lm_ms * 1e-3) / 1e9
-    launches_per_step = 2 + K * 13 + 2
     res = {
         "metric": METRIC, "value": world * 1000.0 / ms_step, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded random-init weights, N(0,1) aux states and context K/V)",
         "config": {"workload": w.name, "H": w.H, "heads": [w.nq, w.nkv], "head_dim": w.hd, "I": w.I, "V": w.V,
-                   "batch": w.B, "ctx": w.ctx, "K": K, "verify": w.verify,
+                   "batch": w.B, "ctx": list(w.ctx_range) if w.ctx_range else w.ctx, "mode": w.mode,
+                   "K": w.K if w.mode == "chain" else None,
+                   "tree": [w.top_k, w.depth, w.total] if w.mode == "tree" else None,
+                   "window": w.window, "rank": w.rank, "verify": w.verify,
                    "l2": "inputs larger than L2 (weights %.2f GB streamed per step)" % (total_bytes / 1e9),
                    "graph": "one CUDA graph per step"},
-        "draft_tokens_per_s": world * B * K * 1000.0 / ms_step,
+        "draft_tokens_per_s": world * proposed * 1000.0 / ms_step,
         "verified_tokens_per_s": world * verified * 1000.0 / ms_step,
         "step_roofline": {"bytes": total_bytes, "t_roof_ms": total_bytes / (hbm * 1e9) * 1e3,
                           "frac": (total_bytes / (hbm * 1e9) * 1e3) / ms_step},
@@ -265,41 +323,63 @@ def run_gpu(args, w):
                      "peak_kind": kind + " (burst copy)", "ms_per_launch": lm_ms},
         "e2e": {"value": world * 1000.0 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clocks,
         "setup_s": gen_s,
     }
     return res, rank
 
 
-def run_cpu_baseline(w, budget_s=20.0):
-    """The oracle (fp64 numpy) on a bounded sample: one draft pass of the whole
-    batch plus verification; steps/s extrapolated to K passes."""
-    import copy
-    from oracle import draft as od, verify as ov
-    import threadpoolctl  # noqa: F401  (optional)
+class OracleSample:
+    """The oracle (fp64 numpy, as it stands) on a bounded sample of the workload:
+    one draft pass (FC fuse + draft layer + LM head) over the whole batch plus one
+    greedy verification; a step is extrapolated as K such passes + the verify.
+    Inputs are generated and converted to float64 once, outside the timing."""
 
-    t0 = time.time()
-    W = synth.make_weights(w)
-    ctx = synth.context_lengths(w)
-    kv = synth.make_kv(w, ctx)
-    aux = synth.make_aux(w)
-    root = synth.root_tokens(w)
-    gen = time.time() - t0
-    t1 = time.time()
-    h0 = od.fc_fuse(w, W, aux)
-    rows = {"M": w.B, "B": w.B, "R": 1, "step": 0, "ctx_len": ctx, "tok": root}
-    pre, hn = od.draft_layer(w, W, rows, h0, kv)
-    ids, lp, lse, logits = od.lm_head(w, W, hn, 1)
-    t_pass = time.time() - t1
-    target = np.repeat(logits[:, None, :], w.K + 1, axis=1).astype(np.float32)
-    t2 = time.time()
-    ov.verify_greedy_chain(target, np.repeat(ids, w.K, axis=1))
-    t_ver = time.time() - t2
-    step_s = w.K * t_pass + t_ver
-    return {"value": 1.0 / step_s, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": "one draft pass (FC + layer + LM head) over the full batch, timed once, x K passes + "
-                      "one greedy verification; generation %.1fs excluded" % gen}
+    def __init__(self, w):
+        from oracle import draft as od, verify as ov
+        self.od, self.ov, self.w = od, ov, w
+        t0 = time.time()
+        W = synth.make_weights(w)
+        if w.rank > 0:
+            W["lr_down"], W["lr_up"] = synth.lowrank_factors(W["lm_head"], w.rank, w.dtype)
+        self.W = {k: np.asarray(v, dtype=np.float64) for k, v in W.items()}
+        del W
+        self.ctx = synth.context_lengths(w)
+        self.kv = synth.make_kv(w, self.ctx)
+        self.aux = synth.make_aux(w)
+        self.root = synth.root_tokens(w)
+        self.setup_s = time.time() - t0
+
+    def step_seconds(self):
+        od, ov, w = self.od, self.ov, self.w
+        t1 = time.time()
+        h0 = od.fc_fuse(w, self.W, self.aux)
+        rows = {"M": w.B, "B": w.B, "R": 1, "step": 0, "ctx_len": self.ctx, "tok": self.root}
+        pre, hn = od.draft_layer(w, self.W, rows, h0, self.kv)
+        if w.rank > 0:
+            _, _, ids = od.lowrank_candidates(w, self.W, hn, w.num_candidates, 1)
+            logits = hn @ self.W["lm_head"].T
+        else:
+            ids, _, _, logits = od.lm_head(w, self.W, hn, 1)
+        t_pass = time.time() - t1
+        target = np.repeat(logits[:, None, :], w.K + 1, axis=1).astype(np.float32)
+        t2 = time.time()
+        ov.verify_greedy_chain(target, np.repeat(ids, w.K, axis=1))
+        t_ver = time.time() - t2
+        return w.K * t_pass + t_ver
+
+    def describe(self):
+        return ("one draft pass (FC fuse + draft layer + LM head) over the full batch of %d, timed, x K=%d, "
+                "plus one greedy verification of [B, K+1, V] logits; fp64 numpy; input generation and "
+                "float64 conversion (%.1fs) excluded" % (self.w.B, self.w.K, self.setup_s))
+
+
+def cpu_baseline(w, samples=1):
+    o = OracleSample(w)
+    ts = [o.step_seconds() for _ in range(samples)]
+    v = 1.0 / statistics.median(ts)
+    return {"value": v, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle", "sample": o.describe()}
 
 
 def main():
@@ -312,31 +392,31 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = configs.WORKLOADS[args.config]
-    if w.mode != "chain":
-        raise SystemExit("bench.py times chain workloads; tree steps are timed by the tests")
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
+        # the reference arm is the CPU oracle (no other implementation of this path exists)
         if rank != 0:
             return
         t0 = time.time()
-        vals = []
-        for _ in range(args.warmup + args.steps if args.steps <= 3 else 3):
-            vals.append(run_cpu_baseline(w)["value"])
-        v = statistics.median(vals)
-        cb = run_cpu_baseline(w) if False else {"kind": "oracle", "cores": os.cpu_count(),
-                                                "sample": "one draft pass over the full batch x K + verify"}
-        cb["value"] = v
+        o = OracleSample(w)
+        for _ in range(args.warmup):
+            o.step_seconds()
+        ts = [o.step_seconds() for _ in range(args.steps)]
+        ms = 1000.0 * statistics.median(ts)
+        v = 1000.0 / ms
         print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": 1,
-                          "steps": len(vals), "warmup": 0, "higher_is_better": True, "scaling": "weak",
-                          "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                          "config": {"workload": w.name}, "cpu_baseline": cb,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": {"workload": w.name},
+                          "cpu_baseline": {"value": v, "unit": "steps/s", "cores": os.cpu_count(),
+                                           "kind": "oracle", "sample": o.describe()},
                           "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                           "wall_s": time.time() - t0}))
         return
     res, rank = run_gpu(args, w)
     if rank == 0:
         if not args.no_cpu_baseline:
-            res["cpu_baseline"] = run_cpu_baseline(w)
+            res["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(res))
 
 

@@ -51,7 +51,7 @@ class KV(ctypes.Structure):
 class Rows(ctypes.Structure):
     _fields_ = [("M", c_i32), ("B", c_i32), ("rows_per_req", c_i32), ("step", c_i32), ("ctx_len", c_vp),
                 ("tok", c_vp), ("tok_stride", c_i32), ("pos", c_vp), ("kv_idx", c_vp), ("mask", c_vp),
-                ("hid_src", c_vp)]
+                ("hid_src", c_vp), ("max_ctx", c_i32)]
 
 
 class TreeIO(ctypes.Structure):
@@ -83,6 +83,7 @@ EXPORTS = {
                                    ctypes.POINTER(ModelDesc), ctypes.POINTER(KV), c_vp, c_vp, c_size, c_vp]),
     "spec_verify_rejection": (c_i32, [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_u64, c_u64, c_vp, c_vp, c_vp, c_vp,
                                       c_size, c_vp]),
+    "spec_decode_metadata": (c_i32, [c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "spec_verify_greedy_static": (c_i32, [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp,
                                           ctypes.POINTER(ModelDesc), ctypes.POINTER(KV), c_vp, c_vp]),
 }
@@ -146,8 +147,10 @@ def make_kv(kv: dict) -> KV:
     return k
 
 
-def make_rows(M, B, R, ctx_len, tok, step=0, tok_stride=1, pos=None, kv_idx=None, mask=None, hid_src=None) -> Rows:
-    r = Rows(M, B, R, step, _p(ctx_len), _p(tok), tok_stride, _p(pos), _p(kv_idx), _p(mask), _p(hid_src))
+def make_rows(M, B, R, ctx_len, tok, step=0, tok_stride=1, pos=None, kv_idx=None, mask=None, hid_src=None,
+              max_ctx=0) -> Rows:
+    r = Rows(M, B, R, step, _p(ctx_len), _p(tok), tok_stride, _p(pos), _p(kv_idx), _p(mask), _p(hid_src),
+             int(max_ctx))
     r._keep = (ctx_len, tok, pos, kv_idx, mask, hid_src)      # the struct holds raw pointers
     return r
 
@@ -236,3 +239,10 @@ def spec_verify_greedy_static(B, R, V, target_logits, draft_tok, out_tok, accept
                                             ctypes.byref(desc) if desc is not None else None,
                                             ctypes.byref(kv) if kv is not None else None, _p(ctx_len), _stream()),
            "spec_verify_greedy_static")
+
+
+def spec_decode_metadata(R, cu_num_scheduled, num_draft, cu_num_draft, logits_indices, target_logits_indices,
+                         bonus_logits_indices, input_ids=None, draft_token_ids=None, ws=None):
+    _check(_lib().spec_decode_metadata(R, _p(cu_num_scheduled), _p(num_draft), _p(input_ids), _p(cu_num_draft),
+                                       _p(logits_indices), _p(target_logits_indices), _p(bonus_logits_indices),
+                                       _p(draft_token_ids), _p(ws), _stream()), "spec_decode_metadata")

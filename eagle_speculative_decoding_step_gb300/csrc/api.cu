@@ -26,7 +26,8 @@ void launch_simt_gemm(int, const void*, const void*, const void*, int, const voi
 spec_status launch_tc_gemm(const void* const*, const int*, int, int, const void*, int, const SKPlan&, float*, void*,
                            cudaStream_t);
 int tc_mpad(int M);
-int attn_splits(int B, int nkv, int nqg, int sms);
+int attn_splits(int B, int nkv, int nqg, int sms, int max_keys);
+int attn_qmax(int rows_per_req, int G);
 spec_status launch_attention(const spec_model_desc&, const spec_rows&, const void*, const spec_kv&, float*, float2*,
                              void*, int, void*, cudaStream_t);
 void launch_row_stats(const float*, int, int, int, int32_t*, int, float*, float*, cudaStream_t);
@@ -36,6 +37,8 @@ void launch_cand_best(const float*, const int32_t*, int, int, int, int32_t*, int
 spec_status launch_lm_head_fused(const spec_model_desc&, const void*, const void*, int, int, int32_t*, int, float*,
                                  float*, void*, size_t, cudaStream_t);
 size_t lm_fused_ws_bytes(int M, int sms);
+spec_status launch_tc_gemm_store(const void* W, int N, int K, const void* X, int M, float* out, int ld, void* ws,
+                                 cudaStream_t st);
 
 int sm_count() {
   static int cached_dev = -1, cached = 0;
@@ -77,6 +80,8 @@ SKPlan make_plan(const int* rows, int nmat, int K, int M, int G) {
     ms = std::max(ms, segs);
   }
   p.maxseg = ms;
+  // device-side plan arithmetic is 32-bit
+  if ((unsigned long long)p.T * (unsigned long long)(p.G + 1) >= (1ull << 32)) p.G = 0;
   return p;
 }
 
@@ -173,6 +178,7 @@ static spec_status gemm(const spec_model_desc& d, std::initializer_list<const vo
   for (int i = 0; i < nmat; ++i)
     if (!W[i]) return SPEC_ERR_ARG;
   SKPlan p = make_plan(rows, nmat, K, M, sm_count());
+  if (p.G <= 0) return SPEC_ERR_SHAPE;
   *plan_out = p;
   if (d.dtype == SPEC_DTYPE_BF16) return launch_tc_gemm(W, rows, nmat, K, X, M, p, part, ws, st);
   launch_simt_gemm(d.dtype, W[0], W[1] ? W[1] : W[0], W[2] ? W[2] : W[0], K, X, M, p, part, st);
@@ -284,8 +290,11 @@ extern "C" spec_status spec_draft_layer(const spec_model_desc* desc, const spec_
     return s;
   launch_epi_qkv(d, part, p, r, cs, qbuf, *kv, ws, stream);
   const int G = nq / nkv;
-  const int nqg = (r.rows_per_req * G + 31) / 32;
-  const int nsplit = attn_splits(r.B, nkv, nqg, sm_count());
+  const int qmax = attn_qmax(r.rows_per_req, G);
+  const int nqg = (r.rows_per_req * G + qmax - 1) / qmax;
+  int max_keys = 0;
+  if (r.max_ctx > 0) max_keys = (d.window > 0 ? std::min(r.max_ctx, d.window) : r.max_ctx) + 64;
+  const int nsplit = attn_splits(r.B, nkv, nqg, sm_count(), max_keys);
   if ((s = launch_attention(d, r, qbuf, *kv, opart, mlpart, attn, nsplit, ws, stream)) != SPEC_OK) return s;
   if ((s = gemm(d, {w->wo}, {H}, nq * hd, attn, M, part, ws, stream, &p)) != SPEC_OK) return s;
   launch_epi_oproj(d, part, p, r, hid_in, *w, r1, nbuf, stream);
@@ -314,9 +323,14 @@ extern "C" spec_status spec_lm_head(const spec_model_desc* desc, const spec_weig
     return launch_lm_head_fused(d, hn, w->lm_head, M, k, topk_ids, ids_ld, topk_logprob, lse, ws, L.lm_part, stream);
   float* part = at<float>(ws, L.part);
   float* logits = logits_or_null ? logits_or_null : at<float>(ws, L.logits);
-  SKPlan p;
-  if ((s = gemm(d, {w->lm_head}, {d.vocab}, d.hidden, hn, M, part, ws, stream, &p)) != SPEC_OK) return s;
-  launch_epi_store(SPEC_DTYPE_F32, part, p, M, d.vocab, logits, d.vocab, stream);
+  if (d.dtype == SPEC_DTYPE_BF16) {
+    if ((s = launch_tc_gemm_store(w->lm_head, d.vocab, d.hidden, hn, M, logits, d.vocab, ws, stream)) != SPEC_OK)
+      return s;
+  } else {
+    SKPlan p;
+    if ((s = gemm(d, {w->lm_head}, {d.vocab}, d.hidden, hn, M, part, ws, stream, &p)) != SPEC_OK) return s;
+    launch_epi_store(SPEC_DTYPE_F32, part, p, M, d.vocab, logits, d.vocab, stream);
+  }
   launch_row_stats(logits, M, d.vocab, k, topk_ids, ids_ld, topk_logprob, lse, stream);
   return last_launch();
 }
@@ -346,8 +360,12 @@ extern "C" spec_status spec_lowrank_candidates(const spec_model_desc* desc, cons
   SKPlan p;
   if ((s = gemm(d, {w->lr_down}, {d.rank}, d.hidden, hn, M, part, ws, stream, &p)) != SPEC_OK) return s;
   launch_epi_store(d.dtype, part, p, M, d.rank, z, d.rank, stream);
-  if ((s = gemm(d, {w->lr_up}, {d.vocab}, d.rank, z, M, part, ws, stream, &p)) != SPEC_OK) return s;
-  launch_epi_store(SPEC_DTYPE_F32, part, p, M, d.vocab, sc, d.vocab, stream);
+  if (d.dtype == SPEC_DTYPE_BF16) {
+    if ((s = launch_tc_gemm_store(w->lr_up, d.vocab, d.rank, z, M, sc, d.vocab, ws, stream)) != SPEC_OK) return s;
+  } else {
+    if ((s = gemm(d, {w->lr_up}, {d.vocab}, d.rank, z, M, part, ws, stream, &p)) != SPEC_OK) return s;
+    launch_epi_store(SPEC_DTYPE_F32, part, p, M, d.vocab, sc, d.vocab, stream);
+  }
   launch_topk_select(sc, M, d.vocab, Kc, cand, stream);
   launch_rescore(d.dtype, hn, w->lm_head, d.hidden, d.vocab, cand, M, Kc, exact, ws, stream);
   launch_cand_best(exact, cand, M, Kc, k_out, out_ids, out_ld, stream);

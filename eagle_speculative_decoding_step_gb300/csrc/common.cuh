@@ -4,6 +4,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/eaglespec.h"
 
 #define SPEC_DEV __device__ __forceinline__
@@ -122,6 +124,32 @@ SPEC_DEV uint4 philox4x32_10(uint4 c, uint2 k) {
 }
 // 32-bit word -> u = ((x >> 8) + 0.5) * 2^-24 in (0, 1), exact in fp32
 SPEC_DEV float word_to_uniform(uint32_t x) { return ((float)(x >> 8) + 0.5f) * 5.9604644775390625e-8f; }
+
+// ---------------------------------------------------------------- dependent launch
+// Kernels of a step are launched with programmatic stream serialisation: a
+// kernel may start while its predecessor finishes; griddepcontrol.wait blocks
+// until the predecessor grid has completed and its writes are visible, so every
+// kernel calls pdl_wait() before touching data another kernel produced or
+// consumes, then pdl_trigger() to let its own successor launch.  Both are no-ops
+// when the kernel was launched without the attribute.
+SPEC_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+SPEC_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- misc
 SPEC_DEV uint64_t globaltimer_ns() {

@@ -15,9 +15,13 @@
 // the attention output, the post-attention-norm output, the MLP activation,
 // hidden_prenorm and the normed output are stored in bf16; the residual stream
 // stays fp32 inside the workspace; all accumulation is fp32.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "plan.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace spec {
 
@@ -46,43 +50,81 @@ RowInfo to_rowinfo(const spec_rows& r) {
                  r.pos, r.kv_idx, r.mask, r.hid_src};
 }
 
+// ---------------------------------------------------------------- cluster helpers
+// Row-wide reductions (RMSNorm over H) run on a thread-block cluster of kCL
+// CTAs per row: each CTA owns H / kCL features, the per-CTA sums meet in
+// distributed shared memory, summed in rank order (deterministic).
+constexpr int kCL = 8;
+
+SPEC_DEV float2 cluster_sum2(float2 v, float* red, float2* slot) {
+  v.x = block_sum(v.x, red);
+  v.y = block_sum(v.y, red);
+  if (threadIdx.x == 0) *slot = v;
+  cg::cluster_group cl = cg::this_cluster();
+  cl.sync();
+  float2 t = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int r = 0; r < kCL; ++r) {
+    const float2 o = *cl.map_shared_rank(slot, r);
+    t.x += o.x;
+    t.y += o.y;
+  }
+  cl.sync();     // no CTA leaves while another still reads its slot
+  return t;
+}
+
+struct RopeFreq {
+  double inv[128];   // theta^(-2i/hd), i < hd/2 (hd <= 256)
+};
+
 // ---------------------------------------------------------------- prologue
 // x[m] = [ input_layernorm(embed[tok_m]) , hidden_norm(hid_in[src_m]) ] and the
-// row's rotary cos/sin table (angle = pos * theta^(-2i/hd), computed in fp64).
+// row's rotary cos/sin table.  The angle pos * theta^(-2i/hd) is formed in fp64,
+// reduced modulo 2*pi in fp64 (Cody-Waite, two-part 2*pi), then sin/cos are
+// taken in fp32 on the reduced argument.
 template <typename T>
-__global__ void __launch_bounds__(256) prologue_kernel(RowInfo ri, int H, int V, int hd, float eps, float theta,
-                                                       const T* __restrict__ embed, const T* __restrict__ g_in,
-                                                       const T* __restrict__ g_hid, const T* __restrict__ hid_in,
-                                                       T* __restrict__ x, float2* __restrict__ cs, void* ws) {
+__global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(256)
+    prologue_kernel(RowInfo ri, int H, int V, int hd, float eps, const __grid_constant__ RopeFreq rf,
+                    const T* __restrict__ embed, const T* __restrict__ g_in, const T* __restrict__ g_hid,
+                    const T* __restrict__ hid_in, T* __restrict__ x, float2* __restrict__ cs, void* ws) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[32];
-  const int m = blockIdx.x;
+  __shared__ float2 slot;
+  const int m = blockIdx.x / kCL, rk = blockIdx.x % kCL;
   int tok = ri.tok[(size_t)m * ri.tok_stride];
   if (tok < 0 || tok >= V) {
-    if (threadIdx.x == 0) report(ws, SPEC_ERR_DEVICE, m, tok);
+    if (threadIdx.x == 0 && rk == 0) report(ws, SPEC_ERR_DEVICE, m, tok);
     tok = 0;
   }
   const T* e = embed + (size_t)tok * H;
   const T* h = hid_in + (size_t)row_src(ri, m) * H;
-  float se = 0.f, sh = 0.f;
-  for (int n = threadIdx.x; n < H; n += blockDim.x) {
-    float a = ld(e + n), c = ld(h + n);
-    se += a * a;
-    sh += c * c;
+  const int n0 = rk * H / kCL, n1 = (rk + 1) * H / kCL;
+  float2 ss = make_float2(0.f, 0.f);
+  for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) {
+    const float a = ld(e + n), c = ld(h + n);
+    ss.x += a * a;
+    ss.y += c * c;
   }
-  se = block_sum(se, red);
-  sh = block_sum(sh, red);
-  const float re = 1.f / sqrtf(se / H + eps), rh = 1.f / sqrtf(sh / H + eps);
+  const float2 tot = cluster_sum2(ss, red, &slot);
+  const float re = 1.f / sqrtf(tot.x / H + eps), rh = 1.f / sqrtf(tot.y / H + eps);
   T* xo = x + (size_t)m * 2 * H;
-  for (int n = threadIdx.x; n < H; n += blockDim.x) {
+  for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) {
     st(xo + n, ld(e + n) * re * ld(g_in + n));
     st(xo + H + n, ld(h + n) * rh * ld(g_hid + n));
   }
-  const int pos = row_pos(ri, m);
-  for (int i = threadIdx.x; i < hd / 2; i += blockDim.x) {
-    double inv = pow((double)theta, -2.0 * (double)i / (double)hd);
-    double s, c;
-    sincos((double)pos * inv, &s, &c);
-    cs[(size_t)m * (hd / 2) + i] = make_float2((float)c, (float)s);
+  if (rk == 0) {
+    const int pos = row_pos(ri, m);
+    const double two_pi_hi = 6.283185307179586, two_pi_lo = 2.4492935982947064e-16;
+    for (int i = threadIdx.x; i < hd / 2; i += blockDim.x) {
+      const double ang = (double)pos * rf.inv[i];
+      const double k = rint(ang * (1.0 / 6.283185307179586));
+      double r = fma(-k, two_pi_hi, ang);
+      r = fma(-k, two_pi_lo, r);
+      float sn, cn;
+      sincosf((float)r, &sn, &cn);
+      cs[(size_t)m * (hd / 2) + i] = make_float2(cn, sn);
+    }
   }
 }
 
@@ -91,6 +133,8 @@ __global__ void __launch_bounds__(256) prologue_kernel(RowInfo ri, int H, int V,
 template <typename TO>
 __global__ void epi_store_kernel(const float* __restrict__ part, SKPlan p, int M, int N, TO* __restrict__ out,
                                  int ld_out) {
+  pdl_wait();
+  pdl_trigger();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)M * N) return;
   const int m = (int)(idx / N), n = (int)(idx % N);
@@ -102,6 +146,8 @@ __global__ void epi_store_kernel(const float* __restrict__ part, SKPlan p, int M
 template <typename T>
 __global__ void epi_qkv_kernel(const float* __restrict__ part, SKPlan p, RowInfo ri, int nq, int nkv, int hd,
                                const float2* __restrict__ cs, T* __restrict__ qbuf, spec_kv kv, void* ws) {
+  pdl_wait();
+  pdl_trigger();
   const int half = hd / 2;
   const int nh = nq + 2 * nkv;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -138,56 +184,46 @@ __global__ void epi_qkv_kernel(const float* __restrict__ part, SKPlan p, RowInfo
   st(base + i + half, x2);
 }
 
-// r1 = hid_in[src] + o ; n = post_attention_layernorm(r1)
-template <typename T>
-__global__ void __launch_bounds__(256) epi_oproj_kernel(const float* __restrict__ part, SKPlan p, RowInfo ri, int H,
-                                                        float eps, const T* __restrict__ hid_in,
-                                                        const T* __restrict__ g_post, float* __restrict__ r1,
-                                                        T* __restrict__ nout) {
+// MODE 0 (after o_proj):  r = hid_in[src] + o;   out_b = post_attention_layernorm(r)
+// MODE 1 (after down):    r = r + down; out_a = r (hidden_prenorm); out_b = final_norm(r)
+// One cluster of kCL CTAs per row.
+template <typename T, int MODE>
+__global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(256)
+    resnorm_kernel(const float* __restrict__ part, SKPlan p, RowInfo ri, int H, float eps,
+                   const T* __restrict__ hid_in, const T* __restrict__ gain, float* __restrict__ r,
+                   T* __restrict__ out_a, T* __restrict__ out_b) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[32];
-  const int m = blockIdx.x;
-  const T* h = hid_in + (size_t)row_src(ri, m) * H;
+  __shared__ float2 slot;
+  const int m = blockIdx.x / kCL, rk = blockIdx.x % kCL;
+  const int n0 = rk * H / kCL, n1 = (rk + 1) * H / kCL;
+  const T* h = (MODE == 0) ? hid_in + (size_t)row_src(ri, m) * H : nullptr;
+  float* rr = r + (size_t)m * H;
   float ss = 0.f;
-  for (int n = threadIdx.x; n < H; n += blockDim.x) {
-    const float v = ld(h + n) + sk_sum(part, p, m, n);
-    r1[(size_t)m * H + n] = v;
+  for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) {
+    const float base = (MODE == 0) ? ld(h + n) : rr[n];
+    const float v = base + sk_sum(part, p, m, n);
+    rr[n] = v;
+    if (MODE == 1) st(out_a + (size_t)m * H + n, v);
     ss += v * v;
   }
-  ss = block_sum(ss, red);
-  const float rs = 1.f / sqrtf(ss / H + eps);
-  for (int n = threadIdx.x; n < H; n += blockDim.x)
-    st(nout + (size_t)m * H + n, r1[(size_t)m * H + n] * rs * ld(g_post + n));
+  const float2 tot = cluster_sum2(make_float2(ss, 0.f), red, &slot);
+  const float rs = 1.f / sqrtf(tot.x / H + eps);
+  for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) st(out_b + (size_t)m * H + n, rr[n] * rs * ld(gain + n));
 }
 
 // act = silu(gate) * up  (gate rows [0, I), up rows [I, 2I) of the stacked output)
 template <typename T>
 __global__ void epi_swiglu_kernel(const float* __restrict__ part, SKPlan p, int M, int I, T* __restrict__ act) {
+  pdl_wait();
+  pdl_trigger();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)M * I) return;
   const int m = (int)(idx / I), i = (int)(idx % I);
   const float g = sk_sum(part, p, m, i);
   const float u = sk_sum(part, p, m, I + i);
   st(act + (size_t)m * I + i, g / (1.f + expf(-g)) * u);
-}
-
-// r2 = r1 + down ; hidden_prenorm = r2 ; hidden_normed = final_norm(r2)
-template <typename T>
-__global__ void __launch_bounds__(256) epi_down_kernel(const float* __restrict__ part, SKPlan p, int H, float eps,
-                                                       float* __restrict__ r1, const T* __restrict__ g_final,
-                                                       T* __restrict__ prenorm, T* __restrict__ normed) {
-  __shared__ float red[32];
-  const int m = blockIdx.x;
-  float ss = 0.f;
-  for (int n = threadIdx.x; n < H; n += blockDim.x) {
-    const float v = r1[(size_t)m * H + n] + sk_sum(part, p, m, n);
-    r1[(size_t)m * H + n] = v;
-    st(prenorm + (size_t)m * H + n, v);
-    ss += v * v;
-  }
-  ss = block_sum(ss, red);
-  const float rs = 1.f / sqrtf(ss / H + eps);
-  for (int n = threadIdx.x; n < H; n += blockDim.x)
-    st(normed + (size_t)m * H + n, r1[(size_t)m * H + n] * rs * ld(g_final + n));
 }
 
 // ---------------------------------------------------------------- SIMT GEMM
@@ -198,6 +234,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const T* __restrict__ A0, const T* __restrict__ A1,
                                                         const T* __restrict__ A2, int K, const T* __restrict__ X,
                                                         int M, SKPlan p, float* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sW[128][65];
   __shared__ float sX[32][65];
   const int c = blockIdx.x;
@@ -245,6 +283,15 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const T* __restrict__ A0
 }
 
 // ---------------------------------------------------------------- attention
+SPEC_DEV void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+SPEC_DEV void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 template <typename T> SPEC_DEV void unpack16(const uint4& r, float* o);
 template <> SPEC_DEV void unpack16<float>(const uint4& r, float* o) {
   o[0] = __uint_as_float(r.x); o[1] = __uint_as_float(r.y); o[2] = __uint_as_float(r.z); o[3] = __uint_as_float(r.w);
@@ -259,32 +306,37 @@ template <> SPEC_DEV void unpack16<__nv_bfloat16>(const uint4& r, float* o) {
 }
 
 // Split-KV decode attention with the row masks of spec_rows.  grid = (nsplit,
-// nkv, B * nqg); a CTA serves up to 32 queries (rows of one request x the q
-// heads of one kv head) over one slice of that request's key range:
-// context keys [klo, ctx) then draft-region keys [ctx, ctx + nd).
-template <typename T, int HD>
+// nkv, B * nqg); a CTA serves up to QMAX queries (rows of one request x the q
+// heads of one kv head) over one slice of that request's key range: context
+// keys [klo, ctx) then draft-region keys [ctx, ctx + nd).  Keys are processed
+// 128 at a time (one per thread for the scores), K and V staged through shared
+// memory with 16-byte copies.
+template <typename T, int HD, int QMAX>
 __global__ void __launch_bounds__(128) attn_split_kernel(const T* __restrict__ qbuf, spec_kv kv, RowInfo ri,
                                                          int nq, int nkv, int window, int nsplit, int nqg,
                                                          float scale, float* __restrict__ opart,
                                                          float2* __restrict__ mlpart, void* ws) {
-  constexpr int TK = 128;                 // keys per tile (one per thread)
-  constexpr int KP = HD + (16 / sizeof(T));   // padded smem row (elements)
+  pdl_wait();
+  pdl_trigger();
+  constexpr int TK = 128;                      // keys per tile (one per thread)
+  constexpr int KP = HD + (16 / sizeof(T));    // padded smem row (elements)
+  constexpr int QW = QMAX / 4;                 // queries per warp in softmax / PV
   extern __shared__ __align__(16) uint8_t attn_smem[];
-  float* sQ = reinterpret_cast<float*>(attn_smem);                       // [32][HD]
-  float* sS = sQ + 32 * HD;                                             // [32][TK]
-  T* sK = reinterpret_cast<T*>(sS + 32 * TK);                           // [TK][KP]
+  float* sQ = reinterpret_cast<float*>(attn_smem);                       // [QMAX][HD]
+  float* sS = sQ + QMAX * HD;                                           // [QMAX][TK]
+  T* sK = reinterpret_cast<T*>(sS + QMAX * TK);                         // [TK][KP]
   T* sV = sK + TK * KP;                                                 // [TK][HD]
-  __shared__ float sM[32], sL[32], sA[32];
-  __shared__ int s_lo[32];
-  __shared__ unsigned long long s_mask[32];
+  __shared__ float sM[QMAX], sL[QMAX], sA[QMAX];
+  __shared__ int s_lo[QMAX];
+  __shared__ unsigned long long s_mask[QMAX];
   __shared__ int s_klo, s_nd;
 
   const int s = blockIdx.x, g = blockIdx.y;
   const int b = blockIdx.z / nqg, qg = blockIdx.z % nqg;
   const int G = nq / nkv;
   const int nQall = ri.R * G;
-  const int q0 = qg * 32;
-  const int nQ = min(32, nQall - q0);
+  const int q0 = qg * QMAX;
+  const int nQ = min(QMAX, nQall - q0);
   const int ctx = ri.ctx_len[b];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -311,11 +363,12 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const T* __restrict__ q
       s_klo = mlo;
       s_nd = om ? 64 - __clzll((long long)om) : 0;
     }
-    sM[tid] = -INFINITY;
-    sL[tid] = 0.f;
+    if (tid < QMAX) {
+      sM[tid] = -INFINITY;
+      sL[tid] = 0.f;
+    }
   }
-  // queries (scaled), fp32
-  for (int e = tid; e < 32 * HD; e += blockDim.x) {
+  for (int e = tid; e < QMAX * HD; e += blockDim.x) {
     const int qi = e / HD, d = e % HD;
     float v = 0.f;
     if (qi < nQ) {
@@ -329,46 +382,47 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const T* __restrict__ q
   const int klo = s_klo, nd = s_nd;
   const int nctx = ctx - klo;
   const int total = nctx + nd;
-  const int chunk = (total + nsplit - 1) / nsplit;
+  const int chunk = ((total + nsplit - 1) / nsplit + TK - 1) / TK * TK;   // whole tiles per split
   const int kbeg = s * chunk, kend = min(total, kbeg + chunk);
 
-  // per-thread output accumulators: warp w -> queries w, w+4, ..; lane -> dims lane + 32*j
   constexpr int DJ = HD / 32;
-  float acc[8][DJ];
+  float acc[QW][DJ];
 #pragma unroll
-  for (int a = 0; a < 8; ++a)
+  for (int a = 0; a < QW; ++a)
 #pragma unroll
     for (int jj = 0; jj < DJ; ++jj) acc[a][jj] = 0.f;
 
   for (int t0 = kbeg; t0 < kend; t0 += TK) {
-    // stage K / V rows of this tile (coalesced 16-byte copies)
+    const int nk = min(TK, kend - t0);
+    // stage K / V rows of this tile: asynchronous 16-byte copies, all in flight
+    // together (a key's row of one kv head is HD contiguous elements)
     constexpr int CH = HD * sizeof(T) / 16;        // 16-byte chunks per row
-    for (int e = tid; e < TK * CH; e += blockDim.x) {
+    for (int e = tid; e < nk * CH; e += blockDim.x) {
       const int kt = e / CH, ch = e % CH;
       const int kidx = t0 + kt;
-      uint4 kvv = make_uint4(0, 0, 0, 0), vvv = make_uint4(0, 0, 0, 0);
-      if (kidx < kend) {
-        const int ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
-        const long long slot = slot_of(kv, b, ci);
-        if (slot >= 0) {
-          const size_t off = ((size_t)slot * nkv + g) * HD;
-          kvv = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(kv.k) + off)[ch];
-          vvv = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(kv.v) + off)[ch];
-        }
+      const int ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
+      const long long slot = slot_of(kv, b, ci);
+      uint4* dk = reinterpret_cast<uint4*>(sK + kt * KP) + ch;
+      uint4* dv = reinterpret_cast<uint4*>(sV + kt * HD) + ch;
+      if (slot >= 0) {
+        const size_t off = ((size_t)slot * nkv + g) * HD;
+        cp_async16(dk, reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(kv.k) + off) + ch);
+        cp_async16(dv, reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(kv.v) + off) + ch);
+      } else {
+        *dk = make_uint4(0, 0, 0, 0);
+        *dv = make_uint4(0, 0, 0, 0);
       }
-      reinterpret_cast<uint4*>(sK + kt * KP)[ch] = kvv;
-      reinterpret_cast<uint4*>(sV + kt * HD)[ch] = vvv;
     }
+    cp_async_wait_all();
     __syncthreads();
     // scores: thread tid owns key tid of the tile
-    {
+    if (tid < nk) {
       const int kidx = t0 + tid;
       const int ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
-      const bool valid = kidx < kend && slot_of(kv, b, ci) >= 0;
-      float sc[32];
+      const bool valid = slot_of(kv, b, ci) >= 0;
+      float sc[QMAX];
 #pragma unroll
-      for (int qi = 0; qi < 32; ++qi) sc[qi] = 0.f;
-      // 16-byte reads of the thread's own K row (padded rows: conflict-free)
+      for (int qi = 0; qi < QMAX; ++qi) sc[qi] = 0.f;
       constexpr int EPV = 16 / sizeof(T);
       const uint4* kr = reinterpret_cast<const uint4*>(sK + tid * KP);
 #pragma unroll 2
@@ -378,11 +432,11 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const T* __restrict__ q
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
 #pragma unroll
-          for (int qi = 0; qi < 32; ++qi) sc[qi] += sQ[qi * HD + d0 + e] * kd[e];
+          for (int qi = 0; qi < QMAX; ++qi) sc[qi] += sQ[qi * HD + d0 + e] * kd[e];
         }
       }
 #pragma unroll
-      for (int qi = 0; qi < 32; ++qi) {
+      for (int qi = 0; qi < QMAX; ++qi) {
         bool ok = valid && qi < nQ;
         if (ok) {
           if (ci < ctx) ok = ci >= s_lo[qi];
@@ -390,10 +444,15 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const T* __restrict__ q
         }
         sS[qi * TK + tid] = ok ? sc[qi] : -INFINITY;
       }
+    } else {
+#pragma unroll
+      for (int qi = 0; qi < QMAX; ++qi) sS[qi * TK + tid] = -INFINITY;
     }
     __syncthreads();
     // online softmax: warp w handles queries w, w+4, ...
-    for (int qi = warp; qi < 32; qi += 4) {
+#pragma unroll
+    for (int a = 0; a < QW; ++a) {
+      const int qi = warp + 4 * a;
       float v[TK / 32];
       float mx = -INFINITY;
 #pragma unroll
@@ -412,29 +471,24 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const T* __restrict__ q
         sum += e;
       }
       sum = warp_sum(sum);
+      const float alpha = (mold == -INFINITY) ? 0.f : expf(mold - mnew);
+      __syncwarp();
       if (lane == 0) {
-        const float alpha = (mold == -INFINITY) ? 0.f : expf(mold - mnew);
         sA[qi] = alpha;
         sL[qi] = sL[qi] * alpha + sum;
         sM[qi] = mnew;
       }
-    }
-    __syncthreads();
-    // P @ V
-#pragma unroll
-    for (int a = 0; a < 8; ++a) {
-      const int qi = warp + 4 * a;
-      const float alpha = sA[qi];
 #pragma unroll
       for (int jj = 0; jj < DJ; ++jj) acc[a][jj] *= alpha;
     }
-    const int nk = min(TK, kend - t0);
+    __syncwarp();
+    // P @ V (each warp reads only the probabilities of its own queries)
     for (int kt = 0; kt < nk; ++kt) {
       float vv[DJ];
 #pragma unroll
       for (int jj = 0; jj < DJ; ++jj) vv[jj] = ld(sV + kt * HD + lane + 32 * jj);
 #pragma unroll
-      for (int a = 0; a < 8; ++a) {
+      for (int a = 0; a < QW; ++a) {
         const float pw = sS[(warp + 4 * a) * TK + kt];
 #pragma unroll
         for (int jj = 0; jj < DJ; ++jj) acc[a][jj] += pw * vv[jj];
@@ -444,7 +498,7 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const T* __restrict__ q
   }
   // write this split's partials
 #pragma unroll
-  for (int a = 0; a < 8; ++a) {
+  for (int a = 0; a < QW; ++a) {
     const int qi = warp + 4 * a;
     if (qi >= nQ) continue;
     const int q = q0 + qi;
@@ -461,6 +515,8 @@ template <typename T, int HD>
 __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restrict__ opart,
                                                           const float2* __restrict__ mlpart, int nq, int nsplit,
                                                           T* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int mh = blockIdx.x;          // m * nq + h
   const int d = threadIdx.x;
   float M = -INFINITY;
@@ -483,6 +539,8 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restric
 __global__ void __launch_bounds__(256) row_stats_kernel(const float* __restrict__ logits, int V, int k,
                                                         int32_t* __restrict__ ids, int ld_ids, float* __restrict__ lp,
                                                         float* __restrict__ lse_out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[32];
   __shared__ int redi[32];
   __shared__ int chosen[8];
@@ -525,6 +583,8 @@ SPEC_DEV uint32_t order_key(float f) {
 // of the ties, bitonic sort of the selected.  One CTA of 1024 threads per row.
 __global__ void __launch_bounds__(1024) topk_select_kernel(const float* __restrict__ s, int V, int Kc,
                                                            int32_t* __restrict__ out_ids) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int hist[256];
   __shared__ uint32_t s_prefix;
   __shared__ int s_need;
@@ -631,6 +691,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) rescore_kernel(const T* __restrict__ hn, const T* __restrict__ lm_head,
                                                       int H, int V, const int32_t* __restrict__ cand, int Kc,
                                                       float* __restrict__ exact, void* ws) {
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.y;
   const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -652,6 +714,8 @@ __global__ void __launch_bounds__(256) rescore_kernel(const T* __restrict__ hn, 
 __global__ void __launch_bounds__(128) cand_best_kernel(const float* __restrict__ exact,
                                                         const int32_t* __restrict__ cand, int Kc, int k_out,
                                                         int32_t* __restrict__ out, int ld_out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[32];
   __shared__ int redi[32];
   __shared__ int chosen[8];
@@ -692,8 +756,11 @@ static inline unsigned blocks_for(long long n, int bs) { return (unsigned)((n + 
 void launch_prologue(const spec_model_desc& d, const spec_rows& rows, const spec_weights& w, const void* hid_in,
                      void* x, float2* cs, void* ws, cudaStream_t st) {
   RowInfo ri = to_rowinfo(rows);
-  DISPATCH_T(d.dtype, prologue_kernel<T><<<rows.M, 256, 0, st>>>(
-                          ri, d.hidden, d.vocab, d.head_dim, d.rms_eps, d.rope_theta,
+  RopeFreq rf;
+  for (int i = 0; i < d.head_dim / 2 && i < 128; ++i)
+    rf.inv[i] = pow((double)d.rope_theta, -2.0 * (double)i / (double)d.head_dim);
+  DISPATCH_T(d.dtype, launch_pdl(prologue_kernel<T>, dim3(rows.M * kCL), dim3(256), 0, st, 
+                          ri, d.hidden, d.vocab, d.head_dim, d.rms_eps, rf,
                           (const T*)w.embed, (const T*)w.in_norm, (const T*)w.hidden_norm, (const T*)hid_in,
                           (T*)x, cs, ws));
 }
@@ -702,114 +769,155 @@ void launch_epi_store(int dtype_out, const float* part, const SKPlan& p, int M, 
                       cudaStream_t st) {
   const long long n = (long long)M * N;
   if (dtype_out == SPEC_DTYPE_BF16)
-    epi_store_kernel<__nv_bfloat16><<<blocks_for(n, 256), 256, 0, st>>>(part, p, M, N, (__nv_bfloat16*)out, ld_out);
+    launch_pdl(epi_store_kernel<__nv_bfloat16>, dim3(blocks_for(n, 256)), dim3(256), 0, st, part, p, M, N, (__nv_bfloat16*)out, ld_out);
   else
-    epi_store_kernel<float><<<blocks_for(n, 256), 256, 0, st>>>(part, p, M, N, (float*)out, ld_out);
+    launch_pdl(epi_store_kernel<float>, dim3(blocks_for(n, 256)), dim3(256), 0, st, part, p, M, N, (float*)out, ld_out);
 }
 
 void launch_epi_qkv(const spec_model_desc& d, const float* part, const SKPlan& p, const spec_rows& rows,
                     const float2* cs, void* qbuf, const spec_kv& kv, void* ws, cudaStream_t st) {
   RowInfo ri = to_rowinfo(rows);
   const long long n = (long long)rows.M * (d.n_q_heads + 2 * d.n_kv_heads) * (d.head_dim / 2);
-  DISPATCH_T(d.dtype, epi_qkv_kernel<T><<<blocks_for(n, 256), 256, 0, st>>>(
+  DISPATCH_T(d.dtype, launch_pdl(epi_qkv_kernel<T>, dim3(blocks_for(n, 256)), dim3(256), 0, st, 
                           part, p, ri, d.n_q_heads, d.n_kv_heads, d.head_dim, cs, (T*)qbuf, kv, ws));
 }
 
 void launch_epi_oproj(const spec_model_desc& d, const float* part, const SKPlan& p, const spec_rows& rows,
                       const void* hid_in, const spec_weights& w, float* r1, void* nout, cudaStream_t st) {
   RowInfo ri = to_rowinfo(rows);
-  DISPATCH_T(d.dtype, epi_oproj_kernel<T><<<rows.M, 256, 0, st>>>(part, p, ri, d.hidden, d.rms_eps, (const T*)hid_in,
-                                                                   (const T*)w.post_norm, r1, (T*)nout));
+  DISPATCH_T(d.dtype, (launch_pdl(resnorm_kernel<T, 0>, dim3(rows.M * kCL), dim3(256), 0, st, 
+                          part, p, ri, d.hidden, d.rms_eps, (const T*)hid_in, (const T*)w.post_norm, r1, nullptr,
+                          (T*)nout)));
 }
 
 void launch_epi_swiglu(const spec_model_desc& d, const float* part, const SKPlan& p, int M, void* act,
                        cudaStream_t st) {
   const long long n = (long long)M * d.intermediate;
   DISPATCH_T(d.dtype,
-             epi_swiglu_kernel<T><<<blocks_for(n, 256), 256, 0, st>>>(part, p, M, d.intermediate, (T*)act));
+             launch_pdl(epi_swiglu_kernel<T>, dim3(blocks_for(n, 256)), dim3(256), 0, st, part, p, M, d.intermediate, (T*)act));
 }
 
 void launch_epi_down(const spec_model_desc& d, const float* part, const SKPlan& p, int M, float* r1,
                      const spec_weights& w, void* prenorm, void* normed, cudaStream_t st) {
-  DISPATCH_T(d.dtype, epi_down_kernel<T><<<M, 256, 0, st>>>(part, p, d.hidden, d.rms_eps, r1,
-                                                             (const T*)w.final_norm, (T*)prenorm, (T*)normed));
+  RowInfo ri{};
+  DISPATCH_T(d.dtype, (launch_pdl(resnorm_kernel<T, 1>, dim3(M * kCL), dim3(256), 0, st, part, p, ri, d.hidden, d.rms_eps, nullptr,
+                                                                     (const T*)w.final_norm, r1, (T*)prenorm,
+                                                                     (T*)normed)));
 }
 
 void launch_simt_gemm(int dtype, const void* A0, const void* A1, const void* A2, int K, const void* X, int M,
                       const SKPlan& p, float* part, cudaStream_t st) {
-  DISPATCH_T(dtype, simt_gemm_kernel<T><<<p.G, 256, 0, st>>>((const T*)A0, (const T*)A1, (const T*)A2, K,
+  DISPATCH_T(dtype, launch_pdl(simt_gemm_kernel<T>, dim3(p.G), dim3(256), 0, st, (const T*)A0, (const T*)A1, (const T*)A2, K,
                                                               (const T*)X, M, p, part));
 }
 
-int attn_splits(int B, int nkv, int nqg, int sms) {
+int attn_qmax(int rows_per_req, int G) {
+  const int n = rows_per_req * G;
+  if (n <= 4) return 4;
+  if (n <= 8) return 8;
+  if (n <= 16) return 16;
+  return 32;
+}
+
+// Splits per (request, kv head, query group): enough CTAs for ~2 per SM, but no
+// split shorter than one 128-key tile when an upper bound of the context is known.
+int attn_splits(int B, int nkv, int nqg, int sms, int max_keys) {
   const int ctas = B * nkv * nqg;
   int s = (2 * sms + ctas - 1) / ctas;
+  if (max_keys > 0) {
+    const int by_len = (max_keys + 127) / 128;
+    if (s > by_len) s = by_len;
+  }
   if (s < 1) s = 1;
   if (s > 64) s = 64;
   return s;
 }
 
-size_t attn_smem_bytes(int dtype, int hd) {
+size_t attn_smem_bytes(int dtype, int hd, int qmax) {
   const size_t es = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
   const size_t kp = hd + 16 / es;
-  return 32 * hd * 4 + 32 * 128 * 4 + 128 * kp * es + 128 * hd * es;
+  return (size_t)qmax * hd * 4 + (size_t)qmax * 128 * 4 + 128 * kp * es + 128 * hd * es;
+}
+
+template <typename TT, int HDV, int QM>
+static spec_status attn_launch(const spec_model_desc& d, const RowInfo& ri, const spec_rows& rows, const void* qbuf,
+                               const spec_kv& kv, float* opart, float2* mlpart, void* attn_out, int nsplit, int nqg,
+                               void* ws, cudaStream_t st) {
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const size_t smem = attn_smem_bytes(d.dtype, HDV, QM);
+  if (attr_dev != dev) {
+    if (cudaFuncSetAttribute(attn_split_kernel<TT, HDV, QM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    attr_dev = dev;
+  }
+  dim3 grid(nsplit, d.n_kv_heads, rows.B * nqg);
+  const float scale = 1.f / sqrtf((float)d.head_dim);
+  launch_pdl(attn_split_kernel<TT, HDV, QM>, dim3(grid), dim3(128), smem, st, (const TT*)qbuf, kv, ri, d.n_q_heads, d.n_kv_heads,
+                                                          d.window, nsplit, nqg, scale, opart, mlpart, ws);
+  launch_pdl(attn_combine_kernel<TT, HDV>, dim3(rows.M * d.n_q_heads), dim3(HDV), 0, st, opart, mlpart, d.n_q_heads, nsplit,
+                                                                     (TT*)attn_out);
+  return SPEC_OK;
+}
+
+template <typename TT, int HDV>
+static spec_status attn_qdispatch(int qmax, const spec_model_desc& d, const RowInfo& ri, const spec_rows& rows,
+                                  const void* qbuf, const spec_kv& kv, float* opart, float2* mlpart, void* out,
+                                  int nsplit, int nqg, void* ws, cudaStream_t st) {
+  switch (qmax) {
+    case 4: return attn_launch<TT, HDV, 4>(d, ri, rows, qbuf, kv, opart, mlpart, out, nsplit, nqg, ws, st);
+    case 8: return attn_launch<TT, HDV, 8>(d, ri, rows, qbuf, kv, opart, mlpart, out, nsplit, nqg, ws, st);
+    case 16: return attn_launch<TT, HDV, 16>(d, ri, rows, qbuf, kv, opart, mlpart, out, nsplit, nqg, ws, st);
+    default: return attn_launch<TT, HDV, 32>(d, ri, rows, qbuf, kv, opart, mlpart, out, nsplit, nqg, ws, st);
+  }
 }
 
 spec_status launch_attention(const spec_model_desc& d, const spec_rows& rows, const void* qbuf, const spec_kv& kv,
                              float* opart, float2* mlpart, void* attn_out, int nsplit, void* ws, cudaStream_t st) {
   RowInfo ri = to_rowinfo(rows);
   const int G = d.n_q_heads / d.n_kv_heads;
-  const int nqg = (rows.rows_per_req * G + 31) / 32;
-  dim3 grid(nsplit, d.n_kv_heads, rows.B * nqg);
-  const float scale = 1.f / sqrtf((float)d.head_dim);
-  const size_t smem = attn_smem_bytes(d.dtype, d.head_dim);
-  static bool attr_set[4] = {false, false, false, false};
-  cudaError_t e = cudaSuccess;
-#define ATTN_CASE(TT, HDV, IDX)                                                                                   \
-  {                                                                                                               \
-    if (!attr_set[IDX]) {                                                                                         \
-      e = cudaFuncSetAttribute(attn_split_kernel<TT, HDV>, cudaFuncAttributeMaxDynamicSharedMemorySize,           \
-                               (int)smem);                                                                        \
-      if (e != cudaSuccess) return SPEC_ERR_CUDA;                                                                 \
-      attr_set[IDX] = true;                                                                                       \
-    }                                                                                                             \
-    attn_split_kernel<TT, HDV><<<grid, 128, smem, st>>>((const TT*)qbuf, kv, ri, d.n_q_heads, d.n_kv_heads,      \
-                                                         d.window, nsplit, nqg, scale, opart, mlpart, ws);        \
-    attn_combine_kernel<TT, HDV><<<rows.M * d.n_q_heads, HDV, 0, st>>>(opart, mlpart, d.n_q_heads, nsplit,       \
-                                                                        (TT*)attn_out);                           \
-  }
+  const int qmax = attn_qmax(rows.rows_per_req, G);
+  const int nqg = (rows.rows_per_req * G + qmax - 1) / qmax;
+  spec_status s;
   if (d.dtype == SPEC_DTYPE_BF16) {
-    if (d.head_dim == 128) ATTN_CASE(__nv_bfloat16, 128, 0)
-    else if (d.head_dim == 64) ATTN_CASE(__nv_bfloat16, 64, 1)
-    else return SPEC_ERR_UNSUPPORTED;
+    if (d.head_dim == 128)
+      s = attn_qdispatch<__nv_bfloat16, 128>(qmax, d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st);
+    else if (d.head_dim == 64)
+      s = attn_qdispatch<__nv_bfloat16, 64>(qmax, d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st);
+    else
+      return SPEC_ERR_UNSUPPORTED;
   } else {
-    if (d.head_dim == 128) ATTN_CASE(float, 128, 2)
-    else if (d.head_dim == 64) ATTN_CASE(float, 64, 3)
-    else return SPEC_ERR_UNSUPPORTED;
+    if (d.head_dim == 128)
+      s = attn_qdispatch<float, 128>(qmax, d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st);
+    else if (d.head_dim == 64)
+      s = attn_qdispatch<float, 64>(qmax, d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st);
+    else
+      return SPEC_ERR_UNSUPPORTED;
   }
-#undef ATTN_CASE
-  return SPEC_OK;
+  return s;
 }
 
 void launch_row_stats(const float* logits, int M, int V, int k, int32_t* ids, int ld_ids, float* lp, float* lse,
                       cudaStream_t st) {
-  row_stats_kernel<<<M, 256, 0, st>>>(logits, V, k, ids, ld_ids, lp, lse);
+  launch_pdl(row_stats_kernel, dim3(M), dim3(256), 0, st, logits, V, k, ids, ld_ids, lp, lse);
 }
 
 void launch_topk_select(const float* s, int M, int V, int Kc, int32_t* out_ids, cudaStream_t st) {
-  topk_select_kernel<<<M, 1024, 0, st>>>(s, V, Kc, out_ids);
+  launch_pdl(topk_select_kernel, dim3(M), dim3(1024), 0, st, s, V, Kc, out_ids);
 }
 
 void launch_rescore(int dtype, const void* hn, const void* lm_head, int H, int V, const int32_t* cand, int M, int Kc,
                     float* exact, void* ws, cudaStream_t st) {
   dim3 grid((Kc + 7) / 8, M);
-  DISPATCH_T(dtype, rescore_kernel<T><<<grid, 256, 0, st>>>((const T*)hn, (const T*)lm_head, H, V, cand, Kc, exact,
+  DISPATCH_T(dtype, launch_pdl(rescore_kernel<T>, dim3(grid), dim3(256), 0, st, (const T*)hn, (const T*)lm_head, H, V, cand, Kc, exact,
                                                              ws));
 }
 
 void launch_cand_best(const float* exact, const int32_t* cand, int M, int Kc, int k_out, int32_t* out, int ld_out,
                       cudaStream_t st) {
-  cand_best_kernel<<<M, 128, 0, st>>>(exact, cand, Kc, k_out, out, ld_out);
+  launch_pdl(cand_best_kernel, dim3(M), dim3(128), 0, st, exact, cand, Kc, k_out, out, ld_out);
 }
 
 }  // namespace spec

@@ -180,15 +180,18 @@ struct EpiStats {
 
 }  // namespace tc
 
-// Merge the per-CTA records of row m: lse and the k best.
+// Merge the per-CTA records of row m: lse (whole block) and the k best (warp 0:
+// every lane keeps a sorted top-KT of the records it scans, then k rounds of a
+// warp argmax over the lanes' heads).
 template <int KT>
 __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__ part, int G, int mpad, int k,
                                                        int32_t* __restrict__ ids, int ld_ids,
                                                        float* __restrict__ lp, float* __restrict__ lse_out) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int REC = 2 + 2 * KT;
   __shared__ float red[32];
-  __shared__ int redi[32];
-  __shared__ int chosen[8];
+  __shared__ float s_lse;
   const int m = blockIdx.x;
   float mx = -INFINITY;
   for (int c = threadIdx.x; c < G; c += blockDim.x) mx = fmaxf(mx, part[((size_t)c * mpad + m) * REC]);
@@ -200,26 +203,46 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__
   }
   s = block_sum(s, red);
   const float lse = mx + logf(s);
-  for (int rr = 0; rr < k; ++rr) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int e = threadIdx.x; e < G * KT; e += blockDim.x) {
-      const float* r = part + ((size_t)(e / KT) * mpad + m) * REC;
-      const float v = r[2 + e % KT];
-      const int i = __float_as_int(r[2 + KT + e % KT]);
-      bool used = false;
-      for (int q = 0; q < rr; ++q) used |= chosen[q] == i;
-      if (!used && better(v, i, bv, bi)) { bv = v; bi = i; }
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  float tv[KT];
+  int ti[KT];
+#pragma unroll
+  for (int q = 0; q < KT; ++q) { tv[q] = -INFINITY; ti[q] = 0x7fffffff; }
+  for (int e = lane; e < G * KT; e += 32) {
+    const float* r = part + ((size_t)(e / KT) * mpad + m) * REC;
+    const float v = r[2 + e % KT];
+    const int i = __float_as_int(r[2 + KT + e % KT]);
+    if (!better(v, i, tv[KT - 1], ti[KT - 1])) continue;
+#pragma unroll
+    for (int q = KT - 1; q >= 0; --q) {
+      if (better(v, i, tv[q], ti[q])) {
+        if (q > 0 && better(v, i, tv[q - 1], ti[q - 1])) {
+          tv[q] = tv[q - 1];
+          ti[q] = ti[q - 1];
+        } else {
+          tv[q] = v;
+          ti[q] = i;
+        }
+      }
     }
-    block_argmax(bv, bi, red, redi);
-    if (threadIdx.x == 0) {
-      chosen[rr] = bi;
+  }
+  for (int rr = 0; rr < k; ++rr) {
+    float bv = tv[0];
+    int bi = ti[0];
+    warp_argmax(bv, bi);
+    if (ti[0] == bi) {          // the lane whose head won pops it (ids are distinct)
+#pragma unroll
+      for (int q = 0; q < KT - 1; ++q) { tv[q] = tv[q + 1]; ti[q] = ti[q + 1]; }
+      tv[KT - 1] = -INFINITY;
+      ti[KT - 1] = 0x7fffffff;
+    }
+    if (lane == 0) {
       ids[(size_t)m * ld_ids + rr] = bi;
       lp[(size_t)m * ld_ids + rr] = bv - lse;
     }
-    __syncthreads();
   }
-  if (threadIdx.x == 0 && lse_out) lse_out[m] = lse;
+  if (lane == 0 && lse_out) lse_out[m] = lse;
 }
 
 size_t lm_fused_ws_bytes(int /*M*/, int sms) {
@@ -262,7 +285,7 @@ spec_status launch_lm_head_fused(const spec_model_desc& d, const void* hn, const
       default: s = lm_launch<64, 1>(a, b, V, H, M, part, G, ws, st); break;
     }
     if (s != SPEC_OK) return s;
-    lm_merge_kernel<1><<<M, 256, 0, st>>>(part, G, mpad, k, ids, ld_ids, lp, lse);
+    launch_pdl(lm_merge_kernel<1>, dim3(M), dim3(256), 0, st, part, G, mpad, k, ids, ld_ids, lp, lse);
   } else {
     switch (mpad) {
       case 16: s = lm_launch<16, 8>(a, b, V, H, M, part, G, ws, st); break;
@@ -270,7 +293,7 @@ spec_status launch_lm_head_fused(const spec_model_desc& d, const void* hn, const
       default: s = lm_launch<64, 8>(a, b, V, H, M, part, G, ws, st); break;
     }
     if (s != SPEC_OK) return s;
-    lm_merge_kernel<8><<<M, 256, 0, st>>>(part, G, mpad, k, ids, ld_ids, lp, lse);
+    launch_pdl(lm_merge_kernel<8>, dim3(M), dim3(256), 0, st, part, G, mpad, k, ids, ld_ids, lp, lse);
   }
   return last_launch();
 }

@@ -101,3 +101,40 @@ spec_status launch_tc_gemm(const void* const* W, const int* rows, int nmat, int 
 }
 
 }  // namespace spec
+
+namespace spec {
+
+// out[M, N] (fp32, row stride ld) = X[M, K] @ W[N, K]^T with every 128-row tile
+// finished by one CTA (contiguous row ranges per CTA): no partial sums.
+spec_status launch_tc_gemm_store(const void* W, int N, int K, const void* X, int M, float* out, int ld, void* ws,
+                                 cudaStream_t st) {
+  using namespace tc;
+  if (M < 1 || M > 256 || K % 8 != 0) return SPEC_ERR_SHAPE;
+  if (!aligned(W, 16) || !aligned(X, 16)) return SPEC_ERR_ALIGN;
+  const int mpad = tc_mpad(M);
+  int G = sm_count();
+  if (G > (N + 127) / 128) G = (N + 127) / 128;
+  CUtensorMap a[3];
+  if (!make_map(&a[0], W, N, K, 128)) return SPEC_ERR_CUDA;
+  a[1] = a[0];
+  a[2] = a[0];
+  CUtensorMap b;
+  if (!make_map(&b, X, M, K, mpad)) return SPEC_ERR_CUDA;
+  RowsParams rp{N, G, (K + kBK - 1) / kBK};
+  switch (mpad) {
+#define STORE_CASE(MP)                                                                          \
+  case MP: {                                                                                    \
+    typename EpiStore<MP>::Params ep{M, ld, out};                                               \
+    return launch_tc<MP, SchedRows, EpiStore<MP>>(a, b, rp, ep, G, 0, ws, st);                  \
+  }
+    STORE_CASE(16)
+    STORE_CASE(32)
+    STORE_CASE(64)
+    STORE_CASE(128)
+    STORE_CASE(256)
+#undef STORE_CASE
+    default: return SPEC_ERR_SHAPE;
+  }
+}
+
+}  // namespace spec

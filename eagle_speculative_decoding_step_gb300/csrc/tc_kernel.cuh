@@ -99,6 +99,38 @@ struct EpiPartial {
   SPEC_DEV void finish(int, int) {}
 };
 
+// fp32 outputs written straight from TMEM: out[m * ld + n] for the segment's
+// rows [lo, hi) (row-range schedule: every tile is complete within one CTA)
+template <int MPAD>
+struct EpiStore {
+  struct Params {
+    int M;
+    int ld;
+    float* out;
+  };
+  const Params& P;
+  SPEC_DEV EpiStore(const Params& pp, int) : P(pp) {}
+  SPEC_DEV void segment(const Seg& s, uint32_t tb, int warp, int lane) {
+    const int n = s.row0 + warp * 32 + lane;
+    const bool valid = n >= s.lo && n < s.hi;
+#pragma unroll
+    for (int c16 = 0; c16 < MPAD / 16; ++c16) {
+      if (c16 * 16 >= P.M) break;
+      uint32_t r[16];
+      tmem_ld16(tb + (uint32_t)(c16 * 16), r);
+      tmem_ld_wait();
+      if (valid) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int m = c16 * 16 + q;
+          if (m < P.M) P.out[(size_t)m * P.ld + n] = __uint_as_float(r[q]);
+        }
+      }
+    }
+  }
+  SPEC_DEV void finish(int, int) {}
+};
+
 // ---------------------------------------------------------------- kernel
 template <int MPAD, class Sched, class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -146,16 +178,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ---------------- TMA producer
       const uint64_t pw = policy_evict_first(), px = policy_evict_last();
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tA0)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tB)) : "memory");
       int stage = 0;
       uint32_t phase = 0;
       int pending[16];
       for (int s = 0; s < S; ++s) pending[s] = -1;
       Sched sch(sp, c);
       Seg sg;
-      bool ok = true;
-      while (ok && sch.next(sg)) {
+      bool have = sch.next(sg);
+      int kk = have ? sg.k0 : 0;
+      // Weights do not depend on the previous kernel: fill the ring with weight
+      // tiles before waiting for it, then add the activation tiles.
+      int primed = 0;
+      int pk[16];
+      while (have && primed < S) {
         const CUtensorMap* ta = sg.mat == 0 ? &tA0 : (sg.mat == 1 ? &tA1 : &tA2);
-        for (int kk = sg.k0; kk < sg.k1; ++kk) {
+        const uint32_t sa = su32(smem + (size_t)primed * C::kStage);
+        const uint32_t fb = full0 + 8 * primed;
+        mbar_expect_tx(fb, C::kStage);
+        tma_load_2d(sa, ta, fb, kk * kBK, sg.row0, pw);
+        pending[primed] = 0;
+        pk[primed] = kk;
+        ++primed;
+        if (++kk >= sg.k1) {
+          have = sch.next(sg);
+          if (have) kk = sg.k0;
+        }
+      }
+      pdl_wait();
+      pdl_trigger();
+      for (int i = 0; i < primed; ++i)
+        tma_load_2d(su32(smem + (size_t)i * C::kStage) + kABytes, &tB, full0 + 8 * i, pk[i] * kBK, 0, px);
+      stage = primed % S;
+      phase = (primed == S) ? 1u : 0u;
+      bool ok = true;
+      while (ok && have) {
+        const CUtensorMap* ta = sg.mat == 0 ? &tA0 : (sg.mat == 1 ? &tA1 : &tA2);
+        for (; kk < sg.k1; ++kk) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort)) { ok = false; break; }
           const uint32_t sa = su32(smem + (size_t)stage * C::kStage);
           const uint32_t fb = full0 + 8 * stage;
@@ -165,14 +225,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           pending[stage] = (int)phase;
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
+        if (!ok) break;
+        have = sch.next(sg);
+        if (have) kk = sg.k0;
       }
       if (*abort) {
         // let copies in flight land before the CTA exits
         for (int s = 0; s < S; ++s)
           if (pending[s] >= 0) mbar_wait(full0 + 8 * s, (uint32_t)pending[s], abort, false);
       }
+    } else {
+      pdl_wait();
+      pdl_trigger();
     }
   } else if (warp == 5) {
+    pdl_wait();
+    pdl_trigger();
     if (lane == 0) {
       // ---------------- MMA issuer
       constexpr uint32_t idesc = idesc_bf16(128, MPAD);
@@ -209,6 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- epilogue warps 0-3: TMEM lanes 32*warp .. 32*warp+31
+    pdl_wait();
+    pdl_trigger();
     Epi epi(ep, c);
     int abuf = 0;
     uint32_t aphase = 0;
@@ -251,7 +321,7 @@ spec_status launch_tc(const CUtensorMap* a, const CUtensorMap& b, const typename
     attr_dev = dev;
   }
   (void)extra_static;
-  kern<<<G, kThreads, C::kSmem, st>>>(a[0], a[1], a[2], b, sp, ep, ws);
+  launch_pdl(kern, dim3(G), dim3(kThreads), C::kSmem, st, a[0], a[1], a[2], b, sp, ep, ws);
   return last_launch();
 }
 

@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(256) tree_expand_kernel(TreeDims td, int d, co
                                                           const int32_t* __restrict__ ids,
                                                           const float* __restrict__ lp, void* state,
                                                           spec_tree_io io) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const int k = td.k, P = td.P;
   TreeView tv = tree_view(static_cast<char*>(state) + (size_t)b * tree_req_bytes(k, P), k, P);
@@ -214,7 +216,7 @@ extern "C" spec_status spec_tree_expand(int32_t B, int32_t top_k, int32_t depth_
       return SPEC_ERR_ARG;
   }
   TreeDims td{top_k, draft_depth, total, P};
-  tree_expand_kernel<<<B, 256, 0, stream>>>(td, depth_idx, ctx_len, root_tok, topk_ids, topk_logprob, tree_state,
+  launch_pdl(tree_expand_kernel, dim3(B), dim3(256), 0, stream, td, depth_idx, ctx_len, root_tok, topk_ids, topk_logprob, tree_state,
                                             *io);
   return last_launch();
 }

@@ -41,6 +41,8 @@ static int chunk_len(int V, int nch) { int L = (V + nch - 1) / nch; return (L + 
 template <bool VEC>
 __global__ void __launch_bounds__(256) argmax_chunks_kernel(const float* __restrict__ logits, int V,
                                                            int nch, int L, ArgPart* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float rv[32];
   __shared__ int ri[32];
   const int row = blockIdx.y, c = blockIdx.x;
@@ -104,6 +106,8 @@ __global__ void __launch_bounds__(128) verify_greedy_finalize_kernel(
     const int32_t* __restrict__ parent, int max_depth, int32_t* __restrict__ out,
     int32_t* __restrict__ acc_out, int32_t* __restrict__ kv_src, spec_kv kv, int has_kv,
     int row_elems, int elem_bytes, const int32_t* __restrict__ ctx_len, void* ws) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int t[64];
   __shared__ int path[65];
   __shared__ int s_a;
@@ -179,6 +183,8 @@ template <bool VEC>
 __global__ void __launch_bounds__(256) rejection_chunks_kernel(
     const float* __restrict__ logits, int K, int V, int nch, int L, const int32_t* __restrict__ draft,
     const float* __restrict__ temperature, uint2 key, uint32_t ctr_w, RejPart* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[32];
   __shared__ int redi[32];
   const int row = blockIdx.y, c = blockIdx.x;
@@ -232,6 +238,8 @@ __global__ void __launch_bounds__(32) rejection_finalize_kernel(
     const float* __restrict__ logits, int K, int V, int nch, const RejPart* __restrict__ part,
     const int32_t* __restrict__ draft, const float* __restrict__ temperature, uint2 key, uint32_t ctr_w0,
     int32_t* __restrict__ out, int32_t* __restrict__ acc_out, int32_t* __restrict__ kv_src) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   if (threadIdx.x != 0) return;
   const float T = temperature[b];
@@ -308,10 +316,10 @@ extern "C" spec_status spec_verify_greedy(int32_t B, int32_t R, int32_t V, const
   dim3 grid(nch, rows);
   const bool vec = (V % 4 == 0) && aligned(target_logits, 16);
   if (vec)
-    argmax_chunks_kernel<true><<<grid, 256, 0, stream>>>(target_logits, V, nch, L, part);
+    launch_pdl(argmax_chunks_kernel<true>, dim3(grid), dim3(256), 0, stream, target_logits, V, nch, L, part);
   else
-    argmax_chunks_kernel<false><<<grid, 256, 0, stream>>>(target_logits, V, nch, L, part);
-  verify_greedy_finalize_kernel<<<B, 128, 0, stream>>>(R, nch, part, draft_tok, parent, max_depth, out_tok,
+    launch_pdl(argmax_chunks_kernel<false>, dim3(grid), dim3(256), 0, stream, target_logits, V, nch, L, part);
+  launch_pdl(verify_greedy_finalize_kernel, dim3(B), dim3(128), 0, stream, R, nch, part, draft_tok, parent, max_depth, out_tok,
                                                        accept_len, kv_src, kvv, has_kv, row_elems, elem_bytes,
                                                        ctx_len, ws);
   return last_launch();
@@ -335,12 +343,12 @@ extern "C" spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, co
   dim3 grid(nch, rows);
   const bool vec = (V % 4 == 0) && aligned(target_logits, 16);
   if (vec)
-    rejection_chunks_kernel<true><<<grid, 256, 0, stream>>>(target_logits, K, V, nch, L, draft_tok, temperature,
+    launch_pdl(rejection_chunks_kernel<true>, dim3(grid), dim3(256), 0, stream, target_logits, K, V, nch, L, draft_tok, temperature,
                                                             key, w0 + 1u, part);
   else
-    rejection_chunks_kernel<false><<<grid, 256, 0, stream>>>(target_logits, K, V, nch, L, draft_tok, temperature,
+    launch_pdl(rejection_chunks_kernel<false>, dim3(grid), dim3(256), 0, stream, target_logits, K, V, nch, L, draft_tok, temperature,
                                                              key, w0 + 1u, part);
-  rejection_finalize_kernel<<<B, 32, 0, stream>>>(target_logits, K, V, nch, part, draft_tok, temperature, key, w0,
+  launch_pdl(rejection_finalize_kernel, dim3(B), dim3(32), 0, stream, target_logits, K, V, nch, part, draft_tok, temperature, key, w0,
                                                   out_tok, accept_len, kv_src);
   return last_launch();
 }
@@ -409,10 +417,10 @@ extern "C" spec_status spec_verify_greedy_static(int32_t B, int32_t R, int32_t V
   dim3 grid(nch, rows);
   const bool vec = (V % 4 == 0) && aligned(target_logits, 16);
   if (vec)
-    argmax_chunks_kernel<true><<<grid, 256, 0, stream>>>(target_logits, V, nch, L, part);
+    launch_pdl(argmax_chunks_kernel<true>, dim3(grid), dim3(256), 0, stream, target_logits, V, nch, L, part);
   else
-    argmax_chunks_kernel<false><<<grid, 256, 0, stream>>>(target_logits, V, nch, L, part);
-  verify_greedy_finalize_kernel<<<B, 128, 0, stream>>>(R, nch, part, draft_tok, parent, max_depth, out_tok,
+    launch_pdl(argmax_chunks_kernel<false>, dim3(grid), dim3(256), 0, stream, target_logits, V, nch, L, part);
+  launch_pdl(verify_greedy_finalize_kernel, dim3(B), dim3(128), 0, stream, R, nch, part, draft_tok, parent, max_depth, out_tok,
                                                        accept_len, kv_src, kvv, has_kv, row_elems, elem_bytes,
                                                        ctx_len, ws);
   return last_launch();

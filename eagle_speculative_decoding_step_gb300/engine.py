@@ -94,10 +94,10 @@ class ChainStep:
         hid = self.h0
         for i in range(K):
             if i == 0:
-                rows = lib.make_rows(B, B, 1, dm.ctx_len, self.root, step=0)
+                rows = lib.make_rows(B, B, 1, dm.ctx_len, self.root, step=0, max_ctx=w.max_ctx)
             else:
                 rows = lib.make_rows(B, B, 1, dm.ctx_len, self.drafts.data_ptr() + 4 * (i - 1), step=i,
-                                     tok_stride=K)
+                                     tok_stride=K, max_ctx=w.max_ctx)
             out = self.pre[i % 2]
             lib.spec_draft_layer(dm.desc, dm.weights, rows, hid, out, self.hn, dm.kv, dm.ws)
             ids = self.drafts.data_ptr() + 4 * i
@@ -160,13 +160,13 @@ class TreeStep:
     def draft(self):
         dm, B, k, D, N = self.dm, self.B, self.k, self.D, self.N
         lib.spec_fc_fuse(dm.desc, dm.weights, self.aux, self.h0, B, dm.ws)
-        rows = lib.make_rows(B, B, 1, dm.ctx_len, self.root, step=0)
+        rows = lib.make_rows(B, B, 1, dm.ctx_len, self.root, step=0, max_ctx=dm.w.max_ctx)
         lib.spec_draft_layer(dm.desc, dm.weights, rows, self.h0, self.pre[0], self.hn, dm.kv, dm.ws)
         lib.spec_lm_head(dm.desc, dm.weights, self.hn, B, k, self.ids, self.lp, ws=dm.ws)
         lib.spec_tree_expand(B, k, 1, D, N, dm.ctx_len, self.root, self.ids, self.lp, self.state, self.io)
         for d in range(2, D + 1):
             rows = lib.make_rows(B * k, B, k, dm.ctx_len, self.f_tok, pos=self.f_pos, kv_idx=self.f_kv,
-                                 mask=self.f_mask, hid_src=self.f_src)
+                                 mask=self.f_mask, hid_src=self.f_src, max_ctx=dm.w.max_ctx)
             src, dst = self.pre[d % 2], self.pre[(d + 1) % 2]
             lib.spec_draft_layer(dm.desc, dm.weights, rows, src, dst, self.hn, dm.kv, dm.ws)
             lib.spec_lm_head(dm.desc, dm.weights, self.hn, B * k, k, self.ids, self.lp, ws=dm.ws)

@@ -141,6 +141,8 @@ typedef struct {
   const int32_t *kv_idx;   /* [M] or NULL; each < 64 */
   const uint64_t *mask;    /* [M] or NULL */
   const int32_t *hid_src;  /* [M] or NULL: row of hid_in feeding row m */
+  int32_t max_ctx;         /* an upper bound of ctx_len[b] over the batch, or 0 if
+                              unknown; only sizes the attention's key splits */
 } spec_rows;
 
 /* Outputs of tree expansion (spec_tree_expand).  Frontier arrays hold the next
@@ -311,6 +313,28 @@ spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, const float *
                                   uint64_t seed, uint64_t step_offset, int32_t *out_tok,
                                   int32_t *accept_len, int32_t *kv_src,
                                   void *ws, size_t ws_bytes, spec_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Ragged batches.                                                     */
+
+/* SpecDecodeMetadata index builder.  [NEURON] "SpecDecodeMetadata: Index
+ * Bookkeeping": for R requests with cumulative scheduled-token counts
+ * cu_num_scheduled [R] and draft counts num_draft [R] (each request schedules
+ * its last accepted token followed by its drafts):
+ *   cu_num_draft [R]            cumulative draft counts;
+ *   logits_indices [S + R]      each request's last num_draft+1 scheduled
+ *                               positions (S = total drafts);
+ *   target_logits_indices [S]   entries of logits_indices that verify drafts;
+ *   bonus_logits_indices [R]    the last entry of each request's block;
+ *   draft_token_ids [S] or NULL input_ids at the position after each verified
+ *                               one (input_ids required then).
+ * ws: NULL or a workspace whose error word receives SPEC_ERR_DEVICE when a
+ * request schedules fewer than num_draft+1 tokens or a count is negative. */
+spec_status spec_decode_metadata(int32_t R, const int32_t *cu_num_scheduled, const int32_t *num_draft,
+                                 const int32_t *input_ids, int32_t *cu_num_draft,
+                                 int32_t *logits_indices, int32_t *target_logits_indices,
+                                 int32_t *bonus_logits_indices, int32_t *draft_token_ids, void *ws,
+                                 spec_stream_t stream);
 
 /* Greedy verification without caller-provided scratch.  The paper has no
  * counterpart: this entry point exists for callers that cannot allocate device

@@ -34,10 +34,11 @@ Pins (what each function is checked against, in ``tests/test_oracle_pins.py``):
   q/k give a uniform average of the allowed values) and a torch.nn.functional
   restatement; RoPE: norm preservation and relative-position invariance;
 * LM-head statistics: scipy logsumexp;
-* Philox4x32-10: the published known-answer vectors of the generator's authors.
+* Philox4x32-10: the published known-answer vectors of the generator's authors;
+* SpecDecodeMetadata indices: the worked example printed on the Neuron page.
 
 Parity unpinned: none of the functions above is left without a pin; the
 absolute Philox stream beyond the three known-answer vectors is pinned only by
 those vectors plus uniformity tests.
 """
-from . import numerics, draft, tree, verify, philox, step  # noqa: F401
+from . import numerics, draft, tree, verify, philox, step, metadata  # noqa: F401

@@ -588,3 +588,17 @@ def test_rejection_sampler_greedy_rows_and_reject_excludes_draft():
         a = acc[b]
         if a < K:
             assert out[b, a] != drafts[b, a]
+
+
+# ---------------------------------------------------------------- SpecDecodeMetadata
+def test_spec_decode_metadata_printed_example():
+    """The worked example printed in the Neuron page's SpecDecodeMetadata section."""
+    from oracle import metadata
+    g = json.load(open(os.path.join(GOLDEN, "spec_decode_metadata.json")))
+    got = metadata.spec_decode_metadata(g["cu_num_scheduled_tokens"], g["num_draft_tokens"])
+    for k in ("cu_num_draft_tokens", "logits_indices", "target_logits_indices", "bonus_logits_indices"):
+        assert got[k].tolist() == g[k], k
+    ids = np.arange(1000, 1209)
+    got = metadata.spec_decode_metadata(g["cu_num_scheduled_tokens"], g["num_draft_tokens"], ids)
+    # drafts follow the verified position: request 0 -> input positions 1, 2, 3
+    assert got["draft_token_ids"].tolist() == [1001, 1002, 1003, 1105, 1106, 1208]
