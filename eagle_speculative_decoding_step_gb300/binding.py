@@ -32,11 +32,12 @@ class SpecError(RuntimeError):
 class ModelDesc(ctypes.Structure):
     _fields_ = [("hidden", c_i32), ("n_q_heads", c_i32), ("n_kv_heads", c_i32), ("head_dim", c_i32),
                 ("intermediate", c_i32), ("vocab", c_i32), ("dtype", c_i32), ("rms_eps", ctypes.c_float),
-                ("rope_theta", ctypes.c_float), ("window", c_i32), ("rank", c_i32), ("num_candidates", c_i32)]
+                ("rope_theta", ctypes.c_float), ("window", c_i32), ("rank", c_i32), ("num_candidates", c_i32),
+                ("draft_vocab", c_i32)]
 
 
 _WEIGHT_NAMES = ["fc", "embed", "hidden_norm", "in_norm", "post_norm", "final_norm", "wq", "wk", "wv", "wo",
-                 "wgate", "wup", "wdown", "lm_head", "lr_down", "lr_up"]
+                 "wgate", "wup", "wdown", "lm_head", "lr_down", "lr_up", "d2t"]
 
 
 class Weights(ctypes.Structure):
@@ -84,6 +85,9 @@ EXPORTS = {
     "spec_verify_rejection": (c_i32, [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_u64, c_u64, c_vp, c_vp, c_vp, c_vp,
                                       c_size, c_vp]),
     "spec_decode_metadata": (c_i32, [c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "spec_prefill_inputs": (c_i32, [c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                    c_vp]),
+    "spec_gather_rows": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp]),
     "spec_verify_greedy_static": (c_i32, [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp,
                                           ctypes.POINTER(ModelDesc), ctypes.POINTER(KV), c_vp, c_vp]),
 }
@@ -130,7 +134,7 @@ def _check(st, what):
 def make_desc(w) -> ModelDesc:
     """ModelDesc from a workload (configs.Workload)."""
     return ModelDesc(w.H, w.nq, w.nkv, w.hd, w.I, w.V, DTYPE_BF16 if w.dtype == "bf16" else DTYPE_F32,
-                     w.rms_eps, w.rope_theta, w.window, w.rank, w.num_candidates)
+                     w.rms_eps, w.rope_theta, w.window, w.rank, w.num_candidates, w.draft_vocab)
 
 
 def make_weights(W: dict) -> Weights:
@@ -246,3 +250,16 @@ def spec_decode_metadata(R, cu_num_scheduled, num_draft, cu_num_draft, logits_in
     _check(_lib().spec_decode_metadata(R, _p(cu_num_scheduled), _p(num_draft), _p(input_ids), _p(cu_num_draft),
                                        _p(logits_indices), _p(target_logits_indices), _p(bonus_logits_indices),
                                        _p(draft_token_ids), _p(ws), _stream()), "spec_decode_metadata")
+
+
+def spec_prefill_inputs(B, R, input_ids, next_token, last_idx, ctx_len, tok, pos, kv_idx, mask, last_row,
+                        ctx_next=None, ws=None):
+    _check(_lib().spec_prefill_inputs(B, R, _p(input_ids), _p(next_token), _p(last_idx), _p(ctx_len), _p(tok),
+                                      _p(pos), _p(kv_idx), _p(mask), _p(last_row), _p(ctx_next), _p(ws),
+                                      _stream()),
+           "spec_prefill_inputs")
+
+
+def spec_gather_rows(src, n_src, row_bytes, rows, n, dst, ws=None):
+    _check(_lib().spec_gather_rows(_p(src), n_src, row_bytes, _p(rows), n, _p(dst), _p(ws), _stream()),
+           "spec_gather_rows")

@@ -49,6 +49,7 @@ class Workload:
     window: int = 0            # 0 = full causal attention
     rank: int = 0              # 0 = full-vocabulary LM head
     num_candidates: int = 0
+    draft_vocab: int = 0       # reduced draft vocabulary (LM-head rows); 0 = the full vocabulary
     # misc
     rms_eps: float = 1e-6
     rope_theta: float = 10000.0

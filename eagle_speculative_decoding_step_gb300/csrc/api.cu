@@ -27,15 +27,16 @@ spec_status launch_tc_gemm(const void* const*, const int*, int, int, const void*
                            cudaStream_t);
 int tc_mpad(int M);
 int attn_splits(int B, int nkv, int nqg, int sms, int max_keys);
+int attn_splits_max(const spec_model_desc& d, int M, int sms);
 int attn_qmax(int rows_per_req, int G);
 spec_status launch_attention(const spec_model_desc&, const spec_rows&, const void*, const spec_kv&, float*, float2*,
                              void*, int, void*, cudaStream_t);
-void launch_row_stats(const float*, int, int, int, int32_t*, int, float*, float*, cudaStream_t);
+void launch_row_stats(const float*, int, int, int, int32_t*, int, float*, float*, const int32_t*, cudaStream_t);
 void launch_topk_select(const float*, int, int, int, int32_t*, cudaStream_t);
 void launch_rescore(int, const void*, const void*, int, int, const int32_t*, int, int, float*, void*, cudaStream_t);
 void launch_cand_best(const float*, const int32_t*, int, int, int, int32_t*, int, cudaStream_t);
 spec_status launch_lm_head_fused(const spec_model_desc&, const void*, const void*, int, int, int32_t*, int, float*,
-                                 float*, void*, size_t, cudaStream_t);
+                                 float*, const int32_t*, void*, size_t, cudaStream_t);
 size_t lm_fused_ws_bytes(int M, int sms);
 spec_status launch_tc_gemm_store(const void* W, int N, int K, const void* X, int M, float* out, int ld, void* ws,
                                  cudaStream_t st);
@@ -102,9 +103,10 @@ WsLayout ws_layout(const spec_model_desc& d, int M, int /*max_ctx*/, int sms) {
   };
   L.err = 0;
   L.x = take((size_t)M * 2 * H * es);
-  L.attn_splits = 64;
   L.q = take((size_t)M * nq * hd * es + (size_t)M * (hd / 2) * 8);     // q + rotary table
-  L.attn_part = take((size_t)M * nq * 64 * hd * 4 + (size_t)M * nq * 64 * 8);
+  const int smax = attn_splits_max(d, M, sms);
+  L.attn_splits = smax;
+  L.attn_part = take((size_t)M * nq * smax * hd * 4 + (size_t)M * nq * smax * 8);
   L.attn = take((size_t)M * nq * hd * es);
   L.r1 = take((size_t)M * H * 4);
   L.n = take((size_t)M * H * es);
@@ -146,6 +148,7 @@ static spec_status check_desc(const spec_model_desc* d) {
   if (d->rank < 0 || (d->rank > 0 && (d->num_candidates <= 0 || d->num_candidates > 1024 ||
                                       d->num_candidates > d->vocab)))
     return SPEC_ERR_SHAPE;
+  if (d->draft_vocab < 0 || d->draft_vocab > d->vocab || (d->draft_vocab > 0 && d->rank > 0)) return SPEC_ERR_SHAPE;
   if (d->dtype == SPEC_DTYPE_BF16) {
     // TMA rows must be multiples of 16 bytes
     if (d->hidden % 8 || d->intermediate % 8 || (d->n_q_heads * d->head_dim) % 8 || (d->rank > 0 && d->rank % 8))
@@ -162,7 +165,7 @@ static spec_status check_ws(const spec_model_desc& d, int M, void* ws, size_t by
   return SPEC_OK;
 }
 
-static int max_rows_for(const spec_model_desc& d) { return d.dtype == SPEC_DTYPE_BF16 ? 256 : 32; }
+static int max_rows_for(const spec_model_desc& d) { return d.dtype == SPEC_DTYPE_BF16 ? 384 : 32; }
 
 // Partial sums of X[M, K] @ [W...]^T with the model dtype's GEMM.
 static spec_status gemm(const spec_model_desc& d, std::initializer_list<const void*> Wl,
@@ -213,7 +216,12 @@ extern "C" int spec_version(void) { return 1; }
 
 extern "C" size_t spec_workspace_bytes(const spec_model_desc* desc, int32_t max_rows, int32_t max_ctx) {
   if (check_desc(desc) != SPEC_OK || max_rows <= 0) return 0;
-  return ws_layout(*desc, max_rows, max_ctx, sm_count()).total;
+  // the layout of a call depends on its own row count (not monotonically):
+  // size for the largest over every row count up to max_rows
+  size_t best = 0;
+  const int sms = sm_count();
+  for (int m = 1; m <= max_rows; ++m) best = std::max(best, ws_layout(*desc, m, max_ctx, sms).total);
+  return best;
 }
 
 extern "C" spec_status spec_get_device_error(const void* ws, int32_t* code_out, spec_stream_t stream) {
@@ -276,7 +284,7 @@ extern "C" spec_status spec_draft_layer(const spec_model_desc* desc, const spec_
   void* qbuf = at<void>(ws, L.q);
   float2* cs = reinterpret_cast<float2*>(static_cast<char*>(qbuf) + align_up((size_t)M * nq * hd * es, 16));
   float* opart = at<float>(ws, L.attn_part);
-  float2* mlpart = reinterpret_cast<float2*>(opart + (size_t)M * nq * 64 * hd);
+  float2* mlpart = reinterpret_cast<float2*>(opart + (size_t)M * nq * L.attn_splits * hd);
   void* attn = at<void>(ws, L.attn);
   float* r1 = at<float>(ws, L.r1);
   void* nbuf = at<void>(ws, L.n);
@@ -294,7 +302,7 @@ extern "C" spec_status spec_draft_layer(const spec_model_desc* desc, const spec_
   const int nqg = (r.rows_per_req * G + qmax - 1) / qmax;
   int max_keys = 0;
   if (r.max_ctx > 0) max_keys = (d.window > 0 ? std::min(r.max_ctx, d.window) : r.max_ctx) + 64;
-  const int nsplit = attn_splits(r.B, nkv, nqg, sm_count(), max_keys);
+  const int nsplit = std::min(attn_splits(r.B, nkv, nqg, sm_count(), max_keys), L.attn_splits);
   if ((s = launch_attention(d, r, qbuf, *kv, opart, mlpart, attn, nsplit, ws, stream)) != SPEC_OK) return s;
   if ((s = gemm(d, {w->wo}, {H}, nq * hd, attn, M, part, ws, stream, &p)) != SPEC_OK) return s;
   launch_epi_oproj(d, part, p, r, hid_in, *w, r1, nbuf, stream);
@@ -313,25 +321,29 @@ extern "C" spec_status spec_lm_head(const spec_model_desc* desc, const spec_weig
   if (!w || !w->lm_head || !hn || !topk_ids || !topk_logprob) return SPEC_ERR_ARG;
   const spec_model_desc& d = *desc;
   if (M <= 0 || M > max_rows_for(d)) return SPEC_ERR_SHAPE;
-  if (k < 1 || k > 8 || k > d.vocab) return SPEC_ERR_SHAPE;
+  // a reduced draft vocabulary: lm_head has draft_vocab rows, ids map through d2t
+  const int dv = d.draft_vocab > 0 ? d.draft_vocab : d.vocab;
+  const int32_t* d2t = d.draft_vocab > 0 ? w->d2t : nullptr;
+  if (d.draft_vocab > 0 && !d2t) return SPEC_ERR_ARG;
+  if (k < 1 || k > 8 || k > dv) return SPEC_ERR_SHAPE;
   if (ids_ld == 0) ids_ld = k;
   if (ids_ld < k) return SPEC_ERR_SHAPE;
   if (!aligned(hn, 16) || !aligned(w->lm_head, 16)) return SPEC_ERR_ALIGN;
   WsLayout L;
   if ((s = check_ws(d, M, ws, ws_bytes, &L)) != SPEC_OK) return s;
   if (d.dtype == SPEC_DTYPE_BF16 && logits_or_null == nullptr && M <= 64)
-    return launch_lm_head_fused(d, hn, w->lm_head, M, k, topk_ids, ids_ld, topk_logprob, lse, ws, L.lm_part, stream);
+    return launch_lm_head_fused(d, hn, w->lm_head, M, k, topk_ids, ids_ld, topk_logprob, lse, d2t, ws, L.lm_part,
+                                stream);
   float* part = at<float>(ws, L.part);
   float* logits = logits_or_null ? logits_or_null : at<float>(ws, L.logits);
   if (d.dtype == SPEC_DTYPE_BF16) {
-    if ((s = launch_tc_gemm_store(w->lm_head, d.vocab, d.hidden, hn, M, logits, d.vocab, ws, stream)) != SPEC_OK)
-      return s;
+    if ((s = launch_tc_gemm_store(w->lm_head, dv, d.hidden, hn, M, logits, dv, ws, stream)) != SPEC_OK) return s;
   } else {
     SKPlan p;
-    if ((s = gemm(d, {w->lm_head}, {d.vocab}, d.hidden, hn, M, part, ws, stream, &p)) != SPEC_OK) return s;
-    launch_epi_store(SPEC_DTYPE_F32, part, p, M, d.vocab, logits, d.vocab, stream);
+    if ((s = gemm(d, {w->lm_head}, {dv}, d.hidden, hn, M, part, ws, stream, &p)) != SPEC_OK) return s;
+    launch_epi_store(SPEC_DTYPE_F32, part, p, M, dv, logits, dv, stream);
   }
-  launch_row_stats(logits, M, d.vocab, k, topk_ids, ids_ld, topk_logprob, lse, stream);
+  launch_row_stats(logits, M, dv, k, topk_ids, ids_ld, topk_logprob, lse, d2t, stream);
   return last_launch();
 }
 

@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restric
 // From full fp32 logits [M, V]: lse and the k largest (ties to smaller id).
 __global__ void __launch_bounds__(256) row_stats_kernel(const float* __restrict__ logits, int V, int k,
                                                         int32_t* __restrict__ ids, int ld_ids, float* __restrict__ lp,
-                                                        float* __restrict__ lse_out) {
+                                                        float* __restrict__ lse_out, const int32_t* __restrict__ d2t) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[32];
@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(256) row_stats_kernel(const float* __restrict_
     block_argmax(bv, bi, red, redi);
     if (threadIdx.x == 0) {
       chosen[r] = bi;
-      ids[(size_t)m * ld_ids + r] = bi;
+      ids[(size_t)m * ld_ids + r] = d2t ? d2t[bi] : bi;
       lp[(size_t)m * ld_ids + r] = bv - lse;
     }
     __syncthreads();
@@ -833,6 +833,17 @@ int attn_splits(int B, int nkv, int nqg, int sms, int max_keys) {
   return s;
 }
 
+// Upper bound of the split count for any call with M rows: every CTA serves at
+// most 32 query slots, so a pass has at least nkv * ceil(M * G / 32) CTAs.
+int attn_splits_max(const spec_model_desc& d, int M, int sms) {
+  const int G = d.n_q_heads / d.n_kv_heads;
+  const int min_ctas = d.n_kv_heads * ((M * G + 31) / 32);
+  int s = (2 * sms + min_ctas - 1) / min_ctas;
+  if (s < 1) s = 1;
+  if (s > 64) s = 64;
+  return s;
+}
+
 size_t attn_smem_bytes(int dtype, int hd, int qmax) {
   const size_t es = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
   const size_t kp = hd + 16 / es;
@@ -900,8 +911,8 @@ spec_status launch_attention(const spec_model_desc& d, const spec_rows& rows, co
 }
 
 void launch_row_stats(const float* logits, int M, int V, int k, int32_t* ids, int ld_ids, float* lp, float* lse,
-                      cudaStream_t st) {
-  launch_pdl(row_stats_kernel, dim3(M), dim3(256), 0, st, logits, V, k, ids, ld_ids, lp, lse);
+                      const int32_t* d2t, cudaStream_t st) {
+  launch_pdl(row_stats_kernel, dim3(M), dim3(256), 0, st, logits, V, k, ids, ld_ids, lp, lse, d2t);
 }
 
 void launch_topk_select(const float* s, int M, int V, int Kc, int32_t* out_ids, cudaStream_t st) {

@@ -186,7 +186,8 @@ struct EpiStats {
 template <int KT>
 __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__ part, int G, int mpad, int k,
                                                        int32_t* __restrict__ ids, int ld_ids,
-                                                       float* __restrict__ lp, float* __restrict__ lse_out) {
+                                                       float* __restrict__ lp, float* __restrict__ lse_out,
+                                                       const int32_t* __restrict__ d2t) {
   pdl_wait();
   pdl_trigger();
   constexpr int REC = 2 + 2 * KT;
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__
       ti[KT - 1] = 0x7fffffff;
     }
     if (lane == 0) {
-      ids[(size_t)m * ld_ids + rr] = bi;
+      ids[(size_t)m * ld_ids + rr] = d2t ? d2t[bi] : bi;
       lp[(size_t)m * ld_ids + rr] = bv - lse;
     }
   }
@@ -261,10 +262,10 @@ static spec_status lm_launch(const CUtensorMap* a, const CUtensorMap& b, int V, 
 }
 
 spec_status launch_lm_head_fused(const spec_model_desc& d, const void* hn, const void* lm_head, int M, int k,
-                                 int32_t* ids, int ld_ids, float* lp, float* lse, void* ws, size_t part_off,
-                                 cudaStream_t st) {
+                                 int32_t* ids, int ld_ids, float* lp, float* lse, const int32_t* d2t, void* ws,
+                                 size_t part_off, cudaStream_t st) {
   using namespace tc;
-  const int V = d.vocab, H = d.hidden;
+  const int V = d.draft_vocab > 0 ? d.draft_vocab : d.vocab, H = d.hidden;
   if (M > kLmMaxMpad) return SPEC_ERR_UNSUPPORTED;
   if (!aligned(hn, 16) || !aligned(lm_head, 16)) return SPEC_ERR_ALIGN;
   const int mpad = tc_mpad(M);
@@ -285,7 +286,7 @@ spec_status launch_lm_head_fused(const spec_model_desc& d, const void* hn, const
       default: s = lm_launch<64, 1>(a, b, V, H, M, part, G, ws, st); break;
     }
     if (s != SPEC_OK) return s;
-    launch_pdl(lm_merge_kernel<1>, dim3(M), dim3(256), 0, st, part, G, mpad, k, ids, ld_ids, lp, lse);
+    launch_pdl(lm_merge_kernel<1>, dim3(M), dim3(256), 0, st, part, G, mpad, k, ids, ld_ids, lp, lse, d2t);
   } else {
     switch (mpad) {
       case 16: s = lm_launch<16, 8>(a, b, V, H, M, part, G, ws, st); break;
@@ -293,7 +294,7 @@ spec_status launch_lm_head_fused(const spec_model_desc& d, const void* hn, const
       default: s = lm_launch<64, 8>(a, b, V, H, M, part, G, ws, st); break;
     }
     if (s != SPEC_OK) return s;
-    launch_pdl(lm_merge_kernel<8>, dim3(M), dim3(256), 0, st, part, G, mpad, k, ids, ld_ids, lp, lse);
+    launch_pdl(lm_merge_kernel<8>, dim3(M), dim3(256), 0, st, part, G, mpad, k, ids, ld_ids, lp, lse, d2t);
   }
   return last_launch();
 }

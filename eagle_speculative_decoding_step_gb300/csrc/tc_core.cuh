@@ -21,10 +21,22 @@ constexpr int kABytes = 128 * kBK * 2;           // A stage: 128 rows x 128 B
 constexpr uint64_t kWaitNs = 2000000000ull;      // bounded waits: 2 s
 
 template <int MPAD> struct Cfg {
+  static_assert(MPAD % 16 == 0 && MPAD <= 384, "activation tile rows");
   static constexpr int kBBytes = MPAD * kBK * 2;
   static constexpr int kStage = kABytes + kBBytes;
-  static constexpr int kStages = (196 * 1024) / kStage > 10 ? 10 : (196 * 1024) / kStage;
-  static constexpr int kCols = (2 * MPAD) < 32 ? 32 : 2 * MPAD;   // two accumulators
+  static constexpr int kBudget = MPAD > 256 ? 212 * 1024 : 196 * 1024;
+  static constexpr int kStages = kBudget / kStage > 10 ? 10 : kBudget / kStage;
+  // two TMEM accumulators (MMA of the next segment overlaps the drain of the
+  // previous one) when they fit in TMEM's 512 columns, else one
+  static constexpr int kBufs = 2 * MPAD <= 512 ? 2 : 1;
+  static constexpr int kCols = kBufs * MPAD <= 32 ? 32 : (kBufs * MPAD <= 64 ? 64 : (kBufs * MPAD <= 128 ? 128 :
+                               (kBufs * MPAD <= 256 ? 256 : 512)));
+  // B (activation) tile: one TMA box of MPAD rows, or 128-row boxes above 256
+  static constexpr int kBBox = MPAD <= 256 ? MPAD : 128;
+  static constexpr int kBLoads = MPAD / kBBox;
+  // MMA N per instruction: MPAD, or 256 + the remainder above 256
+  static constexpr int kN0 = MPAD <= 256 ? MPAD : 256;
+  static constexpr int kN1 = MPAD - kN0;
   static constexpr size_t kSmem = (size_t)kStages * kStage + 1024 + 256;
 };
 

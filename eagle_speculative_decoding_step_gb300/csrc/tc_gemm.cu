@@ -71,14 +71,16 @@ int tc_mpad(int M) {
   if (M <= 32) return 32;
   if (M <= 64) return 64;
   if (M <= 128) return 128;
-  return 256;
+  if (M <= 256) return 256;
+  return 384;
 }
+static int bbox_rows(int mpad) { return mpad <= 256 ? mpad : 128; }
 
 // Partial sums of X[M, K] @ [W0; W1; W2]^T into `part` (plan p), bf16 operands.
 spec_status launch_tc_gemm(const void* const* W, const int* rows, int nmat, int K, const void* X, int M,
                            const SKPlan& p, float* part, void* ws, cudaStream_t st) {
   using namespace tc;
-  if (M < 1 || M > 256 || K % 8 != 0) return SPEC_ERR_SHAPE;
+  if (M < 1 || M > 384 || K % 8 != 0) return SPEC_ERR_SHAPE;
   for (int i = 0; i < nmat; ++i)
     if (!aligned(W[i], 16)) return SPEC_ERR_ALIGN;
   if (!aligned(X, 16)) return SPEC_ERR_ALIGN;
@@ -89,8 +91,9 @@ spec_status launch_tc_gemm(const void* const* W, const int* rows, int nmat, int 
     if (!make_map(&a[i], W[src], rows[src], K, 128)) return SPEC_ERR_CUDA;
   }
   CUtensorMap b;
-  if (!make_map(&b, X, M, K, mpad)) return SPEC_ERR_CUDA;
+  if (!make_map(&b, X, M, K, bbox_rows(mpad))) return SPEC_ERR_CUDA;
   switch (mpad) {
+    case 384: return launch_mpad<384>(a, b, p, M, part, ws, st);
     case 16: return launch_mpad<16>(a, b, p, M, part, ws, st);
     case 32: return launch_mpad<32>(a, b, p, M, part, ws, st);
     case 64: return launch_mpad<64>(a, b, p, M, part, ws, st);
@@ -109,7 +112,7 @@ namespace spec {
 spec_status launch_tc_gemm_store(const void* W, int N, int K, const void* X, int M, float* out, int ld, void* ws,
                                  cudaStream_t st) {
   using namespace tc;
-  if (M < 1 || M > 256 || K % 8 != 0) return SPEC_ERR_SHAPE;
+  if (M < 1 || M > 384 || K % 8 != 0) return SPEC_ERR_SHAPE;
   if (!aligned(W, 16) || !aligned(X, 16)) return SPEC_ERR_ALIGN;
   const int mpad = tc_mpad(M);
   int G = sm_count();
@@ -119,7 +122,7 @@ spec_status launch_tc_gemm_store(const void* W, int N, int K, const void* X, int
   a[1] = a[0];
   a[2] = a[0];
   CUtensorMap b;
-  if (!make_map(&b, X, M, K, mpad)) return SPEC_ERR_CUDA;
+  if (!make_map(&b, X, M, K, bbox_rows(mpad))) return SPEC_ERR_CUDA;
   RowsParams rp{N, G, (K + kBK - 1) / kBK};
   switch (mpad) {
 #define STORE_CASE(MP)                                                                          \
@@ -132,6 +135,7 @@ spec_status launch_tc_gemm_store(const void* W, int N, int K, const void* X, int
     STORE_CASE(64)
     STORE_CASE(128)
     STORE_CASE(256)
+    STORE_CASE(384)
 #undef STORE_CASE
     default: return SPEC_ERR_SHAPE;
   }

@@ -209,7 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       pdl_wait();
       pdl_trigger();
       for (int i = 0; i < primed; ++i)
-        tma_load_2d(su32(smem + (size_t)i * C::kStage) + kABytes, &tB, full0 + 8 * i, pk[i] * kBK, 0, px);
+#pragma unroll
+        for (int j = 0; j < C::kBLoads; ++j)
+          tma_load_2d(su32(smem + (size_t)i * C::kStage) + kABytes + j * C::kBBox * 128, &tB, full0 + 8 * i,
+                      pk[i] * kBK, j * C::kBBox, px);
       stage = primed % S;
       phase = (primed == S) ? 1u : 0u;
       bool ok = true;
@@ -221,7 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = full0 + 8 * stage;
           mbar_expect_tx(fb, C::kStage);
           tma_load_2d(sa, ta, fb, kk * kBK, sg.row0, pw);
-          tma_load_2d(sa + kABytes, &tB, fb, kk * kBK, 0, px);
+#pragma unroll
+          for (int j = 0; j < C::kBLoads; ++j)
+            tma_load_2d(sa + kABytes + j * C::kBBox * 128, &tB, fb, kk * kBK, j * C::kBBox, px);
           pending[stage] = (int)phase;
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
@@ -243,7 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_trigger();
     if (lane == 0) {
       // ---------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16(128, MPAD);
+      constexpr uint32_t idesc0 = idesc_bf16(128, C::kN0);
+      constexpr uint32_t idesc1 = idesc_bf16(128, C::kN1 > 0 ? C::kN1 : 16);
       int stage = 0;
       uint32_t phase = 0;
       int abuf = 0;
@@ -262,14 +268,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t da = desc_sw128(sa), db = desc_sw128(sa + kABytes);
 #pragma unroll
           for (int k16 = 0; k16 < kBK / 16; ++k16)
-            tc_mma(d, da + (uint64_t)(2 * k16), db + (uint64_t)(2 * k16), idesc,
-                   (kk == sg.k0 && k16 == 0) ? 0u : 1u);
+          {
+            const uint32_t acc = (kk == sg.k0 && k16 == 0) ? 0u : 1u;
+            tc_mma(d, da + (uint64_t)(2 * k16), db + (uint64_t)(2 * k16), idesc0, acc);
+            if (C::kN1 > 0)   // rows 256.. of the activation tile: 256 * 128 B further, TMEM columns 256..
+              tc_mma(d + 256u, da + (uint64_t)(2 * k16), db + (uint64_t)(2 * k16) + (uint64_t)((256 * 128) >> 4),
+                     idesc1, acc);
+          }
           tc_commit(empty0 + 8 * stage);
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         tc_commit(afull0 + 8 * abuf);
-        if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
+        if (++abuf == C::kBufs) { abuf = 0; aphase ^= 1u; }
       }
       // all MMAs issued by this thread complete before TMEM is released
       tc_commit(drain);
@@ -291,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(aempty0 + 8 * abuf);
-      if (++abuf == 2) { abuf = 0; aphase ^= 1u; }
+      if (++abuf == C::kBufs) { abuf = 0; aphase ^= 1u; }
     }
     epi.finish(warp, lane);
   }

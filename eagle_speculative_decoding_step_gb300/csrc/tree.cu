@@ -102,12 +102,21 @@ __global__ void __launch_bounds__(256) tree_expand_kernel(TreeDims td, int d, co
     tv.mask[p] = 0ull;
   }
   __syncthreads();
+  // pool scores / depths staged in shared memory for the rank counting below
+  __shared__ float s_score[1024];
+  __shared__ unsigned char s_depth[1024];
+  const int cnt = c0 + nc;
+  for (int p = threadIdx.x; p < cnt; p += blockDim.x) {
+    s_score[p] = tv.score[p];
+    s_depth[p] = (unsigned char)tv.depth[p];
+  }
+  __syncthreads();
   // 2. next frontier = the k best new candidates
   for (int t = threadIdx.x; t < nc; t += blockDim.x) {
     const int p = c0 + t;
-    const float sp = tv.score[p];
+    const float sp = s_score[p];
     int r = 0;
-    for (int u = 0; u < nc; ++u) r += ranks_before(tv.score[c0 + u], c0 + u, sp, p) ? 1 : 0;
+    for (int u = 0; u < nc; ++u) r += ranks_before(s_score[c0 + u], c0 + u, sp, p) ? 1 : 0;
     if (r < k) s_order[r] = p;
   }
   __syncthreads();
@@ -134,24 +143,23 @@ __global__ void __launch_bounds__(256) tree_expand_kernel(TreeDims td, int d, co
     return;
   }
   // 3b. final selection: the N best of the pool, numbered by (depth, score, creation)
-  const int cnt = c0 + nc;
   const int N = td.N;
   for (int p = threadIdx.x; p < cnt; p += blockDim.x) {
-    const float sp = tv.score[p];
+    const float sp = s_score[p];
     int r = 0;
-    for (int u = 0; u < cnt; ++u) r += ranks_before(tv.score[u], u, sp, p) ? 1 : 0;
+    for (int u = 0; u < cnt; ++u) r += ranks_before(s_score[u], u, sp, p) ? 1 : 0;
     s_map[p] = (r < N) ? 0 : -1;
   }
   __syncthreads();
   for (int p = threadIdx.x; p < cnt; p += blockDim.x) {
     if (s_map[p] < 0) continue;
-    const int dp = tv.depth[p];
-    const float sp = tv.score[p];
+    const int dp = s_depth[p];
+    const float sp = s_score[p];
     int r = 0;
     for (int u = 0; u < cnt; ++u) {
       if (s_map[u] < 0) continue;
-      const int du = tv.depth[u];
-      r += (du < dp || (du == dp && ranks_before(tv.score[u], u, sp, p))) ? 1 : 0;
+      const int du = s_depth[u];
+      r += (du < dp || (du == dp && ranks_before(s_score[u], u, sp, p))) ? 1 : 0;
     }
     s_order[r] = p;    // final index r + 1
   }

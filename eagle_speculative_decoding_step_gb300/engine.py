@@ -40,7 +40,8 @@ class DeviceModel:
         self.w = w
         self.device = device
         self.desc = lib.make_desc(w)
-        self.tW = {k: to_device(v, w.dtype, device) for k, v in W.items()}
+        self.tW = {k: (torch.from_numpy(np.asarray(v, dtype=np.int32)).to(device) if k == "d2t"
+                       else to_device(v, w.dtype, device)) for k, v in W.items()}
         self.weights = lib.make_weights(self.tW)
         self.tkv = {
             "k": to_device(kv["k"], w.dtype, device),
@@ -177,6 +178,75 @@ class TreeStep:
         lib.spec_verify_greedy(self.B, self.N + 1, self.V, self.target, self.t_tok, self.out, self.acc, self.kv_src,
                                parent=self.t_par, max_depth=self.D, desc=dm.desc if compact else None,
                                kv=dm.kv if compact else None, ctx_len=dm.ctx_len, ws=self.vws)
+
+    def run(self):
+        self.draft()
+        self.verify()
+
+
+class PrefillChainStep:
+    """Chain step whose first draft pass runs over all R = 1 + K verified tokens of
+    every request ([NEURON] "EagleProposer", propose() prefill phase): index
+    kernel (shifted ids, positions, causal masks), FC fuse over the B*R aux
+    rows, one draft pass over B*R rows, gather of each request's last accepted
+    row, LM head, then K-1 recurrent passes after the accepted tokens, then
+    verification against target logits [B, K+1, V]."""
+
+    def __init__(self, dm: DeviceModel, aux_rows, input_ids, next_token, last_idx, target, K=None):
+        w = dm.w
+        self.dm = dm
+        B = w.B
+        R = input_ids.shape[1]
+        K = K or w.K
+        self.B, self.R, self.K, self.V = B, R, K, w.V
+        dev = dm.device
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.aux, self.ids_in, self.next_tok, self.last_idx, self.target = aux_rows, input_ids, next_token, last_idx, target
+        M = B * R
+        self.tok = torch.zeros(M, **i32)
+        self.pos = torch.zeros(M, **i32)
+        self.kv_idx = torch.zeros(M, **i32)
+        self.mask = torch.zeros(M, dtype=torch.int64, device=dev)
+        self.last_row = torch.zeros(B, **i32)
+        self.ctx_next = torch.zeros(B, **i32)
+        self.h0 = dm.hidden(M)
+        self.pre_all = dm.hidden(M)
+        self.hn_all = dm.hidden(M)
+        self.pre = [dm.hidden(B), dm.hidden(B)]
+        self.hn = dm.hidden(B)
+        self.drafts = torch.zeros(B, K, **i32)
+        self.lp = torch.zeros(B, K, dtype=torch.float32, device=dev)
+        self.out = torch.zeros(B, K + 1, **i32)
+        self.acc = torch.zeros(B, **i32)
+        self.kv_src = torch.zeros(B, K + 1, **i32)
+        self.vws = torch.zeros(lib.spec_verify_workspace_bytes(B, K + 1, w.V), dtype=torch.uint8, device=dev)
+
+    def draft(self):
+        dm, w, B, R, K = self.dm, self.dm.w, self.B, self.R, self.K
+        M = B * R
+        es = 2 if w.dtype == "bf16" else 4
+        lib.spec_prefill_inputs(B, R, self.ids_in, self.next_tok, self.last_idx, dm.ctx_len, self.tok, self.pos,
+                                self.kv_idx, self.mask, self.last_row, self.ctx_next, ws=dm.ws)
+        lib.spec_fc_fuse(dm.desc, dm.weights, self.aux, self.h0, M, dm.ws)
+        rows = lib.make_rows(M, B, R, dm.ctx_len, self.tok, pos=self.pos, kv_idx=self.kv_idx, mask=self.mask,
+                             max_ctx=w.max_ctx)
+        lib.spec_draft_layer(dm.desc, dm.weights, rows, self.h0, self.pre_all, self.hn_all, dm.kv, dm.ws)
+        lib.spec_gather_rows(self.hn_all, M, w.H * es, self.last_row, B, self.hn, ws=dm.ws)
+        lib.spec_gather_rows(self.pre_all, M, w.H * es, self.last_row, B, self.pre[1], ws=dm.ws)
+        lib.spec_lm_head(dm.desc, dm.weights, self.hn, B, 1, self.drafts, self.lp, ws=dm.ws, ids_ld=K)
+        hid = self.pre[1]
+        for i in range(1, K):
+            rows = lib.make_rows(B, B, 1, self.ctx_next, self.drafts.data_ptr() + 4 * (i - 1), step=i - 1,
+                                 tok_stride=K, max_ctx=w.max_ctx + R)
+            out = self.pre[(i + 1) % 2]
+            lib.spec_draft_layer(dm.desc, dm.weights, rows, hid, out, self.hn, dm.kv, dm.ws)
+            lib.spec_lm_head(dm.desc, dm.weights, self.hn, B, 1, self.drafts.data_ptr() + 4 * i,
+                             self.lp.data_ptr() + 4 * i, ws=dm.ws, ids_ld=K)
+            hid = out
+
+    def verify(self):
+        lib.spec_verify_greedy(self.B, self.K + 1, self.V, self.target, self.drafts, self.out, self.acc, self.kv_src,
+                               ws=self.vws)
 
     def run(self):
         self.draft()

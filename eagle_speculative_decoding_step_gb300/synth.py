@@ -33,7 +33,7 @@ _TID = {
     "fc": 1, "embed": 2, "hidden_norm": 3, "in_norm": 4, "post_norm": 5, "final_norm": 6,
     "wq": 7, "wk": 8, "wv": 9, "wo": 10, "wgate": 11, "wup": 12, "wdown": 13, "lm_head": 14,
     "aux": 20, "kv_k": 21, "kv_v": 22, "ctx": 23, "blocks": 24, "root": 25, "noise": 26,
-    "hid": 27, "misc": 28,
+    "hid": 27, "misc": 28, "d2t": 29,
 }
 
 
@@ -103,8 +103,18 @@ def make_weights(w, with_lm_head: bool = True) -> dict:
     W["wup"] = _store(normal((I, H), s, "wup", 0.02), w.dtype)
     W["wdown"] = _store(normal((H, I), s, "wdown", 0.02), w.dtype)
     if with_lm_head:
-        W["lm_head"] = _store(normal((V, H), s, "lm_head", 0.02), w.dtype)
+        rows = w.draft_vocab if w.draft_vocab > 0 else V
+        W["lm_head"] = _store(normal((rows, H), s, "lm_head", 0.02), w.dtype)
+        if w.draft_vocab > 0:
+            W["d2t"] = draft_vocab_map(w)
     return W
+
+
+def draft_vocab_map(w) -> np.ndarray:
+    """Target token id of each draft-vocabulary entry: a seeded, sorted subset of
+    the target vocabulary (stand-in for a calibrated frequent-token list)."""
+    g = np.random.default_rng([w.seed, _TID["d2t"]])
+    return np.sort(g.choice(w.V, size=w.draft_vocab, replace=False)).astype(np.int32)
 
 
 def lowrank_factors(lm_head: np.ndarray, rank: int, dtype: str):

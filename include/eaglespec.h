@@ -78,6 +78,10 @@ typedef struct {
                              draft-region key of a row is inside the window. */
   int32_t rank;           /* rank r of the EAGLE-4 candidate head; 0 = none */
   int32_t num_candidates; /* candidates kept from the low-rank scores (Kc) */
+  int32_t draft_vocab;    /* rows of lm_head when the draft predicts over a
+                             reduced vocabulary ([QUARK] calibrate_draft_vocab,
+                             draft_vocab_size; [EAGLE4] selected_token_ids);
+                             0 = the full vocabulary.  Needs weights.d2t. */
 } spec_model_desc;
 
 /* Draft weights, device pointers, dtype of the descriptor.  [NEURON] "Eagle3
@@ -101,6 +105,9 @@ typedef struct {
   const void *lm_head;     /* [V, H] */
   const void *lr_down;     /* [r, H]  efficient_lm_head_down_proj (rank > 0) */
   const void *lr_up;       /* [V, r]  efficient_lm_head (rank > 0) */
+  const int32_t *d2t;      /* [draft_vocab] target token id of each draft-vocabulary
+                              entry (draft_vocab > 0); lm_head is then
+                              [draft_vocab, H] */
 } spec_weights;
 
 /* Paged K/V cache of the draft layer ([NEURON] "KV Cache Sharing" and
@@ -217,7 +224,9 @@ spec_status spec_draft_layer(const spec_model_desc *desc, const spec_weights *w,
  * lse = log(sum(exp(logits))).
  * [NEURON] "Eagle3 Draft Model Architecture" (LM head) and "Design Choices"
  * (greedy draft sampling: k = 1); top-k per node for trees from [EAGLET]
- * draft_top_k.  hn [M, H]; topk_ids / topk_logprob at [m * ids_ld + j]
+ * draft_top_k.  With a reduced draft vocabulary (desc.draft_vocab > 0) the
+ * softmax and top-k run over the draft_vocab rows of lm_head and the emitted
+ * ids are the mapped target ids d2t[row].  hn [M, H]; topk_ids / topk_logprob at [m * ids_ld + j]
  * (ids_ld >= k; 0 means k); lse [M] or NULL; 1 <= k <= 8.
  * logits_or_null: if not NULL, also writes the fp32 logits [M, V]. */
 spec_status spec_lm_head(const spec_model_desc *desc, const spec_weights *w,
@@ -335,6 +344,32 @@ spec_status spec_decode_metadata(int32_t R, const int32_t *cu_num_scheduled, con
                                  int32_t *logits_indices, int32_t *target_logits_indices,
                                  int32_t *bonus_logits_indices, int32_t *draft_token_ids, void *ws,
                                  spec_stream_t stream);
+
+/* Inputs of the batched initial draft pass over the verified tokens ([NEURON]
+ * "EagleProposer", propose() prefill phase: the draft processes all target
+ * tokens; input ids shifted by one with the new token scattered at the last
+ * token position).  Request b verified R tokens input_ids[b, 0..R-1] at
+ * positions ctx_len[b] .. ctx_len[b]+R-1 and accepted through row last_idx[b]
+ * (0 <= last_idx < R); next_token[b] is the target's new token.  Writes the
+ * pass's rows in spec_rows form, all [B*R]:
+ *   tok[b*R+j]    = next_token[b] if j == last_idx[b], else input_ids[b, j+1]
+ *                   (0 past the end);
+ *   pos = ctx_len[b] + j, kv_idx = j, mask = bits 0..j (causal within the
+ *   request), and last_row[b] = b*R + last_idx[b] (the row whose LM head gives
+ *   the first draft token; gather it with spec_gather_rows), and, if not NULL,
+ *   ctx_next[b] = ctx_len[b] + last_idx[b] + 1 (the context of the recurrent
+ *   passes that follow).  R <= 64.
+ * ws: NULL or a workspace whose error word flags last_idx out of range. */
+spec_status spec_prefill_inputs(int32_t B, int32_t R, const int32_t *input_ids, const int32_t *next_token,
+                                const int32_t *last_idx, const int32_t *ctx_len, int32_t *tok,
+                                int32_t *pos, int32_t *kv_idx, uint64_t *mask, int32_t *last_row,
+                                int32_t *ctx_next, void *ws, spec_stream_t stream);
+
+/* dst[r] = src[rows[r]] for r < n; rows of row_bytes bytes (a multiple of 16,
+ * 16-byte aligned buffers); src has n_src rows.  An out-of-range index sets the
+ * error word of ws (if not NULL) and leaves that row untouched. */
+spec_status spec_gather_rows(const void *src, int32_t n_src, int32_t row_bytes, const int32_t *rows,
+                             int32_t n, void *dst, void *ws, spec_stream_t stream);
 
 /* Greedy verification without caller-provided scratch.  The paper has no
  * counterpart: this entry point exists for callers that cannot allocate device

@@ -164,7 +164,7 @@ def draft_layer(desc, W, rows, hid_in, kv):
 
 
 def lm_head(desc, W, hn, k):
-    """Full-vocabulary LM head with per-row top-k and log-softmax statistics.
+    """LM head with per-row top-k and log-softmax statistics.
 
     logits = hn @ lm_head^T ([NEURON] "Eagle3 Draft Model Architecture", LM head;
     greedy draft sampling in "Design Choices" is top-1).  lse = log sum exp of
@@ -175,6 +175,11 @@ def lm_head(desc, W, hn, k):
     lse = logsumexp(logits, axis=-1)
     ids = topk_desc(logits.astype(np.float32), k)
     lp = np.take_along_axis(logits, ids, axis=-1) - lse[:, None]
+    if getattr(desc, "draft_vocab", 0) > 0:
+        # reduced draft vocabulary: rows of lm_head are draft entries, emitted ids are
+        # the mapped target ids ([QUARK] calibrate_draft_vocab / d2t; [EAGLE4]
+        # selected_token_ids); logits stay indexed by draft entry
+        ids = np.asarray(W["d2t"], dtype=np.int64)[ids]
     return ids, lp, lse, logits
 
 

@@ -99,3 +99,50 @@ def chain_step(desc, W, aux, root_tok, ctx_len, kv, K, target, temperature=None,
     else:
         out, acc, _ = verify.verify_greedy_chain(target, drafts)
     return drafts, out, acc
+
+
+def prefill_inputs(input_ids, next_token, last_idx, ctx_len):
+    """Rows of the batched initial draft pass ([NEURON] "EagleProposer", prefill
+    phase: ids shifted by one, the new token scattered at the last accepted row;
+    row j of request b at position ctx + j, draft-region entry j, causal mask)."""
+    ids = np.asarray(input_ids, dtype=np.int64)
+    B, R = ids.shape
+    tok = np.zeros((B, R), dtype=np.int64)
+    tok[:, :R - 1] = ids[:, 1:]
+    for b in range(B):
+        tok[b, int(last_idx[b])] = next_token[b]
+    ctx = np.asarray(ctx_len, dtype=np.int64)
+    pos = (ctx[:, None] + np.arange(R)[None, :]).reshape(-1)
+    kv_idx = np.tile(np.arange(R), B)
+    mask = [(1 << (j + 1)) - 1 for b in range(B) for j in range(R)]
+    last_row = np.arange(B) * R + np.asarray(last_idx, dtype=np.int64)
+    return {"M": B * R, "B": B, "R": R, "step": 0, "ctx_len": ctx, "tok": tok.reshape(-1), "pos": pos,
+            "kv_idx": kv_idx, "mask": mask}, last_row
+
+
+def prefill_chain_draft(desc, W, aux_rows, input_ids, next_token, last_idx, ctx_len, kv, K, keep_logits=False):
+    """propose() with the prefill phase: FC over every verified token's aux
+    states, one draft pass over all of them, the first draft token from each
+    request's last accepted row, then K-1 recurrent passes starting after the
+    accepted tokens (context ctx + last_idx + 1).  Returns drafts [B, K]."""
+    rows, last_row = prefill_inputs(input_ids, next_token, last_idx, ctx_len)
+    h0 = draft.fc_fuse(desc, W, aux_rows)
+    pre, hn = draft.draft_layer(desc, W, rows, h0, kv)
+    ids, _, _, lg = draft.lm_head(desc, W, hn[last_row], 1)
+    B = len(next_token)
+    drafts = np.zeros((B, K), dtype=np.int64)
+    drafts[:, 0] = ids[:, 0]
+    logits = [lg]
+    hid = pre[last_row]
+    ctx2 = np.asarray(ctx_len, dtype=np.int64) + np.asarray(last_idx, dtype=np.int64) + 1
+    tok = ids[:, 0]
+    for i in range(1, K):
+        r = {"M": B, "B": B, "R": 1, "step": i - 1, "ctx_len": ctx2, "tok": tok}
+        hid, hn = draft.draft_layer(desc, W, r, hid, kv)
+        ids, _, _, lg = draft.lm_head(desc, W, hn, 1)
+        drafts[:, i] = ids[:, 0]
+        tok = ids[:, 0]
+        logits.append(lg)
+    if keep_logits:
+        return drafts, np.stack(logits, axis=1)
+    return drafts

@@ -137,3 +137,29 @@ def test_lowrank_candidates(M):
     full = np.asarray(hn, np.float64) @ np.asarray(W["lm_head"], np.float64).T
     ids_match(out, out_ref, full)
     no_device_error(dm)
+
+
+DRAFTVOCAB = replace(SMALL_BF16, name="small_d2t", V=6000, draft_vocab=2500, seed=41)
+
+
+@pytest.mark.parametrize("k,M", [(1, 4), (8, 8)])
+def test_lm_head_reduced_draft_vocabulary(k, M):
+    """LM head over draft_vocab rows; emitted ids are the mapped target ids (d2t)."""
+    w = DRAFTVOCAB
+    W, ctx, kv, dm = setup(w, max_rows=M)
+    assert W["lm_head"].shape[0] == w.draft_vocab
+    hn = synth.make_hidden(w, M, sub=7)
+    ref_ids, ref_lp, ref_lse, ref_logits = od.lm_head(w, W, hn, k)
+    ids = torch.zeros(M, k, dtype=torch.int32, device="cuda")
+    lp = torch.zeros(M, k, dtype=torch.float32, device="cuda")
+    lse = torch.zeros(M, dtype=torch.float32, device="cuda")
+    lib.spec_lm_head(dm.desc, dm.weights, dev_act(hn, w), M, k, ids, lp, lse, ws=dm.ws)
+    got = ids.cpu().numpy()
+    # compare in draft-vocabulary indices (t2d of the emitted ids)
+    t2d = {int(t): i for i, t in enumerate(W["d2t"])}
+    got_d = np.vectorize(t2d.get)(got)
+    ref_d = np.vectorize(t2d.get)(ref_ids)
+    ids_match(got_d, ref_d, ref_logits)
+    assert set(got.reshape(-1).tolist()) <= set(W["d2t"].tolist())
+    assert_close(lse.cpu().numpy(), ref_lse, w, "lse")
+    no_device_error(dm)

@@ -99,3 +99,27 @@ def test_chain_step_graph_replay():
     torch.cuda.synchronize()
     assert torch.equal(st.out, out0)
     no_device_error(dm)
+
+
+def test_chain_step_reduced_draft_vocabulary():
+    w = replace(SMALL_BF16, name="small_d2t_chain", V=6000, draft_vocab=2500, seed=42)
+    W, ctx, kv, dm, aux, root, _ = _chain_case_nolm(w)
+    drafts_ref, logits_ref = ostep.chain_draft(w, W, aux, root, ctx, copy.deepcopy(kv), w.K, keep_logits=True)
+    target = synth.noise(w, (w.B, w.K + 1, w.V))
+    st = engine.ChainStep(dm, dev_act(aux, w), dev(root), dev(target))
+    st.run()
+    torch.cuda.synchronize()
+    drafts = st.drafts.cpu().numpy()
+    t2d = {int(t): i for i, t in enumerate(W["d2t"])}
+    for i in range(w.K):
+        if not np.array_equal(drafts[:, i], drafts_ref[:, i]):
+            ids_match(np.vectorize(t2d.get)(drafts[:, i]), np.vectorize(t2d.get)(drafts_ref[:, i]), logits_ref[:, i])
+            return
+    ref_out, ref_acc, _ = overify.verify_greedy_chain(target, drafts_ref)
+    np.testing.assert_array_equal(st.out.cpu().numpy(), ref_out)
+    no_device_error(dm)
+
+
+def _chain_case_nolm(w):
+    W, ctx, kv, dm = setup(w)
+    return W, ctx, kv, dm, synth.make_aux(w), synth.root_tokens(w), None
