@@ -75,15 +75,15 @@ EXPORTS = {
     "spec_lm_head": (c_i32, [ctypes.POINTER(ModelDesc), ctypes.POINTER(Weights), c_vp, c_i32, c_i32, c_vp, c_i32,
                              c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
     "spec_lowrank_candidates": (c_i32, [ctypes.POINTER(ModelDesc), ctypes.POINTER(Weights), c_vp, c_i32, c_i32,
-                                        c_vp, c_vp, c_vp, c_i32, c_vp, c_size, c_vp]),
+                                        c_vp, c_vp, c_vp, c_vp, c_i32, c_vp, c_size, c_vp]),
     "spec_tree_state_bytes": (c_size, [c_i32, c_i32, c_i32, c_i32]),
     "spec_tree_expand": (c_i32, [c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
                                  ctypes.POINTER(TreeIO), c_vp]),
     "spec_verify_workspace_bytes": (c_size, [c_i32, c_i32, c_i32]),
     "spec_verify_greedy": (c_i32, [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp,
                                    ctypes.POINTER(ModelDesc), ctypes.POINTER(KV), c_vp, c_vp, c_size, c_vp]),
-    "spec_verify_rejection": (c_i32, [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_u64, c_u64, c_vp, c_vp, c_vp, c_vp,
-                                      c_size, c_vp]),
+    "spec_verify_rejection": (c_i32, [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_u64, c_u64, c_vp, c_vp,
+                                      c_vp, c_vp, c_size, c_vp]),
     "spec_decode_metadata": (c_i32, [c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "spec_prefill_inputs": (c_i32, [c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                     c_vp]),
@@ -209,10 +209,11 @@ def spec_lm_head(desc, weights, hn, M, k, topk_ids, topk_logprob, lse=None, logi
 
 
 def spec_lowrank_candidates(desc, weights, hn, M, k_out, out_ids, cand_ids=None, cand_logits=None, ws=None,
-                            out_ld=0):
+                            out_ld=0, out_logprob=None):
     _check(_lib().spec_lowrank_candidates(ctypes.byref(desc), ctypes.byref(weights), _p(hn), M, k_out,
-                                          _p(cand_ids), _p(cand_logits), _p(out_ids), out_ld, _p(ws),
-                                          ws.numel() * ws.element_size(), _stream()), "spec_lowrank_candidates")
+                                          _p(cand_ids), _p(cand_logits), _p(out_ids), _p(out_logprob), out_ld,
+                                          _p(ws), ws.numel() * ws.element_size(), _stream()),
+           "spec_lowrank_candidates")
 
 
 def spec_tree_expand(B, top_k, depth_idx, depth, total, ctx_len, root_tok, topk_ids, topk_logprob, state, io):
@@ -229,10 +230,10 @@ def spec_verify_greedy(B, R, V, target_logits, draft_tok, out_tok, accept_len, k
 
 
 def spec_verify_rejection(B, K, V, target_logits, draft_tok, temperature, seed, step_offset, out_tok, accept_len,
-                          kv_src=None, ws=None):
-    _check(_lib().spec_verify_rejection(B, K, V, _p(target_logits), _p(draft_tok), _p(temperature), seed,
-                                        step_offset, _p(out_tok), _p(accept_len), _p(kv_src), _p(ws),
-                                        ws.numel() * ws.element_size(), _stream()), "spec_verify_rejection")
+                          kv_src=None, ws=None, top_k=None, top_p=None):
+    _check(_lib().spec_verify_rejection(B, K, V, _p(target_logits), _p(draft_tok), _p(temperature), _p(top_k),
+                                        _p(top_p), seed, step_offset, _p(out_tok), _p(accept_len), _p(kv_src),
+                                        _p(ws), ws.numel() * ws.element_size(), _stream()), "spec_verify_rejection")
 
 
 def spec_verify_greedy_static(B, R, V, target_logits, draft_tok, out_tok, accept_len, kv_src=None, parent=None,

@@ -34,7 +34,7 @@ spec_status launch_attention(const spec_model_desc&, const spec_rows&, const voi
 void launch_row_stats(const float*, int, int, int, int32_t*, int, float*, float*, const int32_t*, cudaStream_t);
 void launch_topk_select(const float*, int, int, int, int32_t*, cudaStream_t);
 void launch_rescore(int, const void*, const void*, int, int, const int32_t*, int, int, float*, void*, cudaStream_t);
-void launch_cand_best(const float*, const int32_t*, int, int, int, int32_t*, int, cudaStream_t);
+void launch_cand_best(const float*, const int32_t*, int, int, int, int32_t*, int, float*, cudaStream_t);
 spec_status launch_lm_head_fused(const spec_model_desc&, const void*, const void*, int, int, int32_t*, int, float*,
                                  float*, const int32_t*, void*, size_t, cudaStream_t);
 size_t lm_fused_ws_bytes(int M, int sms);
@@ -349,8 +349,8 @@ extern "C" spec_status spec_lm_head(const spec_model_desc* desc, const spec_weig
 
 extern "C" spec_status spec_lowrank_candidates(const spec_model_desc* desc, const spec_weights* w, const void* hn,
                                                int32_t M, int32_t k_out, int32_t* cand_ids, float* cand_logits,
-                                               int32_t* out_ids, int32_t out_ld, void* ws, size_t ws_bytes,
-                                               spec_stream_t stream) {
+                                               int32_t* out_ids, float* out_logprob, int32_t out_ld, void* ws,
+                                               size_t ws_bytes, spec_stream_t stream) {
   spec_status s = check_desc(desc);
   if (s != SPEC_OK) return s;
   const spec_model_desc& d = *desc;
@@ -380,6 +380,6 @@ extern "C" spec_status spec_lowrank_candidates(const spec_model_desc* desc, cons
   }
   launch_topk_select(sc, M, d.vocab, Kc, cand, stream);
   launch_rescore(d.dtype, hn, w->lm_head, d.hidden, d.vocab, cand, M, Kc, exact, ws, stream);
-  launch_cand_best(exact, cand, M, Kc, k_out, out_ids, out_ld, stream);
+  launch_cand_best(exact, cand, M, Kc, k_out, out_ids, out_ld, out_logprob, stream);
   return last_launch();
 }

@@ -711,15 +711,28 @@ __global__ void __launch_bounds__(256) rescore_kernel(const T* __restrict__ hn, 
 }
 
 // best k_out exact logits among the candidates (ties to the smaller token id)
+// (with out_lp: log-probs of the chosen ids under the softmax over the candidates'
+// exact logits)
 __global__ void __launch_bounds__(128) cand_best_kernel(const float* __restrict__ exact,
                                                         const int32_t* __restrict__ cand, int Kc, int k_out,
-                                                        int32_t* __restrict__ out, int ld_out) {
+                                                        int32_t* __restrict__ out, int ld_out,
+                                                        float* __restrict__ out_lp) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[32];
   __shared__ int redi[32];
   __shared__ int chosen[8];
   const int m = blockIdx.x;
+  float lse = 0.f;
+  if (out_lp) {
+    float mx = -INFINITY;
+    for (int j = threadIdx.x; j < Kc; j += blockDim.x) mx = fmaxf(mx, exact[(size_t)m * Kc + j]);
+    mx = block_max(mx, red);
+    float sm = 0.f;
+    for (int j = threadIdx.x; j < Kc; j += blockDim.x) sm += expf(exact[(size_t)m * Kc + j] - mx);
+    sm = block_sum(sm, red);
+    lse = mx + logf(sm);
+  }
   for (int r = 0; r < k_out; ++r) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
@@ -734,6 +747,7 @@ __global__ void __launch_bounds__(128) cand_best_kernel(const float* __restrict_
     if (threadIdx.x == 0) {
       chosen[r] = bi;
       out[(size_t)m * ld_out + r] = bi;
+      if (out_lp) out_lp[(size_t)m * ld_out + r] = bv - lse;
     }
     __syncthreads();
   }
@@ -927,8 +941,8 @@ void launch_rescore(int dtype, const void* hn, const void* lm_head, int H, int V
 }
 
 void launch_cand_best(const float* exact, const int32_t* cand, int M, int Kc, int k_out, int32_t* out, int ld_out,
-                      cudaStream_t st) {
-  launch_pdl(cand_best_kernel, dim3(M), dim3(128), 0, st, exact, cand, Kc, k_out, out, ld_out);
+                      float* out_lp, cudaStream_t st) {
+  launch_pdl(cand_best_kernel, dim3(M), dim3(128), 0, st, exact, cand, Kc, k_out, out, ld_out, out_lp);
 }
 
 }  // namespace spec

@@ -178,16 +178,189 @@ __global__ void __launch_bounds__(128) verify_greedy_finalize_kernel(
   }
 }
 
+// ---------------------------------------------------------------- top-k / top-p
+// Per-row kept set of a filtered target distribution, as a threshold in the
+// order (value desc, id asc): token x is kept iff key(x) > key or (key(x) == key
+// and x <= id), key() being an order-preserving map of logit / T.
+struct Thr { uint32_t key; int id; };
+
+SPEC_DEV uint32_t okey(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+SPEC_DEV bool kept_by(const Thr& t, uint32_t k, int x) { return k > t.key || (k == t.key && x <= t.id); }
+
+// id of the `need`-th (1-based) smallest index x with key(x) == kk that `inside`
+// accepts; block-wide ordered scan (ballots per 1024-wide chunk)
+template <typename F>
+__device__ int nth_tie_id(const float* x, float T, int V, uint32_t kk, int need, F inside, int* wcount, int* s_taken,
+                          int* s_id) {
+  const int tid = threadIdx.x;
+  if (tid == 0) { *s_taken = 0; *s_id = 0x7fffffff; }
+  __syncthreads();
+  for (int base = 0; base < V; base += blockDim.x) {
+    const int v = base + tid;
+    bool eq = false;
+    if (v < V) {
+      const uint32_t k = okey(x[v] / T);
+      eq = (k == kk) && inside(k, v);
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, eq);
+    if ((tid & 31) == 0) wcount[tid >> 5] = __popc(bal);
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < (tid >> 5); ++w) before += wcount[w];
+    before += __popc(bal & ((1u << (tid & 31)) - 1u));
+    const int taken = *s_taken;
+    if (eq && taken + before + 1 == need) *s_id = v;
+    __syncthreads();
+    if (tid == 0) {
+      int tot = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += wcount[w];
+      *s_taken = taken + tot;
+    }
+    __syncthreads();
+    if (*s_taken >= need) break;
+  }
+  return *s_id;
+}
+
+// One CTA (1024 threads) per row.  top-k: exact radix selection of the k-th key
+// and the id of the last tie kept.  top-p (within the top-k set): radix search
+// of the shortest prefix whose probability mass reaches top_p, masses
+// exp(y - max) in 2^-40 fixed point so the sums do not depend on thread order.
+__global__ void __launch_bounds__(1024) reject_threshold_kernel(const float* __restrict__ logits, int K, int V,
+                                                                const float* __restrict__ temperature,
+                                                                const int32_t* __restrict__ top_k,
+                                                                const float* __restrict__ top_p, Thr* __restrict__ thr) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ unsigned long long hist[256];
+  __shared__ uint32_t s_prefix;
+  __shared__ unsigned long long s_need;
+  __shared__ int wcount[32];
+  __shared__ int s_taken, s_id;
+  __shared__ float red[32];
+  __shared__ unsigned long long s_tot;
+  const int row = blockIdx.x;
+  const int b = row / (K + 1);
+  const int tid = threadIdx.x;
+  const float T = temperature[b];
+  const int kk_req = top_k ? top_k[b] : 0;
+  const float pp = top_p ? top_p[b] : 1.f;
+  Thr t{0u, 0x7fffffff};                       // keep everything
+  const bool do_k = T > 0.f && kk_req > 0 && kk_req < V;
+  const bool do_p = T > 0.f && pp < 1.f;
+  if (!do_k && !do_p) {
+    if (tid == 0) thr[row] = t;
+    return;
+  }
+  const float* x = logits + (size_t)row * V;
+  if (do_k) {
+    if (tid == 0) { s_prefix = 0; s_need = (unsigned long long)kk_req; }
+    __syncthreads();
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      if (tid < 256) hist[tid] = 0;
+      __syncthreads();
+      const uint32_t prefix = s_prefix;
+      const uint32_t pmask = (shift == 24) ? 0u : (0xffffffffu << (shift + 8));
+      for (int v = tid; v < V; v += blockDim.x) {
+        const uint32_t k = okey(x[v] / T);
+        if ((k & pmask) == (prefix & pmask)) atomicAdd(&hist[(k >> shift) & 0xff], 1ull);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        unsigned long long need = s_need, acc = 0;
+        int dsel = 0;
+        for (int d = 255; d >= 0; --d) {
+          if (acc + hist[d] >= need) { dsel = d; break; }
+          acc += hist[d];
+        }
+        s_need = need - acc;
+        s_prefix = prefix | ((uint32_t)dsel << shift);
+      }
+      __syncthreads();
+    }
+    t.key = s_prefix;
+    const int need = (int)s_need;
+    t.id = nth_tie_id(x, T, V, t.key, need, [](uint32_t, int) { return true; }, wcount, &s_taken, &s_id);
+  }
+  if (do_p) {
+    const Thr tk = t;
+    float mx = -INFINITY;
+    for (int v = tid; v < V; v += blockDim.x) mx = fmaxf(mx, x[v] / T);
+    mx = block_max(mx, red);
+    const double scale = 1099511627776.0;     // 2^40
+    if (tid == 0) s_tot = 0;
+    __syncthreads();
+    unsigned long long z = 0;
+    for (int v = tid; v < V; v += blockDim.x) {
+      const float y = x[v] / T;
+      if (kept_by(tk, okey(y), v)) z += (unsigned long long)((double)expf(y - mx) * scale + 0.5);
+    }
+    atomicAdd(&s_tot, z);
+    __syncthreads();
+    if (tid == 0) {
+      s_prefix = 0;
+      s_need = (unsigned long long)ceil((double)pp * (double)s_tot);
+      if (s_need == 0) s_need = 1;
+    }
+    __syncthreads();
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      if (tid < 256) hist[tid] = 0;
+      __syncthreads();
+      const uint32_t prefix = s_prefix;
+      const uint32_t pmask = (shift == 24) ? 0u : (0xffffffffu << (shift + 8));
+      for (int v = tid; v < V; v += blockDim.x) {
+        const float y = x[v] / T;
+        const uint32_t k = okey(y);
+        if ((k & pmask) == (prefix & pmask) && kept_by(tk, k, v))
+          atomicAdd(&hist[(k >> shift) & 0xff], (unsigned long long)((double)expf(y - mx) * scale + 0.5));
+      }
+      __syncthreads();
+      if (tid == 0) {
+        unsigned long long need = s_need, acc = 0;
+        int dsel = 0;
+        for (int d = 255; d >= 0; --d) {
+          if (hist[d] && acc + hist[d] >= need) { dsel = d; break; }
+          acc += hist[d];
+          dsel = d;
+        }
+        s_need = need > acc ? need - acc : 1;
+        s_prefix = prefix | ((uint32_t)dsel << shift);
+      }
+      __syncthreads();
+    }
+    const uint32_t vkey = s_prefix;
+    // every tie at vkey has the same mass; take as many (smallest ids first) as the
+    // remaining mass needs
+    float yv = 0.f;
+    {
+      const uint32_t u = (vkey & 0x80000000u) ? (vkey & 0x7fffffffu) : ~vkey;
+      yv = __uint_as_float(u);
+    }
+    const unsigned long long each = (unsigned long long)((double)expf(yv - mx) * scale + 0.5);
+    int need = each ? (int)((s_need + each - 1) / each) : 1;
+    if (need < 1) need = 1;
+    t.key = vkey;
+    t.id = nth_tie_id(x, T, V, vkey, need, [tk](uint32_t k, int v) { return kept_by(tk, k, v); }, wcount,
+                      &s_taken, &s_id);
+  }
+  if (tid == 0) thr[row] = t;
+}
+
 // ---------------------------------------------------------------- rejection
 template <bool VEC>
 __global__ void __launch_bounds__(256) rejection_chunks_kernel(
     const float* __restrict__ logits, int K, int V, int nch, int L, const int32_t* __restrict__ draft,
-    const float* __restrict__ temperature, uint2 key, uint32_t ctr_w, RejPart* __restrict__ part) {
+    const float* __restrict__ temperature, uint2 key, uint32_t ctr_w, RejPart* __restrict__ part,
+    const Thr* __restrict__ thr) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[32];
   __shared__ int redi[32];
   const int row = blockIdx.y, c = blockIdx.x;
+  const Thr tr = thr ? thr[row] : Thr{0u, 0x7fffffff};
   const int b = row / (K + 1), i = row % (K + 1);
   const float T = temperature[b];
   const bool greedy = !(T > 0.f);
@@ -218,6 +391,7 @@ __global__ void __launch_bounds__(256) rejection_chunks_kernel(
     for (int l = 0; l < 4; ++l) {
       if (j + l >= hi) break;
       float y = v[l] / T;
+      if (!kept_by(tr, okey(y), j + l)) continue;        // filtered out by top-k / top-p
       if (y > m) { s = s * expf(m - y) + 1.f; m = y; }
       else s += expf(y - m);
       if (j + l == excl) continue;
@@ -237,7 +411,8 @@ __global__ void __launch_bounds__(256) rejection_chunks_kernel(
 __global__ void __launch_bounds__(32) rejection_finalize_kernel(
     const float* __restrict__ logits, int K, int V, int nch, const RejPart* __restrict__ part,
     const int32_t* __restrict__ draft, const float* __restrict__ temperature, uint2 key, uint32_t ctr_w0,
-    int32_t* __restrict__ out, int32_t* __restrict__ acc_out, int32_t* __restrict__ kv_src) {
+    int32_t* __restrict__ out, int32_t* __restrict__ acc_out, int32_t* __restrict__ kv_src,
+    const Thr* __restrict__ thr) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
@@ -262,7 +437,12 @@ __global__ void __launch_bounds__(32) rejection_finalize_kernel(
       ok = (d == bi);
     } else {
       float lse = M + logf(S);
-      float pd = (d >= 0 && d < V) ? expf(logits[row * V + d] / T - lse) : 0.f;
+      float pd = 0.f;
+      if (d >= 0 && d < V) {
+        const float yd = logits[row * V + d] / T;
+        const Thr tr = thr ? thr[row] : Thr{0u, 0x7fffffff};
+        if (kept_by(tr, okey(yd), d)) pd = expf(yd - lse);
+      }
       uint4 r = philox4x32_10(make_uint4(0u, (uint32_t)i, (uint32_t)b, ctr_w0), key);
       ok = word_to_uniform(r.x) <= pd;
     }
@@ -284,7 +464,7 @@ extern "C" size_t spec_verify_workspace_bytes(int32_t B, int32_t R, int32_t V) {
   if (B <= 0 || R <= 0 || V <= 0) return 0;
   int rows = B * R;
   int nch = verify_chunks(rows, V);
-  return kWsHeader + align_up((size_t)rows * nch * sizeof(RejPart), 256);
+  return kWsHeader + align_up((size_t)rows * nch * sizeof(RejPart), 256) + align_up((size_t)rows * sizeof(Thr), 256);
 }
 
 extern "C" spec_status spec_verify_greedy(int32_t B, int32_t R, int32_t V, const float* target_logits,
@@ -327,6 +507,7 @@ extern "C" spec_status spec_verify_greedy(int32_t B, int32_t R, int32_t V, const
 
 extern "C" spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, const float* target_logits,
                                              const int32_t* draft_tok, const float* temperature,
+                                             const int32_t* top_k, const float* top_p,
                                              uint64_t seed, uint64_t step_offset, int32_t* out_tok,
                                              int32_t* accept_len, int32_t* kv_src, void* ws,
                                              size_t ws_bytes, spec_stream_t stream) {
@@ -340,16 +521,22 @@ extern "C" spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, co
   RejPart* part = reinterpret_cast<RejPart*>(static_cast<char*>(ws) + kWsHeader);
   uint2 key = make_uint2((uint32_t)(seed & 0xffffffffull), (uint32_t)(seed >> 32));
   uint32_t w0 = (uint32_t)((2ull * step_offset) & 0xffffffffull);
+  Thr* thr = nullptr;
+  if (top_k || top_p) {
+    thr = reinterpret_cast<Thr*>(reinterpret_cast<char*>(part) + align_up((size_t)rows * nch * sizeof(RejPart), 256));
+    launch_pdl(reject_threshold_kernel, dim3(rows), dim3(1024), 0, stream, target_logits, K, V, temperature, top_k,
+               top_p, thr);
+  }
   dim3 grid(nch, rows);
   const bool vec = (V % 4 == 0) && aligned(target_logits, 16);
   if (vec)
-    launch_pdl(rejection_chunks_kernel<true>, dim3(grid), dim3(256), 0, stream, target_logits, K, V, nch, L, draft_tok, temperature,
-                                                            key, w0 + 1u, part);
+    launch_pdl(rejection_chunks_kernel<true>, dim3(grid), dim3(256), 0, stream, target_logits, K, V, nch, L, draft_tok,
+               temperature, key, w0 + 1u, part, (const Thr*)thr);
   else
-    launch_pdl(rejection_chunks_kernel<false>, dim3(grid), dim3(256), 0, stream, target_logits, K, V, nch, L, draft_tok, temperature,
-                                                             key, w0 + 1u, part);
-  launch_pdl(rejection_finalize_kernel, dim3(B), dim3(32), 0, stream, target_logits, K, V, nch, part, draft_tok, temperature, key, w0,
-                                                  out_tok, accept_len, kv_src);
+    launch_pdl(rejection_chunks_kernel<false>, dim3(grid), dim3(256), 0, stream, target_logits, K, V, nch, L, draft_tok,
+               temperature, key, w0 + 1u, part, (const Thr*)thr);
+  launch_pdl(rejection_finalize_kernel, dim3(B), dim3(32), 0, stream, target_logits, K, V, nch, part, draft_tok,
+             temperature, key, w0, out_tok, accept_len, kv_src, (const Thr*)thr);
   return last_launch();
 }
 

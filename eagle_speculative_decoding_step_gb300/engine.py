@@ -67,7 +67,7 @@ class ChainStep:
     """Buffers and call sequence of one chain speculative step."""
 
     def __init__(self, dm: DeviceModel, aux: torch.Tensor, root_tok: torch.Tensor, target: torch.Tensor,
-                 temperature=None, seed=0, step_offset=0):
+                 temperature=None, seed=0, step_offset=0, top_k=None, top_p=None):
         w = dm.w
         self.dm = dm
         B, K, V = w.B, w.K, w.V
@@ -87,6 +87,7 @@ class ChainStep:
         self.temperature = temperature if temperature is not None else torch.full((B,), w.temperature,
                                                                                      device=dev)
         self.seed, self.step_offset = seed, step_offset
+        self.top_k, self.top_p = top_k, top_p
         self.vws = torch.zeros(lib.spec_verify_workspace_bytes(B, K + 1, V), dtype=torch.uint8, device=dev)
 
     def draft(self):
@@ -113,7 +114,8 @@ class ChainStep:
         w = self.dm.w
         if w.verify == "rejection":
             lib.spec_verify_rejection(self.B, self.K, self.V, self.target, self.drafts, self.temperature, self.seed,
-                                      self.step_offset, self.out, self.acc, self.kv_src, ws=self.vws)
+                                      self.step_offset, self.out, self.acc, self.kv_src, ws=self.vws,
+                                      top_k=self.top_k, top_p=self.top_p)
         else:
             lib.spec_verify_greedy(self.B, self.K + 1, self.V, self.target, self.drafts, self.out, self.acc,
                                    self.kv_src, ws=self.vws)
@@ -163,15 +165,24 @@ class TreeStep:
         lib.spec_fc_fuse(dm.desc, dm.weights, self.aux, self.h0, B, dm.ws)
         rows = lib.make_rows(B, B, 1, dm.ctx_len, self.root, step=0, max_ctx=dm.w.max_ctx)
         lib.spec_draft_layer(dm.desc, dm.weights, rows, self.h0, self.pre[0], self.hn, dm.kv, dm.ws)
-        lib.spec_lm_head(dm.desc, dm.weights, self.hn, B, k, self.ids, self.lp, ws=dm.ws)
+        self._head(B)
         lib.spec_tree_expand(B, k, 1, D, N, dm.ctx_len, self.root, self.ids, self.lp, self.state, self.io)
         for d in range(2, D + 1):
             rows = lib.make_rows(B * k, B, k, dm.ctx_len, self.f_tok, pos=self.f_pos, kv_idx=self.f_kv,
                                  mask=self.f_mask, hid_src=self.f_src, max_ctx=dm.w.max_ctx)
             src, dst = self.pre[d % 2], self.pre[(d + 1) % 2]
             lib.spec_draft_layer(dm.desc, dm.weights, rows, src, dst, self.hn, dm.kv, dm.ws)
-            lib.spec_lm_head(dm.desc, dm.weights, self.hn, B * k, k, self.ids, self.lp, ws=dm.ws)
+            self._head(B * k)
             lib.spec_tree_expand(B, k, d, D, N, dm.ctx_len, self.root, self.ids, self.lp, self.state, self.io)
+
+    def _head(self, M):
+        """top-k ids and log-probs per row: full LM head, or the EAGLE-4 candidate head
+        (log-probs over its rescored candidates)."""
+        dm, k = self.dm, self.k
+        if dm.w.rank > 0:
+            lib.spec_lowrank_candidates(dm.desc, dm.weights, self.hn, M, k, self.ids, ws=dm.ws, out_logprob=self.lp)
+        else:
+            lib.spec_lm_head(dm.desc, dm.weights, self.hn, M, k, self.ids, self.lp, ws=dm.ws)
 
     def verify(self, compact=True):
         dm = self.dm

@@ -241,11 +241,14 @@ spec_status spec_lm_head(const spec_model_desc *desc, const spec_weights *w,
  * [EAGLE4] module docstring (low-rank head retrieves, serving rescores the
  * retrieved candidates exactly) and Eagle4CandidateHeadConfig.
  * hn [M, H]; cand_ids / cand_logits [M, Kc] (score order) or NULL;
- * out_ids at [m * out_ld + j], 1 <= k_out <= 8 (out_ld 0 means k_out). */
+ * out_ids at [m * out_ld + j], 1 <= k_out <= 8 (out_ld 0 means k_out);
+ * out_logprob (same layout) or NULL: log-probability of each emitted id under
+ * the softmax over the candidates' exact logits (what a top-k draft tree ranks
+ * with when it drafts from the candidate head). */
 spec_status spec_lowrank_candidates(const spec_model_desc *desc, const spec_weights *w,
                                     const void *hn, int32_t M, int32_t k_out,
                                     int32_t *cand_ids, float *cand_logits,
-                                    int32_t *out_ids, int32_t out_ld,
+                                    int32_t *out_ids, float *out_logprob, int32_t out_ld,
                                     void *ws, size_t ws_bytes, spec_stream_t stream);
 
 /* ------------------------------------------------------------------ */
@@ -316,9 +319,15 @@ spec_status spec_verify_greedy(int32_t B, int32_t R, int32_t V, const float *tar
  * (b, i) (first word of block 0), purpose 1 -> noise of vocabulary id 4j+l
  * (word l of block j); u = ((x >> 8) + 0.5) * 2^-24.
  * target_logits [B, K+1, V] fp32, draft_tok [B, K], out_tok [B, K+1],
- * accept_len [B], kv_src [B, K+1] (as the greedy chain) or NULL. */
+ * accept_len [B], kv_src [B, K+1] (as the greedy chain) or NULL.
+ * top_k [B] (0 = off) and top_p [B] (1.0 = off), each NULL for none, filter the
+ * target distribution per request before the accept test and both samples
+ * ([NEURON] "Rejection Sampling": per-request top-k and top-p): tokens ordered
+ * by logit / T (ties to the smaller id), the first top_k kept, then the
+ * shortest prefix of those whose renormalised mass reaches top_p. */
 spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, const float *target_logits,
                                   const int32_t *draft_tok, const float *temperature,
+                                  const int32_t *top_k, const float *top_p,
                                   uint64_t seed, uint64_t step_offset, int32_t *out_tok,
                                   int32_t *accept_len, int32_t *kv_src,
                                   void *ws, size_t ws_bytes, spec_stream_t stream);

@@ -183,7 +183,7 @@ def lm_head(desc, W, hn, k):
     return ids, lp, lse, logits
 
 
-def lowrank_candidates(desc, W, hn, num_candidates, k_out):
+def lowrank_candidates(desc, W, hn, num_candidates, k_out, with_logprob=False):
     """EAGLE-4 candidate head: low-rank scores retrieve candidates, the full
     lm_head rescores them exactly ([EAGLE4] module docstring and
     Eagle4CandidateHeadConfig: s = (hn @ down^T) @ up^T with down [r, H] and
@@ -203,7 +203,13 @@ def lowrank_candidates(desc, W, hn, num_candidates, k_out):
     for m in range(M):
         exact[m] = Wl[cand[m]] @ _f64(hn[m])
     out = np.empty((M, k_out), dtype=np.int64)
+    out_lp = np.empty((M, k_out), dtype=np.float64)
     for m in range(M):
         order = np.lexsort((cand[m], -exact[m].astype(np.float32)))
         out[m] = cand[m][order[:k_out]]
+        # log-probs under the softmax over the candidates (tree drafting from the
+        # candidate head ranks children with these)
+        out_lp[m] = exact[m][order[:k_out]] - logsumexp(exact[m])
+    if with_logprob:
+        return cand, exact, out, out_lp
     return cand, exact, out

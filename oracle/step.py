@@ -64,7 +64,12 @@ def tree_draft(desc, W, aux, root_tok, ctx_len, kv, top_k, depth, total, trace=N
     hid_in = h0
     for d in range(1, depth + 1):
         prenorm, hn = draft.draft_layer(desc, W, rows, hid_in, kv)
-        ids, lp, _, _ = draft.lm_head(desc, W, hn, top_k)
+        if desc.rank > 0:
+            # EAGLE-4 candidate head drafting a tree: top-k of the rescored candidates,
+            # log-probs under the softmax over the candidates
+            _, _, ids, lp = draft.lowrank_candidates(desc, W, hn, desc.num_candidates, top_k, with_logprob=True)
+        else:
+            ids, lp, _, _ = draft.lm_head(desc, W, hn, top_k)
         if trace is not None:
             trace.append((rows, hid_in, ids, lp))
         res = tree.tree_expand(st, d, ids, lp)

@@ -118,13 +118,45 @@ def compact_kv(kv, ctx_len, kv_src, accept_len):
             kv["v"][t] = kv["v"][s]
 
 
-def verify_rejection(target, drafts, temperature, seed, step_offset=0):
+def kept_set(l, top_k=0, top_p=1.0):
+    """Tokens kept by top-k then top-p filtering of the logits ``l`` (already divided
+    by the temperature).  [NEURON] "Rejection Sampling": the CPU sampler supports
+    per-request top-k and top-p.  Reading (the page gives only the names): order
+    tokens by logit, larger first, ties to the smaller id; top-k keeps the first k;
+    top-p then keeps the shortest prefix of those whose renormalised probability
+    mass reaches top_p.  Returns (boolean mask, top-p margin), the margin being the
+    distance of the deciding cumulative mass from top_p (for near-tie accounting).
+    """
+    l = np.asarray(l, dtype=np.float64)
+    V = l.shape[0]
+    order = np.lexsort((np.arange(V), -l))
+    n = V
+    if top_k and 0 < int(top_k) < V:
+        n = int(top_k)
+    keep = order[:n]
+    margin = np.inf
+    if top_p is not None and float(top_p) < 1.0:
+        p = np.exp(l[keep] - logsumexp(l[keep]))
+        c = np.cumsum(p)
+        m = int(np.searchsorted(c, float(top_p))) + 1
+        m = min(m, n)
+        margin = min(abs(c[m - 1] - top_p), abs(c[m - 2] - top_p) if m >= 2 else np.inf)
+        keep = keep[:m]
+    mask = np.zeros(V, dtype=bool)
+    mask[keep] = True
+    return mask, margin
+
+
+def verify_rejection(target, drafts, temperature, seed, step_offset=0, top_k=None, top_p=None):
     """Probabilistic verification of a greedy-drafted chain.
 
-    target [B, K+1, V] float32, drafts [B, K], temperature [B].  Returns
-    (out [B, K+1], accept_len [B], info) where info holds per (b, i) the
-    acceptance margin u - p(draft) and, for the emitted sampled token, the gap
-    between the best and second-best Gumbel keys (for near-tie accounting).
+    target [B, K+1, V] float32, drafts [B, K], temperature [B]; optional per
+    request top_k [B] (0 = off) and top_p [B] (1.0 = off) restrict the target
+    distribution (see ``kept_set``) before the accept test, the recovered
+    sample and the bonus sample.  Returns (out [B, K+1], accept_len [B], info)
+    where info holds per (b, i) the acceptance margin u - p(draft), for the
+    emitted sampled token the gap between the best and second-best Gumbel keys,
+    and the smallest top-p margin met (for near-tie accounting).
     """
     target = np.asarray(target, dtype=np.float64)
     drafts = np.asarray(drafts, dtype=np.int64)
@@ -134,6 +166,9 @@ def verify_rejection(target, drafts, temperature, seed, step_offset=0):
     acc = np.zeros(B, dtype=np.int64)
     margins = np.full((B, K), np.inf)
     gaps = np.full(B, np.inf)
+    p_margins = np.full(B, np.inf)
+    tk = np.zeros(B, dtype=np.int64) if top_k is None else np.asarray(top_k, dtype=np.int64)
+    tp = np.ones(B) if top_p is None else np.asarray(top_p, dtype=np.float64)
     for b in range(B):
         T = float(temperature[b])
         a = 0
@@ -150,7 +185,9 @@ def verify_rejection(target, drafts, temperature, seed, step_offset=0):
                 emitted = tgt
                 break
             l = row / T
-            p_d = np.exp(l[d] - logsumexp(l))
+            kept, pm = kept_set(l, tk[b], tp[b])
+            p_margins[b] = min(p_margins[b], pm)
+            p_d = np.exp(l[d] - logsumexp(l[kept])) if kept[d] else 0.0
             u = philox.accept_uniform(seed, step_offset, b, a)
             margins[b, a] = u - p_d
             if u <= p_d:
@@ -158,6 +195,7 @@ def verify_rejection(target, drafts, temperature, seed, step_offset=0):
                 a += 1
                 continue
             key = l - np.log(-np.log(philox.noise_uniforms(seed, step_offset, b, a, V)))
+            key[~kept] = -np.inf
             key[d] = -np.inf
             emitted, gaps[b] = _best(key)
             break
@@ -166,11 +204,15 @@ def verify_rejection(target, drafts, temperature, seed, step_offset=0):
             if T <= 0.0:
                 emitted = int(argmax_first(row.astype(np.float32)))
             else:
-                key = row / T - np.log(-np.log(philox.noise_uniforms(seed, step_offset, b, K, V)))
+                l = row / T
+                kept, pm = kept_set(l, tk[b], tp[b])
+                p_margins[b] = min(p_margins[b], pm)
+                key = l - np.log(-np.log(philox.noise_uniforms(seed, step_offset, b, K, V)))
+                key[~kept] = -np.inf
                 emitted, gaps[b] = _best(key)
         out[b, a] = emitted
         acc[b] = a
-    return out, acc, {"accept_margin": margins, "sample_gap": gaps}
+    return out, acc, {"accept_margin": margins, "sample_gap": gaps, "top_p_margin": p_margins}
 
 
 def _best(key):

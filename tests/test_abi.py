@@ -86,15 +86,15 @@ def test_host_checks_reject_before_launch(so):
     assert _status("spec_lm_head", ctypes.byref(d), ctypes.byref(wt), FAKE, 4, 9, FAKE, 0, FAKE, None, None,
                    FAKE, 1 << 40, None) == -2
     # low-rank head on a model without one
-    assert _status("spec_lowrank_candidates", ctypes.byref(d), ctypes.byref(wt), FAKE, 4, 1, None, None, FAKE, 0,
-                   FAKE, 1 << 40, None) == -3
+    assert _status("spec_lowrank_candidates", ctypes.byref(d), ctypes.byref(wt), FAKE, 4, 1, None, None, FAKE, None,
+                   0, FAKE, 1 << 40, None) == -3
     # verifiers
     assert _status("spec_verify_greedy", 2, 70, 100, FAKE, FAKE, None, 0, FAKE, FAKE, None, None, None, None,
                    FAKE, 1 << 40, None) == -4            # more than 64 rows per request
     assert _status("spec_verify_greedy", 2, 6, 100, FAKE, FAKE, None, 0, FAKE, FAKE, None, None, None, None,
                    FAKE, 8, None) == -8                  # workspace too small
-    assert _status("spec_verify_rejection", 2, 0, 100, FAKE, FAKE, FAKE, 0, 0, FAKE, FAKE, None, FAKE, 1 << 40,
-                   None) == -2
+    assert _status("spec_verify_rejection", 2, 0, 100, FAKE, FAKE, FAKE, None, None, 0, 0, FAKE, FAKE, None, FAKE,
+                   1 << 40, None) == -2
     # tree capacity
     io = lib.TreeIO(*([FAKE] * 11))
     assert _status("spec_tree_expand", 1, 8, 1, 9, 31, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(io), None) == -4

