@@ -37,6 +37,23 @@ def _peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def max_over_ranks(ms, dist, device="cpu"):
+    """The slowest rank's time (barrier-bracketed timing of independent replicas).
+    Works for nccl (device tensors) and gloo (host tensors)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_steps_per_s(world, ms_step):
+    """Whole-job steps/s: every rank ran its own replica for the same number of
+    steps, bounded by the slowest rank."""
+    return world * 1000.0 / ms_step
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -248,11 +265,7 @@ def run_gpu(args, w):
     if dist is not None:
         dist.barrier()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, device)
     ms_step = ms / args.steps
     acc = st.acc.cpu().numpy()
     verified = float((acc + 1).sum())
@@ -304,7 +317,7 @@ def run_gpu(args, w):
     total_bytes, lm_bytes = step_bytes(w)
     lm_gbs = lm_bytes / (lm_ms * 1e-3) / 1e9
     res = {
-        "metric": METRIC, "value": world * 1000.0 / ms_step, "unit": "steps/s", "n_gpus": world,
+        "metric": METRIC, "value": aggregate_steps_per_s(world, ms_step), "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded random-init weights, N(0,1) aux states and context K/V)",
         "config": {"workload": w.name, "H": w.H, "heads": [w.nq, w.nkv], "head_dim": w.hd, "I": w.I, "V": w.V,
