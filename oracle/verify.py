@@ -147,13 +147,15 @@ def kept_set(l, top_k=0, top_p=1.0):
     return mask, margin
 
 
-def verify_rejection(target, drafts, temperature, seed, step_offset=0, top_k=None, top_p=None):
+def verify_rejection(target, drafts, temperature, seed, step_offset=0, top_k=None, top_p=None, req_ids=None):
     """Probabilistic verification of a greedy-drafted chain.
 
     target [B, K+1, V] float32, drafts [B, K], temperature [B]; optional per
     request top_k [B] (0 = off) and top_p [B] (1.0 = off) restrict the target
     distribution (see ``kept_set``) before the accept test, the recovered
-    sample and the bonus sample.  Returns (out [B, K+1], accept_len [B], info)
+    sample and the bonus sample.  ``req_ids`` [B] are the requests' indices in the
+    batch (the Philox counter's request word; default 0..B-1), for checking a
+    sample of a larger batch.  Returns (out [B, K+1], accept_len [B], info)
     where info holds per (b, i) the acceptance margin u - p(draft), for the
     emitted sampled token the gap between the best and second-best Gumbel keys,
     and the smallest top-p margin met (for near-tie accounting).
@@ -169,6 +171,7 @@ def verify_rejection(target, drafts, temperature, seed, step_offset=0, top_k=Non
     p_margins = np.full(B, np.inf)
     tk = np.zeros(B, dtype=np.int64) if top_k is None else np.asarray(top_k, dtype=np.int64)
     tp = np.ones(B) if top_p is None else np.asarray(top_p, dtype=np.float64)
+    rid = np.arange(B) if req_ids is None else np.asarray(req_ids, dtype=np.int64)
     for b in range(B):
         T = float(temperature[b])
         a = 0
@@ -188,13 +191,13 @@ def verify_rejection(target, drafts, temperature, seed, step_offset=0, top_k=Non
             kept, pm = kept_set(l, tk[b], tp[b])
             p_margins[b] = min(p_margins[b], pm)
             p_d = np.exp(l[d] - logsumexp(l[kept])) if kept[d] else 0.0
-            u = philox.accept_uniform(seed, step_offset, b, a)
+            u = philox.accept_uniform(seed, step_offset, int(rid[b]), a)
             margins[b, a] = u - p_d
             if u <= p_d:
                 out[b, a] = d
                 a += 1
                 continue
-            key = l - np.log(-np.log(philox.noise_uniforms(seed, step_offset, b, a, V)))
+            key = l - np.log(-np.log(philox.noise_uniforms(seed, step_offset, int(rid[b]), a, V)))
             key[~kept] = -np.inf
             key[d] = -np.inf
             emitted, gaps[b] = _best(key)
@@ -207,7 +210,7 @@ def verify_rejection(target, drafts, temperature, seed, step_offset=0, top_k=Non
                 l = row / T
                 kept, pm = kept_set(l, tk[b], tp[b])
                 p_margins[b] = min(p_margins[b], pm)
-                key = l - np.log(-np.log(philox.noise_uniforms(seed, step_offset, b, K, V)))
+                key = l - np.log(-np.log(philox.noise_uniforms(seed, step_offset, int(rid[b]), K, V)))
                 key[~kept] = -np.inf
                 emitted, gaps[b] = _best(key)
         out[b, a] = emitted

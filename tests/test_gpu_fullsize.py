@@ -67,7 +67,8 @@ def test_chain_full_size(name, sample):
     out = st.out.cpu().numpy()[idx]
     acc = st.acc.cpu().numpy()[idx]
     if w.verify == "rejection":
-        ref_out, ref_acc, info = overify.verify_rejection(target[idx], drafts_ref, temp[idx], w.philox_seed, 0)
+        ref_out, ref_acc, info = overify.verify_rejection(target[idx], drafts_ref, temp[idx], w.philox_seed, 0,
+                                                          req_ids=idx)
     else:
         ref_out, ref_acc, info = overify.verify_greedy_chain(target[idx], drafts_ref)
     compared = 0
