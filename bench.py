@@ -219,6 +219,8 @@ def run_gpu(args, w):
 
     t0 = time.time()
     W = synth.make_weights(w)
+    if w.rank > 0:
+        W["lr_down"], W["lr_up"] = synth.lowrank_factors(W["lm_head"], w.rank, w.dtype)
     ctx = synth.context_lengths(w)
     kv = synth.make_kv(w, ctx)
     aux = synth.make_aux(w)

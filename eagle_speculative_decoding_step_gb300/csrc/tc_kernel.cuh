@@ -14,6 +14,7 @@ namespace tc {
 struct Seg {
   int mat, row0, k0, k1, idx;
   int lo, hi;   // weight rows [lo, hi) of the tile this segment is responsible for
+  int keep;     // the next segment re-reads part of this tile: keep it in L2
 };
 
 // stream-K over tiles x chunks (see SKPlan)
@@ -33,6 +34,7 @@ struct SchedSK {
     s.idx = idx++;
     s.lo = s.row0;
     s.hi = s.row0 + 128;
+    s.keep = 0;
     it = se;
     return true;
   }
@@ -64,6 +66,8 @@ struct SchedRows {
     s.idx = t;
     s.lo = st;
     s.hi = min(st + 128, v1);
+    // the last tile is shifted back to end at v1 and overlaps this one
+    s.keep = (t == nt - 2) && ((v1 - v0) % 128 != 0);
     ++t;
     return true;
   }
@@ -197,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sa = su32(smem + (size_t)primed * C::kStage);
         const uint32_t fb = full0 + 8 * primed;
         mbar_expect_tx(fb, C::kStage);
-        tma_load_2d(sa, ta, fb, kk * kBK, sg.row0, pw);
+        tma_load_2d(sa, ta, fb, kk * kBK, sg.row0, sg.keep ? px : pw);
         pending[primed] = 0;
         pk[primed] = kk;
         ++primed;
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = su32(smem + (size_t)stage * C::kStage);
           const uint32_t fb = full0 + 8 * stage;
           mbar_expect_tx(fb, C::kStage);
-          tma_load_2d(sa, ta, fb, kk * kBK, sg.row0, pw);
+          tma_load_2d(sa, ta, fb, kk * kBK, sg.row0, sg.keep ? px : pw);
 #pragma unroll
           for (int j = 0; j < C::kBLoads; ++j)
             tma_load_2d(sa + kABytes + j * C::kBBox * 128, &tB, fb, kk * kBK, j * C::kBBox, px);
