@@ -6,14 +6,18 @@
 // draft_top_k.
 //
 // logits = hn @ lm_head^T is never written: each CTA of the tensor-core
-// kernel owns a contiguous vocabulary range (one CTA per SM), and its epilogue
-// warps fold every 128-row tile straight out of TMEM into per-row running
-// statistics -- online max / sum of exp (log-sum-exp) and a sorted top-KT list
-// -- held in registers by the lane that owns the row (row m -> lane m % 32).
-// A candidate only enters a list if it beats the list's current last entry, so
-// after the first tiles a tile costs two warp reductions per row.  At the end
-// the four epilogue warps merge through shared memory and write one partial
-// per (CTA, row); a small kernel merges the partials of all CTAs.
+// kernel owns a contiguous vocabulary range (one CTA per SM) and its four
+// epilogue warps fold every 128-row tile out of TMEM into running per-row
+// statistics: online max / sum of exp (log-sum-exp) and the top-KT.  A tile is
+// first transposed through shared memory ([m][128]), so that row m belongs to
+// one warp (m = 4 j + warp) and each lane folds four consecutive vocabulary ids
+// of it: the running max / sum-exp and, for k = 1, the best (value, id) are
+// per lane and need no cross-lane work until the CTA's last tile.  For k > 1
+// the row's sorted list lives in lanes 0..KT-1 of the owning warp (lane q holds
+// entry q), every lane caches entry KT-1, and cross-lane work happens only for
+// a value that beats it -- one list per row and CTA, so few values do.  At the
+// end each warp writes one record per (CTA, row) it owns; a small kernel
+// merges the records of all CTAs.
 #include "tc_kernel.cuh"
 
 namespace spec {
@@ -23,166 +27,172 @@ constexpr int kLmMaxMpad = 64;
 
 template <int MPAD, int KT>
 struct EpiStats {
-  static constexpr int NS = (MPAD + 31) / 32;     // rows owned per lane
+  static_assert(KT >= 1 && KT <= 32, "list spread over the lanes of one warp");
+  static constexpr int R = MPAD / 4;              // rows per warp: m = 4 j + warp
   static constexpr int REC = 2 + 2 * KT;          // floats per (CTA, row) record
+  // two mbarriers (tile written, tile read), then the transposed tile [MPAD][128]
+  static constexpr int kScratch = 128 + MPAD * 128 * 4;
   struct Params {
     int M;
     float* out;      // [G][MPAD][REC]
   };
   const Params& P;
   int c;
-  float RM[NS], RS[NS], TV[NS][KT];
-  int TI[NS][KT];
+  uint32_t bar_w, bar_r;
+  float* S;
+  volatile int* abort;
+  int t = 0;                  // tiles folded so far
+  float RM[R], RS[R];         // this lane's running max / sum of exp(x - max)
+  float LV[R];                // k = 1: this lane's best; k > 1: list entry `lane`
+  int LI[R];
+  float TV[R];                // k > 1: list entry KT-1 (admission threshold)
+  int TI[R];
 
-  SPEC_DEV EpiStats(const Params& pp, int cc) : P(pp), c(cc) {
+  static SPEC_DEV void init(uint8_t* scratch) {
+    mbar_init(su32(scratch), 4);
+    mbar_init(su32(scratch + 8), 4);
+  }
+  SPEC_DEV EpiStats(const Params& pp, int cc, uint8_t* scratch, volatile int* ab) : P(pp), c(cc), abort(ab) {
+    bar_w = su32(scratch);
+    bar_r = su32(scratch + 8);
+    S = reinterpret_cast<float*>(scratch + 128);
 #pragma unroll
-    for (int s = 0; s < NS; ++s) {
-      RM[s] = -INFINITY;
-      RS[s] = 0.f;
-#pragma unroll
-      for (int q = 0; q < KT; ++q) { TV[s][q] = -INFINITY; TI[s][q] = 0x7fffffff; }
+    for (int j = 0; j < R; ++j) {
+      RM[j] = -INFINITY;
+      RS[j] = 0.f;
+      LV[j] = -INFINITY;
+      LI[j] = 0x7fffffff;
+      TV[j] = -INFINITY;
+      TI[j] = 0x7fffffff;
     }
   }
 
-  // sorted insert (descending value, ascending id) into list s of this lane
-  template <int s> SPEC_DEV void insert(float v, int i) {
+  // TMEM -> shared memory, transposed; invalid vocabulary rows become -inf
+  SPEC_DEV bool segment(const Seg& sg, uint32_t tb, int warp, int lane) {
+    const int r = warp * 32 + lane;
+    const int vid = sg.row0 + r;
+    const bool valid = vid >= sg.lo && vid < sg.hi;
 #pragma unroll
-    for (int q = KT - 1; q >= 0; --q) {
-      if (better(v, i, TV[s][q], TI[s][q])) {
-        if (q > 0 && better(v, i, TV[s][q - 1], TI[s][q - 1])) {
-          TV[s][q] = TV[s][q - 1];
-          TI[s][q] = TI[s][q - 1];
-        } else {
-          TV[s][q] = v;
-          TI[s][q] = i;
+    for (int c16 = 0; c16 < MPAD / 16; ++c16) {
+      if (c16 * 16 >= P.M) break;
+      uint32_t x[16];
+      tmem_ld16(tb + (uint32_t)(c16 * 16), x);
+      tmem_ld_wait();
+      // every warp has read the previous tile
+      if (c16 == 0 && t > 0 && !mbar_wait(bar_r, (uint32_t)((t - 1) & 1), abort)) return false;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int m = c16 * 16 + q;
+        if (m < P.M) S[m * 128 + r] = valid ? __uint_as_float(x[q]) : -INFINITY;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_w);
+    return true;
+  }
+
+  SPEC_DEV float comp(const float4& x, int q) { return q == 0 ? x.x : (q == 1 ? x.y : (q == 2 ? x.z : x.w)); }
+
+  SPEC_DEV bool after(const Seg& sg, int warp, int lane) {
+    if (!mbar_wait(bar_w, (uint32_t)(t & 1), abort)) return false;
+    const int id0 = sg.row0 + 4 * lane;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int m = 4 * j + warp;
+      if (m >= P.M) break;
+      const float4 x = *reinterpret_cast<const float4*>(S + m * 128 + 4 * lane);
+      const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+      if (mx > -INFINITY) {
+        const float nm = fmaxf(RM[j], mx);
+        RS[j] = RS[j] * expf(RM[j] - nm) + (expf(x.x - nm) + expf(x.y - nm)) + (expf(x.z - nm) + expf(x.w - nm));
+        RM[j] = nm;
+      }
+      if constexpr (KT == 1) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (better(comp(x, q), id0 + q, LV[j], LI[j])) { LV[j] = comp(x, q); LI[j] = id0 + q; }
+      } else {
+        unsigned cm = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (comp(x, q) > -INFINITY && better(comp(x, q), id0 + q, TV[j], TI[j])) cm |= 1u << q;
+        while (__any_sync(0xffffffffu, cm != 0)) {
+          // this lane's best candidate, then the warp's
+          float bv = -INFINITY;
+          int bi = 0x7fffffff, bq = -1;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (((cm >> q) & 1u) && better(comp(x, q), id0 + q, bv, bi)) { bv = comp(x, q); bi = id0 + q; bq = q; }
+          float wv = bv;
+          int wi = bi;
+          warp_argmax(wv, wi);
+          if (bq >= 0 && bi == wi) cm &= ~(1u << bq);
+          // sorted insert into the list held by lanes 0..KT-1
+          const bool ahead = lane < KT && better(LV[j], LI[j], wv, wi);
+          const int pos = __popc(__ballot_sync(0xffffffffu, ahead));
+          const float uv = __shfl_up_sync(0xffffffffu, LV[j], 1);
+          const int ui = __shfl_up_sync(0xffffffffu, LI[j], 1);
+          if (lane == pos) {
+            LV[j] = wv;
+            LI[j] = wi;
+          } else if (lane > pos && lane < KT) {
+            LV[j] = uv;
+            LI[j] = ui;
+          }
+          TV[j] = __shfl_sync(0xffffffffu, LV[j], KT - 1);
+          TI[j] = __shfl_sync(0xffffffffu, LI[j], KT - 1);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (((cm >> q) & 1u) && !better(comp(x, q), id0 + q, TV[j], TI[j])) cm &= ~(1u << q);
         }
       }
     }
-  }
-
-  template <int m> SPEC_DEV void column(float x, bool valid, int vid, int lane) {
-    constexpr int s = m >> 5;
-    constexpr int owner = m & 31;
-    const float xv = valid ? x : -INFINITY;
-    const float wm = warp_max(xv);
-    if (wm > -INFINITY) {
-      const float e = valid ? expf(xv - wm) : 0.f;
-      const float se = warp_sum(e);
-      if (lane == owner) {
-        const float nm = fmaxf(RM[s], wm);
-        RS[s] = RS[s] * expf(RM[s] - nm) + se * expf(wm - nm);
-        RM[s] = nm;
-      }
-    }
-    float thr = __shfl_sync(0xffffffffu, TV[s][KT - 1], owner);
-    int thri = __shfl_sync(0xffffffffu, TI[s][KT - 1], owner);
-    bool cand = valid && better(xv, vid, thr, thri);
-    while (__any_sync(0xffffffffu, cand)) {
-      float bv = cand ? xv : -INFINITY;
-      int bi = cand ? vid : 0x7fffffff;
-      warp_argmax(bv, bi);
-      if (lane == owner) insert<s>(bv, bi);
-      if (vid == bi) cand = false;
-      thr = __shfl_sync(0xffffffffu, TV[s][KT - 1], owner);
-      thri = __shfl_sync(0xffffffffu, TI[s][KT - 1], owner);
-      cand = cand && better(xv, vid, thr, thri);
-    }
-  }
-
-  template <int c16> SPEC_DEV void chunk(uint32_t tb, bool valid, int vid, int lane) {
-    if (c16 * 16 >= P.M) return;
-    uint32_t r[16];
-    tmem_ld16(tb + (uint32_t)(c16 * 16), r);
-    tmem_ld_wait();
-    unroll_cols<c16 * 16>(r, valid, vid, lane);
-  }
-  template <int m0> SPEC_DEV void unroll_cols(const uint32_t* r, bool valid, int vid, int lane) {
-    if constexpr (m0 < MPAD) {
-      if (m0 < P.M) {
-        column<m0>(__uint_as_float(r[m0 & 15]), valid, vid, lane);
-        if constexpr (((m0 + 1) & 15) != 0) unroll_cols<m0 + 1>(r, valid, vid, lane);
-      }
-    }
-  }
-  template <int c16> SPEC_DEV void chunks(uint32_t tb, bool valid, int vid, int lane) {
-    if constexpr (c16 * 16 < MPAD) {
-      chunk<c16>(tb, valid, vid, lane);
-      chunks<c16 + 1>(tb, valid, vid, lane);
-    }
-  }
-
-  SPEC_DEV void segment(const Seg& sg, uint32_t tb, int warp, int lane) {
-    const int vid = sg.row0 + warp * 32 + lane;
-    const bool valid = vid >= sg.lo && vid < sg.hi;
-    chunks<0>(tb, valid, vid, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_r);
+    ++t;
+    return true;
   }
 
   SPEC_DEV void finish(int warp, int lane) {
-    __shared__ float sh[4][MPAD][REC];
 #pragma unroll
-    for (int s = 0; s < NS; ++s) {
-      const int m = 32 * s + lane;
-      if (m < MPAD) {
-        sh[warp][m][0] = RM[s];
-        sh[warp][m][1] = RS[s];
-#pragma unroll
-        for (int q = 0; q < KT; ++q) {
-          sh[warp][m][2 + q] = TV[s][q];
-          sh[warp][m][2 + KT + q] = __int_as_float(TI[s][q]);
-        }
-      }
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (warp != 0) return;
-#pragma unroll
-    for (int s = 0; s < NS; ++s) {
-      const int m = 32 * s + lane;
-      if (m >= P.M) continue;
-      float M_ = -INFINITY;
-      for (int w = 0; w < 4; ++w) M_ = fmaxf(M_, sh[w][m][0]);
-      float S_ = 0.f;
-      for (int w = 0; w < 4; ++w)
-        if (sh[w][m][0] > -INFINITY) S_ += sh[w][m][1] * expf(sh[w][m][0] - M_);
-      for (int w = 1; w < 4; ++w)
-        for (int q = 0; q < KT; ++q) {
-          const float v = sh[w][m][2 + q];
-          const int i = __float_as_int(sh[w][m][2 + KT + q]);
-          if (better(v, i, TV[s][KT - 1], TI[s][KT - 1])) insert_rt(s, v, i);
-        }
+    for (int j = 0; j < R; ++j) {
+      const int m = 4 * j + warp;
+      if (m >= P.M) break;
+      const float M_ = warp_max(RM[j]);
+      const float S_ = warp_sum(RM[j] > -INFINITY ? RS[j] * expf(RM[j] - M_) : 0.f);
       float* o = P.out + ((size_t)c * MPAD + m) * REC;
-      o[0] = M_;
-      o[1] = S_;
-      for (int q = 0; q < KT; ++q) {
-        o[2 + q] = TV[s][q];
-        o[2 + KT + q] = __int_as_float(TI[s][q]);
-      }
-    }
-  }
-  SPEC_DEV void insert_rt(int s, float v, int i) {
-#pragma unroll
-    for (int ss = 0; ss < NS; ++ss)
-      if (ss == s) {
-#pragma unroll
-        for (int q = KT - 1; q >= 0; --q) {
-          if (better(v, i, TV[ss][q], TI[ss][q])) {
-            if (q > 0 && better(v, i, TV[ss][q - 1], TI[ss][q - 1])) {
-              TV[ss][q] = TV[ss][q - 1];
-              TI[ss][q] = TI[ss][q - 1];
-            } else {
-              TV[ss][q] = v;
-              TI[ss][q] = i;
-            }
-          }
+      if constexpr (KT == 1) {
+        float v = LV[j];
+        int i = LI[j];
+        warp_argmax(v, i);
+        if (lane == 0) {
+          o[0] = M_;
+          o[1] = S_;
+          o[2] = v;
+          o[3] = __int_as_float(i);
+        }
+      } else {
+        if (lane == 0) {
+          o[0] = M_;
+          o[1] = S_;
+        }
+        if (lane < KT) {
+          o[2 + lane] = LV[j];
+          o[2 + KT + lane] = __int_as_float(LI[j]);
         }
       }
+    }
   }
 };
 
 }  // namespace tc
 
-// Merge the per-CTA records of row m: lse (whole block) and the k best (warp 0:
-// every lane keeps a sorted top-KT of the records it scans, then k rounds of a
-// warp argmax over the lanes' heads).
+// Merge the per-CTA records of row m: lse (whole block) and the k best (the
+// records' lists are staged in shared memory; warp 0: every lane keeps a sorted
+// top-KT of the entries it scans, then k rounds of a warp argmax over the
+// lanes' heads).
+constexpr int kLmMaxCtas = 256;
+
 template <int KT>
 __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__ part, int G, int mpad, int k,
                                                        int32_t* __restrict__ ids, int ld_ids,
@@ -192,17 +202,23 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__
   pdl_trigger();
   constexpr int REC = 2 + 2 * KT;
   __shared__ float red[32];
-  __shared__ float s_lse;
+  __shared__ float cv[kLmMaxCtas * KT];
+  __shared__ int ci[kLmMaxCtas * KT];
   const int m = blockIdx.x;
   float mx = -INFINITY;
   for (int c = threadIdx.x; c < G; c += blockDim.x) mx = fmaxf(mx, part[((size_t)c * mpad + m) * REC]);
+  for (int e = threadIdx.x; e < G * KT; e += blockDim.x) {
+    const float* r = part + ((size_t)(e / KT) * mpad + m) * REC;
+    cv[e] = r[2 + e % KT];
+    ci[e] = __float_as_int(r[2 + KT + e % KT]);
+  }
   mx = block_max(mx, red);
   float s = 0.f;
   for (int c = threadIdx.x; c < G; c += blockDim.x) {
     const float* r = part + ((size_t)c * mpad + m) * REC;
     if (r[0] > -INFINITY) s += r[1] * expf(r[0] - mx);
   }
-  s = block_sum(s, red);
+  s = block_sum(s, red);      // its barriers also publish cv / ci
   const float lse = mx + logf(s);
   if (threadIdx.x >= 32) return;
   const int lane = threadIdx.x;
@@ -211,9 +227,8 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__
 #pragma unroll
   for (int q = 0; q < KT; ++q) { tv[q] = -INFINITY; ti[q] = 0x7fffffff; }
   for (int e = lane; e < G * KT; e += 32) {
-    const float* r = part + ((size_t)(e / KT) * mpad + m) * REC;
-    const float v = r[2 + e % KT];
-    const int i = __float_as_int(r[2 + KT + e % KT]);
+    const float v = cv[e];
+    const int i = ci[e];
     if (!better(v, i, tv[KT - 1], ti[KT - 1])) continue;
 #pragma unroll
     for (int q = KT - 1; q >= 0; --q) {
@@ -271,6 +286,7 @@ spec_status launch_lm_head_fused(const spec_model_desc& d, const void* hn, const
   const int mpad = tc_mpad(M);
   int G = sm_count();
   if (G > (V + 127) / 128) G = (V + 127) / 128;
+  if (G > kLmMaxCtas) G = kLmMaxCtas;
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + part_off);
   CUtensorMap a[3];
   if (!make_map(&a[0], lm_head, V, H, 128)) return SPEC_ERR_CUDA;

@@ -20,11 +20,12 @@ constexpr int kBK = 64;                          // K elements per chunk (128 B 
 constexpr int kABytes = 128 * kBK * 2;           // A stage: 128 rows x 128 B
 constexpr uint64_t kWaitNs = 2000000000ull;      // bounded waits: 2 s
 
-template <int MPAD> struct Cfg {
+// EXTRA: bytes of dynamic shared memory the epilogue claims after the stage ring
+template <int MPAD, int EXTRA = 0> struct Cfg {
   static_assert(MPAD % 16 == 0 && MPAD <= 384, "activation tile rows");
   static constexpr int kBBytes = MPAD * kBK * 2;
   static constexpr int kStage = kABytes + kBBytes;
-  static constexpr int kBudget = MPAD > 256 ? 212 * 1024 : 196 * 1024;
+  static constexpr int kBudget = (MPAD > 256 ? 212 * 1024 : 196 * 1024) - EXTRA;
   static constexpr int kStages = kBudget / kStage > 10 ? 10 : kBudget / kStage;
   // two TMEM accumulators (MMA of the next segment overlaps the drain of the
   // previous one) when they fit in TMEM's 512 columns, else one
@@ -37,7 +38,7 @@ template <int MPAD> struct Cfg {
   // MMA N per instruction: MPAD, or 256 + the remainder above 256
   static constexpr int kN0 = MPAD <= 256 ? MPAD : 256;
   static constexpr int kN1 = MPAD - kN0;
-  static constexpr size_t kSmem = (size_t)kStages * kStage + 1024 + 256;
+  static constexpr size_t kSmem = (size_t)kStages * kStage + 1024 + 256 + EXTRA;
 };
 
 SPEC_DEV uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }

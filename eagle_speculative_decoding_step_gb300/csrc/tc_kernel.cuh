@@ -84,8 +84,11 @@ struct EpiPartial {
   };
   const Params& P;
   int c;
-  SPEC_DEV EpiPartial(const Params& pp, int cc) : P(pp), c(cc) {}
-  SPEC_DEV void segment(const Seg& s, uint32_t tb, int warp, int lane) {
+  static constexpr int kScratch = 0;
+  static SPEC_DEV void init(uint8_t*) {}
+  SPEC_DEV EpiPartial(const Params& pp, int cc, uint8_t*, volatile int*) : P(pp), c(cc) {}
+  SPEC_DEV bool after(const Seg&, int, int) { return true; }
+  SPEC_DEV bool segment(const Seg& s, uint32_t tb, int warp, int lane) {
     float* dst = P.part + sk_slot(P.p, c, s.idx) + warp * 32 + lane;
 #pragma unroll
     for (int c16 = 0; c16 < MPAD / 16; ++c16) {
@@ -99,6 +102,7 @@ struct EpiPartial {
         if (m < P.M) dst[(size_t)m * 128] = __uint_as_float(r[q]);
       }
     }
+    return true;
   }
   SPEC_DEV void finish(int, int) {}
 };
@@ -113,8 +117,11 @@ struct EpiStore {
     float* out;
   };
   const Params& P;
-  SPEC_DEV EpiStore(const Params& pp, int) : P(pp) {}
-  SPEC_DEV void segment(const Seg& s, uint32_t tb, int warp, int lane) {
+  static constexpr int kScratch = 0;
+  static SPEC_DEV void init(uint8_t*) {}
+  SPEC_DEV EpiStore(const Params& pp, int, uint8_t*, volatile int*) : P(pp) {}
+  SPEC_DEV bool after(const Seg&, int, int) { return true; }
+  SPEC_DEV bool segment(const Seg& s, uint32_t tb, int warp, int lane) {
     const int n = s.row0 + warp * 32 + lane;
     const bool valid = n >= s.lo && n < s.hi;
 #pragma unroll
@@ -131,6 +138,7 @@ struct EpiStore {
         }
       }
     }
+    return true;
   }
   SPEC_DEV void finish(int, int) {}
 };
@@ -142,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const __grid_constant__ CUtensorMap tA2, const __grid_constant__ CUtensorMap tB,
               const __grid_constant__ typename Sched::Params sp, const __grid_constant__ typename Epi::Params ep,
               void* ws) {
-  using C = Cfg<MPAD>;
+  using C = Cfg<MPAD, Epi::kScratch>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -165,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(aempty0 + 8 * s, 4);
     }
     mbar_init(drain, 1);
+    Epi::init(smem + (size_t)S * C::kStage + 256);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -294,21 +303,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue warps 0-3: TMEM lanes 32*warp .. 32*warp+31
     pdl_wait();
     pdl_trigger();
-    Epi epi(ep, c);
+    Epi epi(ep, c, smem + (size_t)S * C::kStage + 256, abort);
     int abuf = 0;
     uint32_t aphase = 0;
     Sched sch(sp, c);
     Seg sg;
-    while (sch.next(sg)) {
-      if (!mbar_wait(afull0 + 8 * abuf, aphase, abort)) break;
+    bool ok = true;
+    while (ok && sch.next(sg)) {
+      if (!mbar_wait(afull0 + 8 * abuf, aphase, abort)) { ok = false; break; }
       tc_fence_after();
-      epi.segment(sg, tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(abuf * MPAD), warp, lane);
+      ok = epi.segment(sg, tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(abuf * MPAD), warp, lane);
+      if (!ok) break;
+      // the accumulator goes back to the MMA warp before the work that no longer needs it
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(aempty0 + 8 * abuf);
       if (++abuf == C::kBufs) { abuf = 0; aphase ^= 1u; }
+      ok = epi.after(sg, warp, lane);
     }
-    epi.finish(warp, lane);
+    if (ok) epi.finish(warp, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -325,7 +338,7 @@ bool make_map(CUtensorMap* tm, const void* ptr, int rows, int cols, int box_rows
 template <int MPAD, class Sched, class Epi>
 spec_status launch_tc(const CUtensorMap* a, const CUtensorMap& b, const typename Sched::Params& sp,
                       const typename Epi::Params& ep, int G, size_t extra_static, void* ws, cudaStream_t st) {
-  using C = Cfg<MPAD>;
+  using C = Cfg<MPAD, Epi::kScratch>;
   static int attr_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
