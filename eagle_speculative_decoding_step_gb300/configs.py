@@ -50,6 +50,9 @@ class Workload:
     rank: int = 0              # 0 = full-vocabulary LM head
     num_candidates: int = 0
     draft_vocab: int = 0       # reduced draft vocabulary (LM-head rows); 0 = the full vocabulary
+    # EAGLE-3.1 options
+    fc_norm: bool = False      # RMSNorm (own gain) on the FC-fused feature
+    norm_output: bool = False  # the next pass takes the normalised output state
     # misc
     rms_eps: float = 1e-6
     rope_theta: float = 10000.0

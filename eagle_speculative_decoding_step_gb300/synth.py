@@ -33,7 +33,7 @@ _TID = {
     "fc": 1, "embed": 2, "hidden_norm": 3, "in_norm": 4, "post_norm": 5, "final_norm": 6,
     "wq": 7, "wk": 8, "wv": 9, "wo": 10, "wgate": 11, "wup": 12, "wdown": 13, "lm_head": 14,
     "aux": 20, "kv_k": 21, "kv_v": 22, "ctx": 23, "blocks": 24, "root": 25, "noise": 26,
-    "hid": 27, "misc": 28, "d2t": 29,
+    "hid": 27, "misc": 28, "d2t": 29, "fc_norm": 30,
 }
 
 
@@ -95,6 +95,8 @@ def make_weights(w, with_lm_head: bool = True) -> dict:
     W["embed"] = _store(normal((V, H), s, "embed", 0.02), w.dtype)
     for nm in ("hidden_norm", "in_norm", "post_norm", "final_norm"):
         W[nm] = _store(normal((H,), s, nm, 0.1, 1.0), w.dtype)
+    if getattr(w, "fc_norm", False):
+        W["fc_norm"] = _store(normal((H,), s, "fc_norm", 0.1, 1.0), w.dtype)
     W["wq"] = _store(normal((nq * hd, 2 * H), s, "wq", 0.02), w.dtype)
     W["wk"] = _store(normal((nkv * hd, 2 * H), s, "wk", 0.02), w.dtype)
     W["wv"] = _store(normal((nkv * hd, 2 * H), s, "wv", 0.02), w.dtype)

@@ -56,9 +56,26 @@ def slot_of(kv, b, cache_idx):
 def fc_fuse(desc, W, aux):
     """h0 = fc(cat(aux_low, aux_mid, aux_high)); fc is Linear(3H -> H)
     ([NEURON] "Eagle3 Draft Model Architecture", Eagle3LlamaModel.fc and the
-    initial forward mode's combine_hidden_states)."""
+    initial forward mode's combine_hidden_states).
+
+    EAGLE-3.1 ``fc_norm`` ([QUARK] "Background: EAGLE-3 and EAGLE-3.1": extra
+    normalisation inside the draft head; Quickstart's eagle_architecture_config
+    names the flag).  Reading: an RMSNorm with its own gain ``W["fc_norm"]`` on
+    the fused feature, before it enters the decoder layer.
+    """
     h0 = _f64(aux) @ _f64(W["fc"]).T
+    if getattr(desc, "fc_norm", False):
+        h0 = rmsnorm(h0, W["fc_norm"], desc.rms_eps)
     return _r(h0, desc.dtype)
+
+
+def recurrent_state(desc, prenorm, hn):
+    """The hidden state a draft pass hands to the next one: hidden_prenorm
+    ([NEURON] "Eagle3 Draft Model Architecture": the recurrent input is the
+    pre-norm state); with the EAGLE-3.1 ``norm_output`` flag ([QUARK] "Background:
+    EAGLE-3 and EAGLE-3.1", Quickstart) the reading is that the draft's output
+    state is the normalised one, so the next pass takes hn."""
+    return hn if getattr(desc, "norm_output", False) else prenorm
 
 
 def expand_rows(rows):

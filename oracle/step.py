@@ -29,7 +29,8 @@ def chain_draft(desc, W, aux, root_tok, ctx_len, kv, K, keep_logits=False):
     logits = [] if keep_logits else None
     for i in range(K):
         rows = {"M": B, "B": B, "R": 1, "step": i, "ctx_len": ctx_len, "tok": tok}
-        hid, hn = draft.draft_layer(desc, W, rows, hid, kv)
+        prenorm, hn = draft.draft_layer(desc, W, rows, hid, kv)
+        hid = draft.recurrent_state(desc, prenorm, hn)
         if desc.rank > 0:
             _, _, ids = draft.lowrank_candidates(desc, W, hn, desc.num_candidates, 1)
             lg = None
@@ -74,7 +75,7 @@ def tree_draft(desc, W, aux, root_tok, ctx_len, kv, top_k, depth, total, trace=N
             trace.append((rows, hid_in, ids, lp))
         res = tree.tree_expand(st, d, ids, lp)
         if d < depth:
-            rows, hid_in = res, prenorm
+            rows, hid_in = res, draft.recurrent_state(desc, prenorm, hn)
         else:
             return res
 
@@ -138,12 +139,13 @@ def prefill_chain_draft(desc, W, aux_rows, input_ids, next_token, last_idx, ctx_
     drafts = np.zeros((B, K), dtype=np.int64)
     drafts[:, 0] = ids[:, 0]
     logits = [lg]
-    hid = pre[last_row]
+    hid = draft.recurrent_state(desc, pre, hn)[last_row]
     ctx2 = np.asarray(ctx_len, dtype=np.int64) + np.asarray(last_idx, dtype=np.int64) + 1
     tok = ids[:, 0]
     for i in range(1, K):
         r = {"M": B, "B": B, "R": 1, "step": i - 1, "ctx_len": ctx2, "tok": tok}
-        hid, hn = draft.draft_layer(desc, W, r, hid, kv)
+        pre_i, hn = draft.draft_layer(desc, W, r, hid, kv)
+        hid = draft.recurrent_state(desc, pre_i, hn)
         ids, _, _, lg = draft.lm_head(desc, W, hn, 1)
         drafts[:, i] = ids[:, 0]
         tok = ids[:, 0]

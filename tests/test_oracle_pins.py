@@ -640,3 +640,51 @@ def test_kept_set_closed_forms():
     assert m.sum() == 2
     m, _ = verify.kept_set(l, 0, float(p[1] - 1e-9))  # just below -> one token
     assert m.tolist() == [False, True, False, False, False]
+
+
+# ---------------------------------------------------------------- EAGLE-3.1 options
+def test_fc_norm_unit_rms_and_scale_invariance():
+    """fc_norm: the fused feature leaves the FC with unit RMS before its gain, so
+    h0 / gain has mean square ms / (ms + eps) per row (ms = mean square of the raw
+    FC output), and scaling the auxiliary states leaves h0 unchanged up to eps."""
+    w = replace(MICRO, name="fcnorm", dtype="f32", fc_norm=True)
+    W, _, _ = _setup(w)
+    assert "fc_norm" in W and not np.allclose(W["fc_norm"], 1.0)
+    aux = synth.make_aux(w).astype(np.float64)
+    h0 = draft.fc_fuse(w, W, aux)
+    raw = aux @ np.asarray(W["fc"], np.float64).T
+    ms = (raw ** 2).mean(-1)
+    unit = h0 / np.asarray(W["fc_norm"], np.float64)
+    np.testing.assert_allclose((unit ** 2).mean(-1), ms / (ms + w.rms_eps), rtol=1e-12)
+    np.testing.assert_allclose(draft.fc_fuse(w, W, 7.0 * aux), h0, rtol=1e-5, atol=1e-7)
+    # without the flag: the plain projection
+    np.testing.assert_allclose(draft.fc_fuse(replace(w, fc_norm=False), W, aux), raw, rtol=1e-12)
+
+
+def test_norm_output_recurrence_closed_form():
+    """norm_output: with o_proj and down_proj zero the decoder layer passes its
+    hidden input through, so the k-th pass's normalised output is RMSNorm_final
+    applied k times to h0 (each pass takes the previous normalised output), while
+    without the flag every pass sees h0 itself; the first pass is the same either way."""
+    w = replace(MICRO, name="normout", dtype="f32", norm_output=True, K=4)
+    W, ctx, kv = _setup(w)
+    W["wo"] = np.zeros_like(W["wo"])
+    W["wdown"] = np.zeros_like(W["wdown"])
+    # strongly uneven gains, so that repeated normalisation turns the state
+    W["final_norm"] = np.exp(np.random.default_rng(4).normal(0.0, 1.0, w.H)).astype(np.float32)
+    aux = synth.make_aux(w).astype(np.float64)
+    root = np.array([3, 9])
+    lm = np.asarray(W["lm_head"], np.float64)
+    g = np.asarray(W["final_norm"], np.float64)
+    h = draft.fc_fuse(w, W, aux)
+    want_on, want_off = [], []
+    x = h
+    for _ in range(w.K):
+        x = numerics.rmsnorm(x, g, w.rms_eps)
+        want_on.append(np.argmax((x @ lm.T).astype(np.float32), -1))
+        want_off.append(np.argmax((numerics.rmsnorm(h, g, w.rms_eps) @ lm.T).astype(np.float32), -1))
+    got_on = step.chain_draft(w, W, aux, root, ctx, copy.deepcopy(kv), w.K)
+    got_off = step.chain_draft(replace(w, norm_output=False), W, aux, root, ctx, copy.deepcopy(kv), w.K)
+    np.testing.assert_array_equal(got_on, np.stack(want_on, 1))
+    np.testing.assert_array_equal(got_off, np.stack(want_off, 1))
+    assert (got_on[:, 0] == got_off[:, 0]).all() and (got_on != got_off).any()
