@@ -186,6 +186,7 @@ __global__ void epi_qkv_kernel(const float* __restrict__ part, SKPlan p, RowInfo
 
 // MODE 0 (after o_proj):  r = hid_in[src] + o;   out_b = post_attention_layernorm(r)
 // MODE 1 (after down):    r = r + down; out_a = r (hidden_prenorm); out_b = final_norm(r)
+// MODE 2 (after the FC, EAGLE-3.1 fc_norm): r = fc output; out_b = fc_norm(r)
 // One cluster of kCL CTAs per row.
 template <typename T, int MODE>
 __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(256)
@@ -202,7 +203,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(256)
   float* rr = r + (size_t)m * H;
   float ss = 0.f;
   for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) {
-    const float base = (MODE == 0) ? ld(h + n) : rr[n];
+    const float base = (MODE == 0) ? ld(h + n) : (MODE == 1 ? rr[n] : 0.f);
     const float v = base + sk_sum(part, p, m, n);
     rr[n] = v;
     if (MODE == 1) st(out_a + (size_t)m * H + n, v);
@@ -305,209 +306,292 @@ template <> SPEC_DEV void unpack16<__nv_bfloat16>(const uint4& r, float* o) {
   }
 }
 
-// Split-KV decode attention with the row masks of spec_rows.  grid = (nsplit,
-// nkv, B * nqg); a CTA serves up to QMAX queries (rows of one request x the q
-// heads of one kv head) over one slice of that request's key range: context
-// keys [klo, ctx) then draft-region keys [ctx, ctx + nd).  Keys are processed
-// 128 at a time (one per thread for the scores), K and V staged through shared
-// memory with 16-byte copies.
+// Split-KV decode attention with the row masks of spec_rows.
+//
+// Work item = (request b, query group qg, kv head g, split s): up to QMAX
+// queries (rows of one request x the q heads of kv head g) over one slice of
+// that request's keys -- context keys [klo, ctx) then draft-region keys
+// [ctx, ctx + nd).  The grid is persistent (as many CTAs as fit at once); CTA c
+// takes items c, c + grid, ...  Keys stream through shared memory in tiles of
+// 64 with cp.async, NST tiles in flight, so the copies of the next tiles
+// overlap the arithmetic on the current one.  Per tile: scores (thread = key x
+// half of the queries, packed fp32 FMAs), an online softmax per query (warp w:
+// queries w, w + 4, ...), then P.V with warp w taking keys 16w .. 16w+15 for
+// every query and lane l the head dims of l.  The four warps' partial outputs
+// are summed once per item.
+constexpr int kAttnTK = 64;
+constexpr int kAttnNST = 2;
+
+template <typename T, int HD> struct AttnShape {
+  static constexpr int KP = HD + 16 / (int)sizeof(T);          // padded K row (elements)
+  static constexpr int CH = HD * (int)sizeof(T) / 16;          // 16-byte chunks per row
+  static constexpr int STAGE = kAttnTK * KP * (int)sizeof(T) + kAttnTK * HD * (int)sizeof(T);
+  static constexpr int DPL = HD / 32;                          // head dims per lane in P.V
+};
+
+template <typename T, int HD, int QMAX>
+constexpr size_t attn_smem_for() {
+  using A = AttnShape<T, HD>;
+  const size_t stages = (size_t)kAttnNST * A::STAGE;
+  const size_t red = (size_t)4 * QMAX * HD * 4;                // the warps' partial outputs (aliases the stages)
+  return (stages > red ? stages : red) + (size_t)QMAX * HD * 4 + (size_t)QMAX * kAttnTK * 4;
+}
+
+template <typename T> SPEC_DEV void unpack_pair(uint32_t w, float2& o);
+template <> SPEC_DEV void unpack_pair<__nv_bfloat16>(uint32_t w, float2& o) {
+  o.x = __uint_as_float(w << 16);
+  o.y = __uint_as_float(w & 0xffff0000u);
+}
+
 template <typename T, int HD, int QMAX>
 __global__ void __launch_bounds__(128) attn_split_kernel(const T* __restrict__ qbuf, spec_kv kv, RowInfo ri,
                                                          int nq, int nkv, int window, int nsplit, int nqg,
-                                                         float scale, float* __restrict__ opart,
+                                                         int n_items, float scale, float* __restrict__ opart,
                                                          float2* __restrict__ mlpart, void* ws) {
   pdl_wait();
   pdl_trigger();
-  constexpr int TK = 128;                      // keys per tile (one per thread)
-  constexpr int KP = HD + (16 / sizeof(T));    // padded smem row (elements)
-  constexpr int QW = QMAX / 4;                 // queries per warp in softmax / PV
+  using A = AttnShape<T, HD>;
+  constexpr int TK = kAttnTK, NST = kAttnNST, KP = A::KP, CH = A::CH, DPL = A::DPL;
+  constexpr int QH = QMAX / 2;                  // queries per thread in the scores
+  constexpr int QW = QMAX / 4;                  // queries per warp in the softmax
   extern __shared__ __align__(16) uint8_t attn_smem[];
-  float* sQ = reinterpret_cast<float*>(attn_smem);                       // [QMAX][HD]
-  float* sS = sQ + QMAX * HD;                                           // [QMAX][TK]
-  T* sK = reinterpret_cast<T*>(sS + QMAX * TK);                         // [TK][KP]
-  T* sV = sK + TK * KP;                                                 // [TK][HD]
+  constexpr size_t kStages = attn_smem_for<T, HD, QMAX>() - (size_t)QMAX * HD * 4 - (size_t)QMAX * TK * 4;
+  float* sQ = reinterpret_cast<float*>(attn_smem + kStages);          // [QMAX][HD], scaled
+  float* sS = sQ + QMAX * HD;                                         // [QMAX][TK]
+  float* red = reinterpret_cast<float*>(attn_smem);                   // [4][QMAX][HD] after the last tile
   __shared__ float sM[QMAX], sL[QMAX], sA[QMAX];
   __shared__ int s_lo[QMAX];
   __shared__ unsigned long long s_mask[QMAX];
   __shared__ int s_klo, s_nd;
 
-  const int s = blockIdx.x, g = blockIdx.y;
-  const int b = blockIdx.z / nqg, qg = blockIdx.z % nqg;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = nq / nkv;
   const int nQall = ri.R * G;
-  const int q0 = qg * QMAX;
-  const int nQ = min(QMAX, nQall - q0);
-  const int ctx = ri.ctx_len[b];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  if (tid < 32) {
-    int lo = 0x7fffffff;
-    unsigned long long mk = 0;
-    if (tid < nQ) {
-      const int m = b * ri.R + (q0 + tid) / G;
-      const int pos = row_pos(ri, m);
-      lo = window > 0 ? max(0, pos - window + 1) : 0;
-      if (lo > ctx) lo = ctx;
-      mk = row_mask(ri, m);
-      s_lo[tid] = lo;
-      s_mask[tid] = mk;
-    }
-    int mlo = lo;
-    unsigned long long om = mk;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mlo = min(mlo, __shfl_xor_sync(0xffffffffu, mlo, o));
-      om |= __shfl_xor_sync(0xffffffffu, om, o);
-    }
-    if (tid == 0) {
-      s_klo = mlo;
-      s_nd = om ? 64 - __clzll((long long)om) : 0;
-    }
-    if (tid < QMAX) {
-      sM[tid] = -INFINITY;
-      sL[tid] = 0.f;
-    }
-  }
-  for (int e = tid; e < QMAX * HD; e += blockDim.x) {
-    const int qi = e / HD, d = e % HD;
-    float v = 0.f;
-    if (qi < nQ) {
-      const int q = q0 + qi;
-      const int m = b * ri.R + q / G, h = g * G + q % G;
-      v = ld(qbuf + ((size_t)m * nq + h) * HD + d) * scale;
-    }
-    sQ[e] = v;
-  }
-  __syncthreads();
-  const int klo = s_klo, nd = s_nd;
-  const int nctx = ctx - klo;
-  const int total = nctx + nd;
-  const int chunk = ((total + nsplit - 1) / nsplit + TK - 1) / TK * TK;   // whole tiles per split
-  const int kbeg = s * chunk, kend = min(total, kbeg + chunk);
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int s = item % nsplit;
+    const int g = (item / nsplit) % nkv;
+    const int bq = item / (nsplit * nkv);
+    const int b = bq / nqg, qg = bq % nqg;
+    const int q0 = qg * QMAX;
+    const int nQ = min(QMAX, nQall - q0);
+    const int ctx = ri.ctx_len[b];
 
-  constexpr int DJ = HD / 32;
-  float acc[QW][DJ];
+    if (tid < 32) {
+      int lo = 0x7fffffff;
+      unsigned long long mk = 0;
+      if (tid < nQ) {
+        const int m = b * ri.R + (q0 + tid) / G;
+        const int pos = row_pos(ri, m);
+        lo = window > 0 ? max(0, pos - window + 1) : 0;
+        if (lo > ctx) lo = ctx;
+        mk = row_mask(ri, m);
+      }
+      if (tid < QMAX) {
+        s_lo[tid] = lo;
+        s_mask[tid] = mk;
+        sM[tid] = -INFINITY;
+        sL[tid] = 0.f;
+      }
+      int mlo = lo;
+      unsigned long long om = mk;
 #pragma unroll
-  for (int a = 0; a < QW; ++a)
-#pragma unroll
-    for (int jj = 0; jj < DJ; ++jj) acc[a][jj] = 0.f;
-
-  for (int t0 = kbeg; t0 < kend; t0 += TK) {
-    const int nk = min(TK, kend - t0);
-    // stage K / V rows of this tile: asynchronous 16-byte copies, all in flight
-    // together (a key's row of one kv head is HD contiguous elements)
-    constexpr int CH = HD * sizeof(T) / 16;        // 16-byte chunks per row
-    for (int e = tid; e < nk * CH; e += blockDim.x) {
-      const int kt = e / CH, ch = e % CH;
-      const int kidx = t0 + kt;
-      const int ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
-      const long long slot = slot_of(kv, b, ci);
-      uint4* dk = reinterpret_cast<uint4*>(sK + kt * KP) + ch;
-      uint4* dv = reinterpret_cast<uint4*>(sV + kt * HD) + ch;
-      if (slot >= 0) {
-        const size_t off = ((size_t)slot * nkv + g) * HD;
-        cp_async16(dk, reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(kv.k) + off) + ch);
-        cp_async16(dv, reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(kv.v) + off) + ch);
-      } else {
-        *dk = make_uint4(0, 0, 0, 0);
-        *dv = make_uint4(0, 0, 0, 0);
+      for (int o = 16; o > 0; o >>= 1) {
+        mlo = min(mlo, __shfl_xor_sync(0xffffffffu, mlo, o));
+        om |= __shfl_xor_sync(0xffffffffu, om, o);
+      }
+      if (tid == 0) {
+        s_klo = mlo;
+        s_nd = om ? 64 - __clzll((long long)om) : 0;
       }
     }
-    cp_async_wait_all();
-    __syncthreads();
-    // scores: thread tid owns key tid of the tile
-    if (tid < nk) {
-      const int kidx = t0 + tid;
-      const int ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
-      const bool valid = slot_of(kv, b, ci) >= 0;
-      float sc[QMAX];
-#pragma unroll
-      for (int qi = 0; qi < QMAX; ++qi) sc[qi] = 0.f;
-      constexpr int EPV = 16 / sizeof(T);
-      const uint4* kr = reinterpret_cast<const uint4*>(sK + tid * KP);
-#pragma unroll 2
-      for (int d0 = 0; d0 < HD; d0 += EPV) {
-        float kd[EPV];
-        unpack16<T>(kr[d0 / EPV], kd);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-#pragma unroll
-          for (int qi = 0; qi < QMAX; ++qi) sc[qi] += sQ[qi * HD + d0 + e] * kd[e];
-        }
+    for (int e = tid; e < QMAX * HD; e += blockDim.x) {
+      const int qi = e / HD, d = e % HD;
+      float v = 0.f;
+      if (qi < nQ) {
+        const int q = q0 + qi;
+        const int m = b * ri.R + q / G, h = g * G + q % G;
+        v = ld(qbuf + ((size_t)m * nq + h) * HD + d) * scale;
       }
-#pragma unroll
-      for (int qi = 0; qi < QMAX; ++qi) {
-        bool ok = valid && qi < nQ;
-        if (ok) {
-          if (ci < ctx) ok = ci >= s_lo[qi];
-          else ok = (s_mask[qi] >> (ci - ctx)) & 1ull;
-        }
-        sS[qi * TK + tid] = ok ? sc[qi] : -INFINITY;
-      }
-    } else {
-#pragma unroll
-      for (int qi = 0; qi < QMAX; ++qi) sS[qi * TK + tid] = -INFINITY;
+      sQ[e] = v;
     }
     __syncthreads();
-    // online softmax: warp w handles queries w, w+4, ...
-#pragma unroll
-    for (int a = 0; a < QW; ++a) {
-      const int qi = warp + 4 * a;
-      float v[TK / 32];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int u = 0; u < TK / 32; ++u) {
-        v[u] = sS[qi * TK + lane + 32 * u];
-        mx = fmaxf(mx, v[u]);
+    const int klo = s_klo, nd = s_nd;
+    const int nctx = ctx - klo;
+    const int total = nctx + nd;
+    const int chunk = ((total + nsplit - 1) / nsplit + TK - 1) / TK * TK;   // whole tiles per split
+    const int kbeg = min(total, s * chunk), kend = min(total, kbeg + chunk);
+    const int ntiles = (kend - kbeg + TK - 1) / TK;
+
+    // stage tile j (keys kbeg + j*TK ...) into ring slot j % NST: thread t copies
+    // chunk t % CH of keys t / CH, t / CH + 128 / CH, ...
+    auto issue = [&](int j) {
+      if (j < ntiles) {
+        uint8_t* st = attn_smem + (size_t)(j % NST) * A::STAGE;
+        T* sK = reinterpret_cast<T*>(st);
+        T* sV = reinterpret_cast<T*>(st + TK * KP * sizeof(T));
+        const int t0 = kbeg + j * TK;
+        const int nk = min(TK, kend - t0);
+        const int ch = tid % CH;
+        for (int kt = tid / CH; kt < nk; kt += 128 / CH) {
+          const int kidx = t0 + kt;
+          const int ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
+          const long long slot = slot_of(kv, b, ci);
+          uint4* dk = reinterpret_cast<uint4*>(sK + kt * KP) + ch;
+          uint4* dv = reinterpret_cast<uint4*>(sV + kt * HD) + ch;
+          if (slot >= 0) {
+            const size_t off = ((size_t)slot * nkv + g) * HD;
+            cp_async16(dk, reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(kv.k) + off) + ch);
+            cp_async16(dv, reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(kv.v) + off) + ch);
+          } else {
+            *dk = make_uint4(0, 0, 0, 0);
+            *dv = make_uint4(0, 0, 0, 0);
+          }
+        }
       }
-      mx = warp_max(mx);
-      const float mold = sM[qi];
-      const float mnew = fmaxf(mold, mx);
-      float sum = 0.f;
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    float2 acc[QMAX][DPL / 2];
 #pragma unroll
-      for (int u = 0; u < TK / 32; ++u) {
-        const float e = (mnew == -INFINITY) ? 0.f : expf(v[u] - mnew);
-        sS[qi * TK + lane + 32 * u] = e;
-        sum += e;
+    for (int q = 0; q < QMAX; ++q)
+#pragma unroll
+      for (int u = 0; u < DPL / 2; ++u) acc[q][u] = make_float2(0.f, 0.f);
+
+#pragma unroll
+    for (int j = 0; j < NST - 1; ++j) issue(j);
+    for (int j = 0; j < ntiles; ++j) {
+      issue(j + NST - 1);
+      asm volatile("cp.async.wait_group %0;" ::"n"(NST - 1) : "memory");
+      __syncthreads();
+      const uint8_t* st = attn_smem + (size_t)(j % NST) * A::STAGE;
+      const T* sK = reinterpret_cast<const T*>(st);
+      const T* sV = reinterpret_cast<const T*>(st + TK * KP * sizeof(T));
+      const int t0 = kbeg + j * TK;
+      const int nk = min(TK, kend - t0);
+      // scores: thread = (key kt, query half qh)
+      {
+        const int kt = tid % TK, qh = tid / TK;
+        if (kt < nk) {
+          const int kidx = t0 + kt;
+          const int ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
+          const bool valid = slot_of(kv, b, ci) >= 0;
+          float2 sc[QH];
+#pragma unroll
+          for (int q = 0; q < QH; ++q) sc[q] = make_float2(0.f, 0.f);
+          const uint4* kr = reinterpret_cast<const uint4*>(sK + kt * KP);
+#pragma unroll 4
+          for (int c = 0; c < CH; ++c) {
+            const uint4 raw = kr[c];
+            float2 k2[4];
+            if constexpr (sizeof(T) == 2) {
+              unpack_pair<T>(raw.x, k2[0]);
+              unpack_pair<T>(raw.y, k2[1]);
+              unpack_pair<T>(raw.z, k2[2]);
+              unpack_pair<T>(raw.w, k2[3]);
+            } else {
+              k2[0] = make_float2(__uint_as_float(raw.x), __uint_as_float(raw.y));
+              k2[1] = make_float2(__uint_as_float(raw.z), __uint_as_float(raw.w));
+            }
+            constexpr int NP = sizeof(T) == 2 ? 4 : 2;            // float pairs in 16 bytes
+            const int d0 = c * 2 * NP;
+#pragma unroll
+            for (int q = 0; q < QH; ++q) {
+              const float2* qr = reinterpret_cast<const float2*>(sQ + (qh * QH + q) * HD + d0);
+#pragma unroll
+              for (int u = 0; u < NP; ++u) sc[q] = __ffma2_rn(qr[u], k2[u], sc[q]);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < QH; ++q) {
+            const int qi = qh * QH + q;
+            bool ok = valid && qi < nQ;
+            if (ok) {
+              if (ci < ctx) ok = ci >= s_lo[qi];
+              else ok = (s_mask[qi] >> (ci - ctx)) & 1ull;
+            }
+            sS[qi * TK + kt] = ok ? sc[q].x + sc[q].y : -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < QH; ++q) sS[(qh * QH + q) * TK + kt] = -INFINITY;
+        }
       }
-      sum = warp_sum(sum);
-      const float alpha = (mold == -INFINITY) ? 0.f : expf(mold - mnew);
-      __syncwarp();
-      if (lane == 0) {
-        sA[qi] = alpha;
-        sL[qi] = sL[qi] * alpha + sum;
-        sM[qi] = mnew;
-      }
-#pragma unroll
-      for (int jj = 0; jj < DJ; ++jj) acc[a][jj] *= alpha;
-    }
-    __syncwarp();
-    // P @ V (each warp reads only the probabilities of its own queries)
-    for (int kt = 0; kt < nk; ++kt) {
-      float vv[DJ];
-#pragma unroll
-      for (int jj = 0; jj < DJ; ++jj) vv[jj] = ld(sV + kt * HD + lane + 32 * jj);
+      __syncthreads();
+      // online softmax: warp w handles queries w, w + 4, ...
 #pragma unroll
       for (int a = 0; a < QW; ++a) {
-        const float pw = sS[(warp + 4 * a) * TK + kt];
-#pragma unroll
-        for (int jj = 0; jj < DJ; ++jj) acc[a][jj] += pw * vv[jj];
+        const int qi = warp + 4 * a;
+        const float v0 = sS[qi * TK + lane], v1 = sS[qi * TK + lane + 32];
+        const float mx = warp_max(fmaxf(v0, v1));
+        const float mold = sM[qi];
+        const float mnew = fmaxf(mold, mx);
+        const float e0 = mnew == -INFINITY ? 0.f : expf(v0 - mnew);
+        const float e1 = mnew == -INFINITY ? 0.f : expf(v1 - mnew);
+        sS[qi * TK + lane] = e0;
+        sS[qi * TK + lane + 32] = e1;
+        const float sum = warp_sum(e0 + e1);
+        if (lane == 0) {
+          const float al = mold == -INFINITY ? 0.f : expf(mold - mnew);
+          sA[qi] = al;
+          sL[qi] = sL[qi] * al + sum;
+          sM[qi] = mnew;
+        }
       }
+      __syncthreads();
+      // P.V: warp w takes keys 16w .. 16w+15, all queries; lane l head dims DPL*l ..
+#pragma unroll
+      for (int q = 0; q < QMAX; ++q) {
+        const float al = sA[q];
+#pragma unroll
+        for (int u = 0; u < DPL / 2; ++u) acc[q][u] = __fmul2_rn(acc[q][u], make_float2(al, al));
+      }
+      const int kb = warp * (TK / 4), ke = min(nk, kb + TK / 4);
+      for (int kt = kb; kt < ke; ++kt) {
+        float2 v2[DPL / 2];
+        if constexpr (sizeof(T) == 2) {
+          if constexpr (DPL == 4) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(sV + kt * HD + DPL * lane);
+            unpack_pair<T>(raw.x, v2[0]);
+            unpack_pair<T>(raw.y, v2[1]);
+          } else {
+            const uint32_t raw = *reinterpret_cast<const uint32_t*>(sV + kt * HD + DPL * lane);
+            unpack_pair<T>(raw, v2[0]);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < DPL / 2; ++u)
+            v2[u] = *reinterpret_cast<const float2*>(reinterpret_cast<const float*>(sV) + kt * HD + DPL * lane + 2 * u);
+        }
+#pragma unroll
+        for (int q = 0; q < QMAX; ++q) {
+          const float pw = sS[q * TK + kt];
+#pragma unroll
+          for (int u = 0; u < DPL / 2; ++u) acc[q][u] = __ffma2_rn(make_float2(pw, pw), v2[u], acc[q][u]);
+        }
+      }
+      __syncthreads();     // ring slot j % NST is refilled by the next iteration's copies
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-  }
-  // write this split's partials
+    // sum the warps' partial outputs, write this split's partials
 #pragma unroll
-  for (int a = 0; a < QW; ++a) {
-    const int qi = warp + 4 * a;
-    if (qi >= nQ) continue;
-    const int q = q0 + qi;
-    const int m = b * ri.R + q / G, h = g * G + q % G;
-    const size_t base = ((size_t)m * nq + h) * nsplit + s;
-    float* o = opart + base * HD;
+    for (int q = 0; q < QMAX; ++q)
 #pragma unroll
-    for (int jj = 0; jj < DJ; ++jj) o[lane + 32 * jj] = acc[a][jj];
-    if (lane == 0) mlpart[base] = make_float2(sM[qi], sL[qi]);
+      for (int u = 0; u < DPL / 2; ++u)
+        *reinterpret_cast<float2*>(red + ((size_t)warp * QMAX + q) * HD + DPL * lane + 2 * u) = acc[q][u];
+    __syncthreads();
+    for (int e = tid; e < QMAX * HD; e += blockDim.x) {
+      const int qi = e / HD, d = e % HD;
+      if (qi >= nQ) continue;
+      const float o = red[e] + red[QMAX * HD + e] + red[2 * QMAX * HD + e] + red[3 * QMAX * HD + e];
+      const int q = q0 + qi;
+      const int m = b * ri.R + q / G, h = g * G + q % G;
+      const size_t base = ((size_t)m * nq + h) * nsplit + s;
+      opart[base * HD + d] = o;
+      if (d == 0) mlpart[base] = make_float2(sM[qi], sL[qi]);
+    }
+    __syncthreads();     // red / sQ / sM reused by the next item
   }
 }
 
@@ -579,88 +663,207 @@ SPEC_DEV uint32_t order_key(float f) {
 }
 
 // The Kc largest of each row of s [M, V] (ties to the smaller id), in
-// descending order: exact radix selection of the Kc-th key, ordered collection
-// of the ties, bitonic sort of the selected.  One CTA of 1024 threads per row.
+// descending order.  One CTA of 1024 threads per row, on order-preserving
+// 32-bit keys:
+//  1. every thread takes the largest key among its elements (a strided slice of
+//     the row); the Kc-th largest of these 1024 maxima, T0, is a lower bound of
+//     the row's Kc-th largest key (the Kc largest maxima are Kc distinct
+//     elements >= T0);
+//  2. a second pass copies the elements >= T0 -- typically a few hundred -- to
+//     shared memory;
+//  3. an exact radix selection over the copies gives the Kc-th key and how many
+//     of the elements equal to it are taken (smallest ids first);
+//  4. a bitonic sort of the Kc selected.
+// Both passes over the row are plain streaming reads (no atomics on shared
+// counters per element).  If more than the shared-memory capacity passes step
+// 2 (rows with huge runs of equal values), step 3 runs on the row itself, in
+// id order for the ties.
+constexpr int kTkCap = 6144;
+
+size_t topk_select_smem() { return (size_t)kTkCap * 8 + 1024 * 8 + 256 * 4; }
+
+SPEC_DEV int block_excl_scan(int v, int* wsum, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) wsum[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < nw) wsum[lane] = t;     // inclusive prefix of the warp totals
+    if (lane == 31) *total = t;
+  }
+  __syncthreads();
+  return x - v + (w > 0 ? wsum[w - 1] : 0);
+}
+
+// radix select over n keys (shared memory, or the float row x): the key of the
+// need-th largest, digit by digit (8 bits) from the top, and in *tie_need how
+// many elements equal to it belong to the need largest.  Lanes of a warp that
+// fall in the same digit add to the histogram once.
+template <bool SMEM_KEYS>
+SPEC_DEV uint32_t radix_select(const float* x, const uint32_t* keys, int n, int need, int* hist, uint32_t* s_prefix,
+                               int* s_need, int* tie_need) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid == 0) { *s_prefix = 0u; *s_need = need; }
+  for (int lo = 24; lo >= 0; lo -= 8) {
+    if (tid < 256) hist[tid] = 0;
+    __syncthreads();
+    const uint32_t pf = *s_prefix;
+    const uint32_t pmask = lo == 24 ? 0u : (0xffffffffu << (lo + 8));
+    for (int base = 0; base < n; base += blockDim.x) {
+      const int i = base + tid;
+      uint32_t k = 0;
+      bool ok = i < n;
+      if (ok) {
+        k = SMEM_KEYS ? keys[i] : order_key(x[i]);
+        ok = (k & pmask) == (pf & pmask);
+      }
+      const unsigned act = __ballot_sync(0xffffffffu, ok);
+      if (ok) {
+        const uint32_t dg = (k >> lo) & 0xffu;
+        const unsigned peers = __match_any_sync(act, dg);
+        if (lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int nn = *s_need, acc = 0, dsel = 0;
+      for (int dg = 255; dg >= 0; --dg) {
+        if (acc + hist[dg] >= nn) { dsel = dg; break; }
+        acc += hist[dg];
+      }
+      *s_need = nn - acc;
+      *s_prefix = pf | ((uint32_t)dsel << lo);
+    }
+    __syncthreads();
+  }
+  *tie_need = *s_need;
+  return *s_prefix;
+}
+
 __global__ void __launch_bounds__(1024) topk_select_kernel(const float* __restrict__ s, int V, int Kc,
                                                            int32_t* __restrict__ out_ids) {
   pdl_wait();
   pdl_trigger();
-  __shared__ int hist[256];
+  extern __shared__ __align__(16) uint8_t tk_smem[];
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(tk_smem);              // [cap] copies
+  int* cidx = reinterpret_cast<int*>(ckey + kTkCap);                  // [cap]
+  uint32_t* skey = reinterpret_cast<uint32_t*>(cidx + kTkCap);        // [1024] maxima, then the selected
+  int* sidx = reinterpret_cast<int*>(skey + 1024);
+  int* hist = sidx + 1024;                                            // [256]
+  __shared__ int wsum[32];
+  __shared__ int s_total, s_nsel, s_nc, s_need, s_tie;
   __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
-  __shared__ uint32_t skey[1024];
-  __shared__ int sidx[1024];
-  __shared__ int s_cnt, s_tie_taken;
-  __shared__ int wcount[32];
   const int m = blockIdx.x;
   const float* x = s + (size_t)m * V;
-  const int tid = threadIdx.x;
-  if (tid == 0) { s_prefix = 0; s_need = Kc; }
-  __syncthreads();
-  // radix select: find the key value of the Kc-th largest and how many of the
-  // elements equal to it are needed
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    if (tid < 256) hist[tid] = 0;
-    __syncthreads();
-    const uint32_t prefix = s_prefix;
-    const uint32_t pmask = (shift == 24) ? 0u : (0xffffffffu << (shift + 8));
-    for (int v = tid; v < V; v += blockDim.x) {
-      const uint32_t k = order_key(x[v]);
-      if ((k & pmask) == (prefix & pmask)) atomicAdd(&hist[(k >> shift) & 0xff], 1);
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid == 0) { s_nsel = 0; s_nc = 0; }
+  // 1. per-thread maxima, then T0 = the Kc-th largest of them
+  uint32_t tmax = 0;
+  for (int base = 0; base < V; base += 4 * blockDim.x) {
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * blockDim.x + tid;
+      v[u] = i < V ? x[i] : -INFINITY;
     }
-    __syncthreads();
-    if (tid == 0) {
-      int need = s_need, acc = 0, dsel = 0;
-      for (int dgt = 255; dgt >= 0; --dgt) {
-        if (acc + hist[dgt] >= need) { dsel = dgt; break; }
-        acc += hist[dgt];
-      }
-      s_need = need - acc;
-      s_prefix = prefix | ((uint32_t)dsel << shift);
-    }
-    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (base + u * blockDim.x + tid < V) tmax = max(tmax, order_key(v[u]));
   }
-  const uint32_t kth = s_prefix;
-  const int tie_need = s_need;      // elements equal to kth to take (smallest ids)
-  if (tid == 0) { s_cnt = 0; s_tie_taken = 0; }
+  skey[tid] = tmax;           // 0 for a thread without elements: below every key
   __syncthreads();
-  // collect in index order (ties keep the smallest ids)
+  int tie_need;
+  const uint32_t t0 = radix_select<true>(nullptr, skey, blockDim.x, Kc, hist, &s_prefix, &s_need, &tie_need);
+  // 2. copy the elements >= T0 (warp-aggregated slots)
   for (int base = 0; base < V; base += blockDim.x) {
-    const int v = base + tid;
+    const int i = base + tid;
     uint32_t k = 0;
-    bool gt = false, eq = false;
-    if (v < V) {
-      k = order_key(x[v]);
-      gt = k > kth;
-      eq = k == kth;
+    bool take = false;
+    if (i < V) {
+      k = order_key(x[i]);
+      take = k >= t0;
     }
-    if (gt) {
-      const int p = atomicAdd(&s_cnt, 1);
-      skey[p] = k;
-      sidx[p] = v;
+    const unsigned bal = __ballot_sync(0xffffffffu, take);
+    if (bal) {
+      int slot0 = 0;
+      if (lane == 0) slot0 = atomicAdd(&s_nc, __popc(bal));
+      slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+      const int p = slot0 + __popc(bal & ((1u << lane) - 1u));
+      if (take && p < kTkCap) {
+        ckey[p] = k;
+        cidx[p] = i;
+      }
     }
-    // ordered ranks of the ties within this chunk
-    const unsigned bal = __ballot_sync(0xffffffffu, eq);
-    if ((tid & 31) == 0) wcount[tid >> 5] = __popc(bal);
-    __syncthreads();
-    int before = 0;
-    for (int w = 0; w < (tid >> 5); ++w) before += wcount[w];
-    before += __popc(bal & ((1u << (tid & 31)) - 1u));
-    const int taken = s_tie_taken;
-    if (eq && taken + before < tie_need) {
-      const int p = atomicAdd(&s_cnt, 1);
-      skey[p] = k;
-      sidx[p] = v;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      int tot = 0;
-      for (int w = 0; w < 32; ++w) tot += wcount[w];
-      s_tie_taken = taken + tot;
-    }
-    __syncthreads();
   }
-  // bitonic sort of the Kc selected: key descending, index ascending
+  __syncthreads();
+  const int ncand = s_nc;
+  uint32_t kth;
+  if (ncand <= kTkCap) {
+    // 3. exact selection among the copies
+    kth = radix_select<true>(nullptr, ckey, ncand, Kc, hist, &s_prefix, &s_need, &tie_need);
+    for (int i = tid; i < ncand; i += blockDim.x) {
+      const uint32_t k = ckey[i];
+      bool take = k > kth;
+      if (k == kth) {
+        const int id = cidx[i];
+        int rank = 0;
+        for (int j = 0; j < ncand; ++j) rank += (ckey[j] == kth && cidx[j] < id);
+        take = rank < tie_need;
+      }
+      if (take) {
+        const int p = atomicAdd(&s_nsel, 1);
+        skey[p] = k;
+        sidx[p] = cidx[i];
+      }
+    }
+  } else {
+    kth = radix_select<false>(x, nullptr, V, Kc, hist, &s_prefix, &s_need, &tie_need);
+    // ordered pass over the row (ties keep the smallest ids)
+    if (tid == 0) s_tie = 0;
+    __syncthreads();
+    for (int base = 0; base < V; base += blockDim.x) {
+      const int v = base + tid;
+      uint32_t k = 0;
+      bool gt = false, eq = false;
+      if (v < V) {
+        k = order_key(x[v]);
+        gt = k > kth;
+        eq = k == kth;
+      }
+      if (gt) {
+        const int p = atomicAdd(&s_nsel, 1);
+        skey[p] = k;
+        sidx[p] = v;
+      }
+      // rank of this tie in id order: ties of earlier chunks, earlier warps, earlier lanes
+      const unsigned bal = __ballot_sync(0xffffffffu, eq);
+      const int before = block_excl_scan(lane == 0 ? __popc(bal) : 0, wsum, &s_total);
+      const int taken = s_tie;
+      const int off = __shfl_sync(0xffffffffu, before, 0);
+      if (eq && taken + off + __popc(bal & ((1u << lane) - 1u)) < tie_need) {
+        const int p = atomicAdd(&s_nsel, 1);
+        skey[p] = k;
+        sidx[p] = v;
+      }
+      __syncthreads();
+      if (tid == 0) s_tie = taken + s_total;
+      __syncthreads();
+    }
+  }
+  __syncthreads();
+  // 4. bitonic sort of the Kc selected: key descending, index ascending
   int n2 = 1;
   while (n2 < Kc) n2 <<= 1;
   if (tid >= Kc && tid < n2) { skey[tid] = 0; sidx[tid] = 0x7fffffff; }
@@ -705,7 +908,33 @@ __global__ void __launch_bounds__(256) rescore_kernel(const T* __restrict__ hn, 
   const T* w = lm_head + (size_t)c * H;
   const T* h = hn + (size_t)m * H;
   float s = 0.f;
-  for (int n = lane; n < H; n += 32) s += ld(w + n) * ld(h + n);
+  constexpr int EPV = 16 / sizeof(T);          // elements per 16-byte load
+  if (H % EPV == 0 && ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(h)) & 15u) == 0) {
+    // 16-byte loads, four in flight per lane (the row of h is shared by the CTA's warps: L1)
+    const uint4* w4 = reinterpret_cast<const uint4*>(w);
+    const uint4* h4 = reinterpret_cast<const uint4*>(h);
+    const int nch = H / EPV;
+    for (int c0 = lane; c0 < nch; c0 += 4 * 32) {
+      uint4 a[4], b[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c0 + u * 32 < nch) {
+          a[u] = __ldg(w4 + c0 + u * 32);
+          b[u] = __ldg(h4 + c0 + u * 32);
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c0 + u * 32 < nch) {
+          float fa[EPV], fb[EPV];
+          unpack16<T>(a[u], fa);
+          unpack16<T>(b[u], fb);
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) s += fa[e] * fb[e];
+        }
+    }
+  } else {
+    for (int n = lane; n < H; n += 32) s += ld(w + n) * ld(h + n);
+  }
   s = warp_sum(s);
   if (lane == 0) exact[(size_t)m * Kc + j] = s;
 }
@@ -804,6 +1033,13 @@ void launch_epi_oproj(const spec_model_desc& d, const float* part, const SKPlan&
                           (T*)nout)));
 }
 
+void launch_epi_fcnorm(const spec_model_desc& d, const float* part, const SKPlan& p, int M, float* r,
+                       const void* gain, void* h0, cudaStream_t st) {
+  RowInfo ri{};
+  DISPATCH_T(d.dtype, (launch_pdl(resnorm_kernel<T, 2>, dim3(M * kCL), dim3(256), 0, st, part, p, ri, d.hidden,
+                                  d.rms_eps, nullptr, (const T*)gain, r, nullptr, (T*)h0)));
+}
+
 void launch_epi_swiglu(const spec_model_desc& d, const float* part, const SKPlan& p, int M, void* act,
                        cudaStream_t st) {
   const long long n = (long long)M * d.intermediate;
@@ -833,11 +1069,14 @@ int attn_qmax(int rows_per_req, int G) {
   return 32;
 }
 
-// Splits per (request, kv head, query group): enough CTAs for ~2 per SM, but no
-// split shorter than one 128-key tile when an upper bound of the context is known.
+// Splits per (request, kv head, query group): about four work items per
+// resident CTA of the persistent grid (at most three CTAs per SM), but no split
+// shorter than two 64-key tiles when an upper bound of the context is known.
+constexpr int kAttnItemsPerSm = 12;
+
 int attn_splits(int B, int nkv, int nqg, int sms, int max_keys) {
-  const int ctas = B * nkv * nqg;
-  int s = (2 * sms + ctas - 1) / ctas;
+  const int pairs = B * nkv * nqg;
+  int s = (kAttnItemsPerSm * sms + pairs - 1) / pairs;
   if (max_keys > 0) {
     const int by_len = (max_keys + 127) / 128;
     if (s > by_len) s = by_len;
@@ -847,41 +1086,37 @@ int attn_splits(int B, int nkv, int nqg, int sms, int max_keys) {
   return s;
 }
 
-// Upper bound of the split count for any call with M rows: every CTA serves at
-// most 32 query slots, so a pass has at least nkv * ceil(M * G / 32) CTAs.
+// Upper bound of the split count for any call with M rows: a work item serves
+// at most 32 query slots, so a pass has at least nkv * ceil(M * G / 32) pairs.
 int attn_splits_max(const spec_model_desc& d, int M, int sms) {
   const int G = d.n_q_heads / d.n_kv_heads;
-  const int min_ctas = d.n_kv_heads * ((M * G + 31) / 32);
-  int s = (2 * sms + min_ctas - 1) / min_ctas;
+  const int min_pairs = d.n_kv_heads * ((M * G + 31) / 32);
+  int s = (kAttnItemsPerSm * sms + min_pairs - 1) / min_pairs;
   if (s < 1) s = 1;
   if (s > 64) s = 64;
   return s;
-}
-
-size_t attn_smem_bytes(int dtype, int hd, int qmax) {
-  const size_t es = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
-  const size_t kp = hd + 16 / es;
-  return (size_t)qmax * hd * 4 + (size_t)qmax * 128 * 4 + 128 * kp * es + 128 * hd * es;
 }
 
 template <typename TT, int HDV, int QM>
 static spec_status attn_launch(const spec_model_desc& d, const RowInfo& ri, const spec_rows& rows, const void* qbuf,
                                const spec_kv& kv, float* opart, float2* mlpart, void* attn_out, int nsplit, int nqg,
                                void* ws, cudaStream_t st) {
-  static int attr_dev = -1;
+  static int attr_dev = -1, occ = 1;
   int dev = 0;
   cudaGetDevice(&dev);
-  const size_t smem = attn_smem_bytes(d.dtype, HDV, QM);
+  constexpr size_t smem = attn_smem_for<TT, HDV, QM>();
+  auto kern = attn_split_kernel<TT, HDV, QM>;
   if (attr_dev != dev) {
-    if (cudaFuncSetAttribute(attn_split_kernel<TT, HDV, QM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return SPEC_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 128, smem) != cudaSuccess || occ < 1) occ = 1;
     attr_dev = dev;
   }
-  dim3 grid(nsplit, d.n_kv_heads, rows.B * nqg);
+  const int n_items = nsplit * d.n_kv_heads * rows.B * nqg;
+  const int grid = std::min(n_items, occ * sm_count());
   const float scale = 1.f / sqrtf((float)d.head_dim);
-  launch_pdl(attn_split_kernel<TT, HDV, QM>, dim3(grid), dim3(128), smem, st, (const TT*)qbuf, kv, ri, d.n_q_heads, d.n_kv_heads,
-                                                          d.window, nsplit, nqg, scale, opart, mlpart, ws);
+  launch_pdl(kern, dim3(grid), dim3(128), smem, st, (const TT*)qbuf, kv, ri, d.n_q_heads, d.n_kv_heads, d.window,
+             nsplit, nqg, n_items, scale, opart, mlpart, ws);
   launch_pdl(attn_combine_kernel<TT, HDV>, dim3(rows.M * d.n_q_heads), dim3(HDV), 0, st, opart, mlpart, d.n_q_heads, nsplit,
                                                                      (TT*)attn_out);
   return SPEC_OK;
@@ -930,7 +1165,14 @@ void launch_row_stats(const float* logits, int M, int V, int k, int32_t* ids, in
 }
 
 void launch_topk_select(const float* s, int M, int V, int Kc, int32_t* out_ids, cudaStream_t st) {
-  launch_pdl(topk_select_kernel, dim3(M), dim3(1024), 0, st, s, V, Kc, out_ids);
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)topk_select_smem());
+    attr_dev = dev;
+  }
+  launch_pdl(topk_select_kernel, dim3(M), dim3(1024), topk_select_smem(), st, s, V, Kc, out_ids);
 }
 
 void launch_rescore(int dtype, const void* hn, const void* lm_head, int H, int V, const int32_t* cand, int M, int Kc,
