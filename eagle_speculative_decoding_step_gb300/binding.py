@@ -33,11 +33,11 @@ class ModelDesc(ctypes.Structure):
     _fields_ = [("hidden", c_i32), ("n_q_heads", c_i32), ("n_kv_heads", c_i32), ("head_dim", c_i32),
                 ("intermediate", c_i32), ("vocab", c_i32), ("dtype", c_i32), ("rms_eps", ctypes.c_float),
                 ("rope_theta", ctypes.c_float), ("window", c_i32), ("rank", c_i32), ("num_candidates", c_i32),
-                ("draft_vocab", c_i32)]
+                ("draft_vocab", c_i32), ("fc_norm", c_i32), ("norm_output", c_i32)]
 
 
 _WEIGHT_NAMES = ["fc", "embed", "hidden_norm", "in_norm", "post_norm", "final_norm", "wq", "wk", "wv", "wo",
-                 "wgate", "wup", "wdown", "lm_head", "lr_down", "lr_up", "d2t"]
+                 "wgate", "wup", "wdown", "lm_head", "lr_down", "lr_up", "d2t", "fc_norm"]
 
 
 class Weights(ctypes.Structure):
@@ -134,7 +134,8 @@ def _check(st, what):
 def make_desc(w) -> ModelDesc:
     """ModelDesc from a workload (configs.Workload)."""
     return ModelDesc(w.H, w.nq, w.nkv, w.hd, w.I, w.V, DTYPE_BF16 if w.dtype == "bf16" else DTYPE_F32,
-                     w.rms_eps, w.rope_theta, w.window, w.rank, w.num_candidates, w.draft_vocab)
+                     w.rms_eps, w.rope_theta, w.window, w.rank, w.num_candidates, w.draft_vocab,
+                     int(getattr(w, "fc_norm", False)), int(getattr(w, "norm_output", False)))
 
 
 def make_weights(W: dict) -> Weights:

@@ -19,6 +19,8 @@ void launch_epi_qkv(const spec_model_desc&, const float*, const SKPlan&, const s
 void launch_epi_oproj(const spec_model_desc&, const float*, const SKPlan&, const spec_rows&, const void*,
                       const spec_weights&, float*, void*, cudaStream_t);
 void launch_epi_swiglu(const spec_model_desc&, const float*, const SKPlan&, int, void*, cudaStream_t);
+void launch_epi_fcnorm(const spec_model_desc&, const float*, const SKPlan&, int, float*, const void*, void*,
+                       cudaStream_t);
 void launch_epi_down(const spec_model_desc&, const float*, const SKPlan&, int, float*, const spec_weights&, void*,
                      void*, cudaStream_t);
 void launch_simt_gemm(int, const void*, const void*, const void*, int, const void*, int, const SKPlan&, float*,
@@ -244,6 +246,7 @@ extern "C" spec_status spec_fc_fuse(const spec_model_desc* desc, const spec_weig
   if (s != SPEC_OK) return s;
   if (!w || !w->fc || !aux || !h0) return SPEC_ERR_ARG;
   const spec_model_desc& d = *desc;
+  if (d.fc_norm && !w->fc_norm) return SPEC_ERR_ARG;
   if (M <= 0 || M > max_rows_for(d)) return SPEC_ERR_SHAPE;
   if (!aligned(aux, 16) || !aligned(h0, 16) || !aligned(w->fc, 16)) return SPEC_ERR_ALIGN;
   WsLayout L;
@@ -251,7 +254,10 @@ extern "C" spec_status spec_fc_fuse(const spec_model_desc* desc, const spec_weig
   float* part = at<float>(ws, L.part);
   SKPlan p;
   if ((s = gemm(d, {w->fc}, {d.hidden}, 3 * d.hidden, aux, M, part, ws, stream, &p)) != SPEC_OK) return s;
-  launch_epi_store(d.dtype, part, p, M, d.hidden, h0, d.hidden, stream);
+  if (d.fc_norm)
+    launch_epi_fcnorm(d, part, p, M, at<float>(ws, L.r1), w->fc_norm, h0, stream);
+  else
+    launch_epi_store(d.dtype, part, p, M, d.hidden, h0, d.hidden, stream);
   return last_launch();
 }
 

@@ -79,6 +79,7 @@ class ChainStep:
         self.h0 = dm.hidden(B)
         self.pre = [dm.hidden(B), dm.hidden(B)]
         self.hn = dm.hidden(B)
+        self.hns = [self.hn, dm.hidden(B)] if w.norm_output else [self.hn]
         self.drafts = torch.zeros(B, K, dtype=torch.int32, device=dev)
         self.lp = torch.zeros(B, K, dtype=torch.float32, device=dev)
         self.out = torch.zeros(B, K + 1, dtype=torch.int32, device=dev)
@@ -101,14 +102,16 @@ class ChainStep:
                 rows = lib.make_rows(B, B, 1, dm.ctx_len, self.drafts.data_ptr() + 4 * (i - 1), step=i,
                                      tok_stride=K, max_ctx=w.max_ctx)
             out = self.pre[i % 2]
-            lib.spec_draft_layer(dm.desc, dm.weights, rows, hid, out, self.hn, dm.kv, dm.ws)
+            # EAGLE-3.1 norm_output: the next pass takes the normalised state (two buffers)
+            hn = self.hns[i % 2] if w.norm_output else self.hn
+            lib.spec_draft_layer(dm.desc, dm.weights, rows, hid, out, hn, dm.kv, dm.ws)
             ids = self.drafts.data_ptr() + 4 * i
             if w.rank > 0:
-                lib.spec_lowrank_candidates(dm.desc, dm.weights, self.hn, B, 1, ids, ws=dm.ws, out_ld=K)
+                lib.spec_lowrank_candidates(dm.desc, dm.weights, hn, B, 1, ids, ws=dm.ws, out_ld=K)
             else:
-                lib.spec_lm_head(dm.desc, dm.weights, self.hn, B, 1, ids, self.lp.data_ptr() + 4 * i, ws=dm.ws,
+                lib.spec_lm_head(dm.desc, dm.weights, hn, B, 1, ids, self.lp.data_ptr() + 4 * i, ws=dm.ws,
                                  ids_ld=K)
-            hid = out
+            hid = hn if w.norm_output else out
 
     def verify(self):
         w = self.dm.w
@@ -138,6 +141,7 @@ class TreeStep:
         self.h0 = dm.hidden(B)
         self.pre = [dm.hidden(B * k), dm.hidden(B * k)]
         self.hn = dm.hidden(B * k)
+        self.hns = [self.hn, dm.hidden(B * k)]
         self.ids = torch.zeros(B * k, k, dtype=torch.int32, device=dev)
         self.lp = torch.zeros(B * k, k, dtype=torch.float32, device=dev)
         i32 = dict(dtype=torch.int32, device=dev)
@@ -164,25 +168,27 @@ class TreeStep:
         dm, B, k, D, N = self.dm, self.B, self.k, self.D, self.N
         lib.spec_fc_fuse(dm.desc, dm.weights, self.aux, self.h0, B, dm.ws)
         rows = lib.make_rows(B, B, 1, dm.ctx_len, self.root, step=0, max_ctx=dm.w.max_ctx)
-        lib.spec_draft_layer(dm.desc, dm.weights, rows, self.h0, self.pre[0], self.hn, dm.kv, dm.ws)
-        self._head(B)
+        no = dm.w.norm_output          # EAGLE-3.1: children take the parent's normalised state
+        lib.spec_draft_layer(dm.desc, dm.weights, rows, self.h0, self.pre[0], self.hns[0], dm.kv, dm.ws)
+        self._head(B, self.hns[0])
         lib.spec_tree_expand(B, k, 1, D, N, dm.ctx_len, self.root, self.ids, self.lp, self.state, self.io)
         for d in range(2, D + 1):
             rows = lib.make_rows(B * k, B, k, dm.ctx_len, self.f_tok, pos=self.f_pos, kv_idx=self.f_kv,
                                  mask=self.f_mask, hid_src=self.f_src, max_ctx=dm.w.max_ctx)
             src, dst = self.pre[d % 2], self.pre[(d + 1) % 2]
-            lib.spec_draft_layer(dm.desc, dm.weights, rows, src, dst, self.hn, dm.kv, dm.ws)
-            self._head(B * k)
+            hsrc, hdst = self.hns[d % 2], self.hns[(d + 1) % 2]
+            lib.spec_draft_layer(dm.desc, dm.weights, rows, hsrc if no else src, dst, hdst, dm.kv, dm.ws)
+            self._head(B * k, hdst)
             lib.spec_tree_expand(B, k, d, D, N, dm.ctx_len, self.root, self.ids, self.lp, self.state, self.io)
 
-    def _head(self, M):
+    def _head(self, M, hn):
         """top-k ids and log-probs per row: full LM head, or the EAGLE-4 candidate head
         (log-probs over its rescored candidates)."""
         dm, k = self.dm, self.k
         if dm.w.rank > 0:
-            lib.spec_lowrank_candidates(dm.desc, dm.weights, self.hn, M, k, self.ids, ws=dm.ws, out_logprob=self.lp)
+            lib.spec_lowrank_candidates(dm.desc, dm.weights, hn, M, k, self.ids, ws=dm.ws, out_logprob=self.lp)
         else:
-            lib.spec_lm_head(dm.desc, dm.weights, self.hn, M, k, self.ids, self.lp, ws=dm.ws)
+            lib.spec_lm_head(dm.desc, dm.weights, hn, M, k, self.ids, self.lp, ws=dm.ws)
 
     def verify(self, compact=True):
         dm = self.dm
@@ -225,6 +231,7 @@ class PrefillChainStep:
         self.hn_all = dm.hidden(M)
         self.pre = [dm.hidden(B), dm.hidden(B)]
         self.hn = dm.hidden(B)
+        self.hns = [self.hn, dm.hidden(B)]
         self.drafts = torch.zeros(B, K, **i32)
         self.lp = torch.zeros(B, K, dtype=torch.float32, device=dev)
         self.out = torch.zeros(B, K + 1, **i32)
@@ -245,15 +252,17 @@ class PrefillChainStep:
         lib.spec_gather_rows(self.hn_all, M, w.H * es, self.last_row, B, self.hn, ws=dm.ws)
         lib.spec_gather_rows(self.pre_all, M, w.H * es, self.last_row, B, self.pre[1], ws=dm.ws)
         lib.spec_lm_head(dm.desc, dm.weights, self.hn, B, 1, self.drafts, self.lp, ws=dm.ws, ids_ld=K)
-        hid = self.pre[1]
+        # EAGLE-3.1 norm_output: the recurrent passes take the normalised state
+        hid = self.hn if w.norm_output else self.pre[1]
         for i in range(1, K):
             rows = lib.make_rows(B, B, 1, self.ctx_next, self.drafts.data_ptr() + 4 * (i - 1), step=i - 1,
                                  tok_stride=K, max_ctx=w.max_ctx + R)
             out = self.pre[(i + 1) % 2]
-            lib.spec_draft_layer(dm.desc, dm.weights, rows, hid, out, self.hn, dm.kv, dm.ws)
-            lib.spec_lm_head(dm.desc, dm.weights, self.hn, B, 1, self.drafts.data_ptr() + 4 * i,
+            hn = self.hns[i % 2]
+            lib.spec_draft_layer(dm.desc, dm.weights, rows, hid, out, hn, dm.kv, dm.ws)
+            lib.spec_lm_head(dm.desc, dm.weights, hn, B, 1, self.drafts.data_ptr() + 4 * i,
                              self.lp.data_ptr() + 4 * i, ws=dm.ws, ids_ld=K)
-            hid = out
+            hid = hn if w.norm_output else out
 
     def verify(self):
         lib.spec_verify_greedy(self.B, self.K + 1, self.V, self.target, self.drafts, self.out, self.acc, self.kv_src,

@@ -82,6 +82,16 @@ typedef struct {
                              reduced vocabulary ([QUARK] calibrate_draft_vocab,
                              draft_vocab_size; [EAGLE4] selected_token_ids);
                              0 = the full vocabulary.  Needs weights.d2t. */
+  int32_t fc_norm;        /* EAGLE-3.1 ([QUARK] "Background: EAGLE-3 and
+                             EAGLE-3.1", eagle_architecture_config.fc_norm):
+                             nonzero = spec_fc_fuse ends with an RMSNorm of the
+                             fused feature, gain weights.fc_norm.  The page names
+                             the flag only; this is the reading implemented. */
+  int32_t norm_output;    /* EAGLE-3.1 norm_output: nonzero = the caller feeds the
+                             normalised output (hid_normed) of a draft pass, not
+                             hidden_prenorm, to the next pass.  No library call
+                             changes with it; the step sequences built on the
+                             library (the Python engine) read it. */
 } spec_model_desc;
 
 /* Draft weights, device pointers, dtype of the descriptor.  [NEURON] "Eagle3
@@ -108,6 +118,7 @@ typedef struct {
   const int32_t *d2t;      /* [draft_vocab] target token id of each draft-vocabulary
                               entry (draft_vocab > 0); lm_head is then
                               [draft_vocab, H] */
+  const void *fc_norm;     /* [H] gain of the RMSNorm after the FC (desc.fc_norm) */
 } spec_weights;
 
 /* Paged K/V cache of the draft layer ([NEURON] "KV Cache Sharing" and

@@ -24,7 +24,9 @@ def _chain_case(w):
 
 
 @pytest.mark.parametrize("w", [configs.WORKLOADS["tiny"], SMALL_BF16,
-                               replace(SMALL_BF16, name="small_rej", verify="rejection", sigma=1.5, K=4)],
+                               replace(SMALL_BF16, name="small_rej", verify="rejection", sigma=1.5, K=4),
+                               replace(configs.WORKLOADS["tiny"], name="tiny_eagle31", fc_norm=True, norm_output=True),
+                               replace(SMALL_BF16, name="small_eagle31", fc_norm=True, norm_output=True)],
                          ids=lambda w: w.name)
 def test_chain_step(w):
     W, ctx, kv, dm, aux, root, target = _chain_case(w)
@@ -49,8 +51,10 @@ def test_chain_step(w):
     no_device_error(dm)
 
 
-def test_tree_step():
-    w = replace(SMALL_BF16, name="small_tree", mode="tree", top_k=4, depth=3, total=10, B=2)
+@pytest.mark.parametrize("eagle31", [False, True], ids=["eagle3", "eagle31"])
+def test_tree_step(eagle31):
+    w = replace(SMALL_BF16, name="small_tree", mode="tree", top_k=4, depth=3, total=10, B=2, fc_norm=eagle31,
+                norm_output=eagle31)
     W, ctx, kv, dm = setup(w, max_rows=w.B * w.top_k)
     aux = synth.make_aux(w)
     root = synth.root_tokens(w)
