@@ -20,8 +20,9 @@ import numpy as np
 from . import draft, tree, verify
 
 
-def chain_draft(desc, W, aux, root_tok, ctx_len, kv, K, keep_logits=False):
-    """Returns drafts [B, K] and, with keep_logits, the per-pass logits [B, K, V]."""
+def chain_draft(desc, W, aux, root_tok, ctx_len, kv, K, keep_logits=False, trace=None):
+    """Returns drafts [B, K] and, with keep_logits, the per-pass logits [B, K, V].
+    ``trace``, if a list, receives each pass's normalised output hn [B, H]."""
     B = len(root_tok)
     hid = draft.fc_fuse(desc, W, aux)
     tok = np.asarray(root_tok, dtype=np.int64)
@@ -31,6 +32,8 @@ def chain_draft(desc, W, aux, root_tok, ctx_len, kv, K, keep_logits=False):
         rows = {"M": B, "B": B, "R": 1, "step": i, "ctx_len": ctx_len, "tok": tok}
         prenorm, hn = draft.draft_layer(desc, W, rows, hid, kv)
         hid = draft.recurrent_state(desc, prenorm, hn)
+        if trace is not None:
+            trace.append(hn)
         if desc.rank > 0:
             _, _, ids = draft.lowrank_candidates(desc, W, hn, desc.num_candidates, 1)
             lg = None

@@ -26,6 +26,15 @@ def _sub_kv(kv, idx):
     return s
 
 
+def _candidate_boundary_margin(w, W64, hn, ids):
+    """Smallest distance of the ids' low-rank scores from the Kc-th largest score
+    (the oracle's scores for this row)."""
+    z = od._r(np.asarray(hn, np.float64)[None] @ W64["lr_down"].T, w.dtype)
+    s = (z @ W64["lr_up"].T)[0]
+    kth = np.partition(s, -w.num_candidates)[-w.num_candidates]
+    return min(abs(s[i] - kth) for i in ids)
+
+
 def _graph_run(step):
     step.run()
     torch.cuda.synchronize()
@@ -62,7 +71,9 @@ def test_chain_full_size(name, sample):
     st = engine.ChainStep(dm, dev_act(aux, w), dev(root), dev(target), temperature=dev(temp), seed=w.philox_seed)
     _graph_run(st)
     assert dm.device_error() == 0
-    drafts_ref, logits_ref = ostep.chain_draft(w, W64, aux[idx], root[idx], ctx[idx], sub_kv, w.K, keep_logits=True)
+    hn_ref = []
+    drafts_ref, logits_ref = ostep.chain_draft(w, W64, aux[idx], root[idx], ctx[idx], sub_kv, w.K, keep_logits=True,
+                                               trace=hn_ref)
     drafts = st.drafts.cpu().numpy()[idx]
     out = st.out.cpu().numpy()[idx]
     acc = st.acc.cpu().numpy()[idx]
@@ -76,9 +87,16 @@ def test_chain_full_size(name, sample):
         tie = False
         for i in range(w.K):
             if drafts[j, i] != drafts_ref[j, i]:
-                gap = abs(logits_ref[j, i, drafts[j, i]] - logits_ref[j, i, drafts_ref[j, i]])
-                assert gap < BF16_ATOL, "request %d step %d: id %d vs %d, gap %.3g" % (idx[j], i, drafts[j, i],
-                                                                                      drafts_ref[j, i], gap)
+                g, r = int(drafts[j, i]), int(drafts_ref[j, i])
+                gap = abs(logits_ref[j, i, g] - logits_ref[j, i, r])
+                if w.rank > 0 and gap >= BF16_ATOL:
+                    # candidate head: the ids may differ because one of them sits at the
+                    # boundary of the low-rank top-Kc (a near-tie of the scores there)
+                    bm = _candidate_boundary_margin(w, W64, hn_ref[i][j], (g, r))
+                    assert bm < BF16_ATOL, "request %d step %d: id %d vs %d, logit gap %.3g, candidate-boundary " \
+                        "margin %.3g" % (idx[j], i, g, r, gap, bm)
+                else:
+                    assert gap < BF16_ATOL, "request %d step %d: id %d vs %d, gap %.3g" % (idx[j], i, g, r, gap)
                 tie = True
                 break
         if tie:
