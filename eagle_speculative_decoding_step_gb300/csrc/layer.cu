@@ -595,6 +595,327 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const T* __restrict__ q
   }
 }
 
+// ---------------------------------------------------------------- attention on tensor cores (bf16)
+// Same work items, persistent grid and two-stage cp.async ring of 64-key tiles
+// as attn_split_kernel, but the two products run as warp-level bf16 MMAs
+// (m16n8k16, fp32 accumulate): the item's up to 16*MT queries are the MMA rows
+// (padded with zero rows), warp w owns keys 16w .. 16w+15 of every tile and
+// keeps its own running max / sum / output for them (no cross-warp exchange
+// per tile); the four warps' results merge once per item.  Scores:
+// S[q, key] = Q[q, :] . K[key, :] with K rows as the "col" operand; the
+// probabilities P (bf16) go straight from the score accumulators into the
+// P.V product's A operand; V tiles are read transposed by ldmatrix.
+constexpr int kMmaTK = 64;
+
+template <int HD> struct MmaShape {
+  static constexpr int KP = HD + 8;                         // padded bf16 row: ldmatrix rows on distinct banks
+  static constexpr int STAGE = 2 * kMmaTK * KP * 2;          // K and V tiles
+};
+
+template <int HD, int MT>
+constexpr size_t attn_mma_smem() {
+  using S = MmaShape<HD>;
+  const size_t ring = (size_t)2 * S::STAGE;
+  const size_t red = (size_t)4 * 16 * MT * HD * 4;            // the warps' outputs after the last tile (aliases the ring)
+  return (ring > red ? ring : red) + (size_t)16 * MT * S::KP * 2 + (size_t)2 * kMmaTK * 4;
+}
+
+SPEC_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+SPEC_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+SPEC_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+SPEC_DEV void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+SPEC_DEV uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int HD, int MT>
+__global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __restrict__ qbuf, spec_kv kv, RowInfo ri,
+                                                       int nq, int nkv, int window, int nsplit, int nqg,
+                                                       int n_items, float scale_log2, float* __restrict__ opart,
+                                                       float2* __restrict__ mlpart, void* ws) {
+  pdl_wait();
+  pdl_trigger();
+  using Sh = MmaShape<HD>;
+  constexpr int TK = kMmaTK, KP = Sh::KP, CH = HD / 8, QM = 16 * MT, NT = HD / 8, KS = HD / 16;
+  extern __shared__ __align__(16) uint8_t mma_smem[];
+  constexpr size_t kRing = attn_mma_smem<HD, MT>() - (size_t)QM * KP * 2 - (size_t)2 * TK * 4;
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(mma_smem + kRing);   // [QM][KP]
+  int* sCi = reinterpret_cast<int*>(sQ + QM * KP);                          // [2][TK] cache index, -1 = no slot
+  float* red = reinterpret_cast<float*>(mma_smem);                           // [4][QM][HD]
+  __shared__ float sMw[4][QM], sLw[4][QM];
+  __shared__ int s_lo[QM];
+  __shared__ unsigned long long s_mask[QM];
+  __shared__ int s_klo, s_nd;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int grp = lane >> 2, tig = lane & 3;
+  const int G = nq / nkv;
+  const int nQall = ri.R * G;
+  // stale ring contents must be finite (P = 0 times a stale V must stay 0)
+  for (int e = tid; e < (int)(kRing / 16); e += blockDim.x) reinterpret_cast<uint4*>(mma_smem)[e] = make_uint4(0, 0, 0, 0);
+
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int s = item % nsplit;
+    const int g = (item / nsplit) % nkv;
+    const int bq = item / (nsplit * nkv);
+    const int b = bq / nqg, qg = bq % nqg;
+    const int q0 = qg * QM;
+    const int nQ = min(QM, nQall - q0);
+    const int ctx = ri.ctx_len[b];
+
+    if (tid < 32) {
+      int lo = 0x7fffffff;
+      unsigned long long mk = 0;
+      if (tid < nQ) {
+        const int m = b * ri.R + (q0 + tid) / G;
+        const int pos = row_pos(ri, m);
+        lo = window > 0 ? max(0, pos - window + 1) : 0;
+        if (lo > ctx) lo = ctx;
+        mk = row_mask(ri, m);
+      }
+      if (tid < QM) {
+        s_lo[tid] = lo;
+        s_mask[tid] = mk;
+      }
+      int mlo = lo;
+      unsigned long long om = mk;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mlo = min(mlo, __shfl_xor_sync(0xffffffffu, mlo, o));
+        om |= __shfl_xor_sync(0xffffffffu, om, o);
+      }
+      if (tid == 0) {
+        s_klo = mlo;
+        s_nd = om ? 64 - __clzll((long long)om) : 0;
+      }
+    }
+    // queries of the item (bf16, unscaled), zero rows past nQ
+    for (int e = tid; e < QM * CH; e += blockDim.x) {
+      const int qi = e / CH, c = e % CH;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (qi < nQ) {
+        const int q = q0 + qi;
+        const int m = b * ri.R + q / G, h = g * G + q % G;
+        v = *reinterpret_cast<const uint4*>(qbuf + ((size_t)m * nq + h) * HD + c * 8);
+      }
+      *reinterpret_cast<uint4*>(sQ + qi * KP + c * 8) = v;
+    }
+    __syncthreads();
+    const int klo = s_klo, nd = s_nd;
+    const int nctx = ctx - klo;
+    const int total = nctx + nd;
+    const int chunk = ((total + nsplit - 1) / nsplit + TK - 1) / TK * TK;
+    const int kbeg = min(total, s * chunk), kend = min(total, kbeg + chunk);
+    const int ntiles = (kend - kbeg + TK - 1) / TK;
+
+    auto issue = [&](int j) {
+      if (j < ntiles) {
+        uint8_t* st = mma_smem + (size_t)(j & 1) * Sh::STAGE;
+        __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(st);
+        __nv_bfloat16* sV = sK + TK * KP;
+        const int t0 = kbeg + j * TK;
+        const int nk = min(TK, kend - t0);
+        const int ch = tid % CH;
+        for (int kt = tid / CH; kt < TK; kt += 128 / CH) {
+          uint4* dk = reinterpret_cast<uint4*>(sK + kt * KP) + ch;
+          uint4* dv = reinterpret_cast<uint4*>(sV + kt * KP) + ch;
+          int ci = -1;
+          long long slot = -1;
+          if (kt < nk) {
+            const int kidx = t0 + kt;
+            ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
+            slot = slot_of(kv, b, ci);
+          }
+          if (slot >= 0) {
+            const size_t off = ((size_t)slot * nkv + g) * HD;
+            cp_async16(dk, reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(kv.k) + off) + ch);
+            cp_async16(dv, reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(kv.v) + off) + ch);
+          } else {
+            *dk = make_uint4(0, 0, 0, 0);
+            *dv = make_uint4(0, 0, 0, 0);
+          }
+          if (ch == 0) sCi[(j & 1) * TK + kt] = slot >= 0 ? ci : -1;
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    float acc[MT][NT][4];
+    float mrun[MT][2], lrun[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mt][n][e] = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) { mrun[mt][h] = -INFINITY; lrun[mt][h] = 0.f; }
+    }
+    const uint32_t qbase = smem_u32(sQ);
+
+    issue(0);
+    for (int j = 0; j < ntiles; ++j) {
+      issue(j + 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      __syncthreads();
+      const uint8_t* st = mma_smem + (size_t)(j & 1) * Sh::STAGE;
+      const uint32_t kbase = smem_u32(st), vbase = kbase + TK * KP * 2;
+      const int* ci_t = sCi + (j & 1) * TK;
+      // scores for this warp's 16 keys: S[mt][nt] (16 queries x 8 keys)
+      float sc[MT][2][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t b0, b1, b2, b3;   // keys 16w + {0..7, 8..15} x dims ks*16 + {0..7, 8..15}
+        {
+          const int blk = lane >> 3, i = lane & 7;
+          const int key = warp * 16 + 8 * (blk >> 1) + i, dim = ks * 16 + 8 * (blk & 1);
+          ldsm_x4(kbase + (uint32_t)(key * KP + dim) * 2, b0, b1, b2, b3);
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          const int blk = lane >> 3, i = lane & 7;
+          const int row = mt * 16 + 8 * (blk & 1) + i, dim = ks * 16 + 8 * (blk >> 1);
+          ldsm_x4(qbase + (uint32_t)(row * KP + dim) * 2, a0, a1, a2, a3);
+          mma_bf16(sc[mt][0], a0, a1, a2, a3, b0, b1);
+          mma_bf16(sc[mt][1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+      // mask, scale to log2 units, warp-local online softmax
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int qi = mt * 16 + grp + 8 * h;
+          const bool qok = qi < nQ;
+          const int qlo = s_lo[qi];
+          const unsigned long long qmask = s_mask[qi];
+          float mx = -INFINITY;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int kt = warp * 16 + nt * 8 + 2 * tig + e;
+              const int ci = ci_t[kt];
+              bool ok = qok && ci >= 0;
+              if (ok) ok = ci < ctx ? ci >= qlo : ((qmask >> (ci - ctx)) & 1ull) != 0;
+              const float v = ok ? sc[mt][nt][2 * h + e] * scale_log2 : -INFINITY;
+              sc[mt][nt][2 * h + e] = v;
+              mx = fmaxf(mx, v);
+            }
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const float mnew = fmaxf(mrun[mt][h], mx);
+          const float al = mnew == -INFINITY ? 1.f : exp2f(mrun[mt][h] - mnew);
+          float ps = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float p = mnew == -INFINITY ? 0.f : exp2f(sc[mt][nt][2 * h + e] - mnew);
+              sc[mt][nt][2 * h + e] = p;
+              ps += p;
+            }
+          lrun[mt][h] = lrun[mt][h] * al + ps;
+          mrun[mt][h] = mnew;
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            acc[mt][n][2 * h] *= al;
+            acc[mt][n][2 * h + 1] *= al;
+          }
+        }
+      }
+      // P.V: A = P (queries x this warp's 16 keys), B = V^T via transposed ldmatrix
+#pragma unroll
+      for (int n2 = 0; n2 < NT / 2; ++n2) {
+        uint32_t v0, v1, v2, v3;   // keys 16w + {0..7, 8..15} x dims 16*n2 + {0..7, 8..15}
+        {
+          const int blk = lane >> 3, i = lane & 7;
+          const int key = warp * 16 + 8 * (blk & 1) + i, dim = n2 * 16 + 8 * (blk >> 1);
+          ldsm_x4_t(vbase + (uint32_t)(key * KP + dim) * 2, v0, v1, v2, v3);
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint32_t a0 = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
+          const uint32_t a1 = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
+          const uint32_t a2 = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
+          const uint32_t a3 = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
+          mma_bf16(acc[mt][2 * n2], a0, a1, a2, a3, v0, v1);
+          mma_bf16(acc[mt][2 * n2 + 1], a0, a1, a2, a3, v2, v3);
+        }
+      }
+      __syncthreads();     // ring slot j & 1 is refilled by the next iteration's copies
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    // merge the four warps: row sums over the quad, then max / rescale through shared memory
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float l = lrun[mt][h];
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        if (tig == 0) {
+          sMw[warp][mt * 16 + grp + 8 * h] = mrun[mt][h];
+          sLw[warp][mt * 16 + grp + 8 * h] = l;
+        }
+      }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int row = mt * 16 + grp + 8 * h;
+          *reinterpret_cast<float2*>(red + ((size_t)warp * QM + row) * HD + n * 8 + 2 * tig) =
+              make_float2(acc[mt][n][2 * h], acc[mt][n][2 * h + 1]);
+        }
+    __syncthreads();
+    for (int e = tid; e < QM * HD; e += blockDim.x) {
+      const int qi = e / HD, d = e % HD;
+      if (qi >= nQ) continue;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) M = fmaxf(M, sMw[w][qi]);
+      float o = 0.f, L = 0.f;
+      if (M > -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float f = exp2f(sMw[w][qi] - M);
+          o += red[((size_t)w * QM + qi) * HD + d] * f;
+          L += sLw[w][qi] * f;
+        }
+      }
+      const int q = q0 + qi;
+      const int m = b * ri.R + q / G, h = g * G + q % G;
+      const size_t base = ((size_t)m * nq + h) * nsplit + s;
+      opart[base * HD + d] = o;
+      // the combine kernel takes natural-log maxima of the scaled scores
+      if (d == 0) mlpart[base] = make_float2(M == -INFINITY ? -INFINITY : M * 0.69314718055994531f, L);
+    }
+    __syncthreads();     // red / sQ / sMw reused by the next item
+  }
+}
+
 template <typename T, int HD>
 __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restrict__ opart,
                                                           const float2* __restrict__ mlpart, int nq, int nsplit,
@@ -737,14 +1058,34 @@ SPEC_DEV uint32_t radix_select(const float* x, const uint32_t* keys, int n, int 
       }
     }
     __syncthreads();
-    if (tid == 0) {
-      int nn = *s_need, acc = 0, dsel = 0;
-      for (int dg = 255; dg >= 0; --dg) {
-        if (acc + hist[dg] >= nn) { dsel = dg; break; }
-        acc += hist[dg];
+    if (tid < 32) {
+      // lane l owns digits 255-8l .. 248-8l; count of elements above the lane's
+      // digits = suffix sum over the lanes before it
+      const int nn = *s_need;
+      int hv[8], c = 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        hv[u] = hist[255 - 8 * lane - u];
+        c += hv[u];
       }
-      *s_need = nn - acc;
-      *s_prefix = pf | ((uint32_t)dsel << lo);
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int before = incl - c;
+      const bool mine = before < nn && incl >= nn;
+      if (mine) {
+        int acc = before, dsel = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (acc + hv[u] >= nn) { dsel = 255 - 8 * lane - u; break; }
+          acc += hv[u];
+        }
+        *s_need = nn - acc;
+        *s_prefix = pf | ((uint32_t)dsel << lo);
+      }
     }
     __syncthreads();
   }
@@ -769,42 +1110,75 @@ __global__ void __launch_bounds__(1024) topk_select_kernel(const float* __restri
   const float* x = s + (size_t)m * V;
   const int tid = threadIdx.x, lane = tid & 31;
   if (tid == 0) { s_nsel = 0; s_nc = 0; }
+  // The row in groups of four consecutive elements (16-byte loads), group
+  // g = base + u * 1024 + tid; UNR groups (4 * UNR loads) in flight per thread.
+  constexpr int UNR = 4;
+  const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0);
+  const int ng = (V + 3) / 4;
+  auto load4 = [&](int gi, float* v) {
+    if (gi >= ng) {
+      v[0] = v[1] = v[2] = v[3] = -INFINITY;
+    } else if (vec) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(x) + gi);
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = 4 * gi + e < V ? x[4 * gi + e] : -INFINITY;
+    }
+  };
   // 1. per-thread maxima, then T0 = the Kc-th largest of them
   uint32_t tmax = 0;
-  for (int base = 0; base < V; base += 4 * blockDim.x) {
-    float v[4];
+  for (int base = 0; base < ng; base += UNR * blockDim.x) {
+    float v[UNR][4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = base + u * blockDim.x + tid;
-      v[u] = i < V ? x[i] : -INFINITY;
-    }
+    for (int u = 0; u < UNR; ++u) load4(base + u * blockDim.x + tid, v[u]);
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (base + u * blockDim.x + tid < V) tmax = max(tmax, order_key(v[u]));
+    for (int u = 0; u < UNR; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (4 * (base + u * blockDim.x + tid) + e < V) tmax = max(tmax, order_key(v[u][e]));
   }
   skey[tid] = tmax;           // 0 for a thread without elements: below every key
   __syncthreads();
   int tie_need;
   const uint32_t t0 = radix_select<true>(nullptr, skey, blockDim.x, Kc, hist, &s_prefix, &s_need, &tie_need);
-  // 2. copy the elements >= T0 (warp-aggregated slots)
-  for (int base = 0; base < V; base += blockDim.x) {
-    const int i = base + tid;
-    uint32_t k = 0;
-    bool take = false;
-    if (i < V) {
-      k = order_key(x[i]);
-      take = k >= t0;
-    }
-    const unsigned bal = __ballot_sync(0xffffffffu, take);
-    if (bal) {
-      int slot0 = 0;
-      if (lane == 0) slot0 = atomicAdd(&s_nc, __popc(bal));
-      slot0 = __shfl_sync(0xffffffffu, slot0, 0);
-      const int p = slot0 + __popc(bal & ((1u << lane) - 1u));
-      if (take && p < kTkCap) {
-        ckey[p] = k;
-        cidx[p] = i;
+  // 2. copy the elements >= T0 (one shared counter update per warp and round)
+  for (int base = 0; base < ng; base += UNR * blockDim.x) {
+    float v[UNR][4];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) load4(base + u * blockDim.x + tid, v[u]);
+    uint32_t takem = 0;
+    int cnt = 0;
+#pragma unroll
+    for (int u = 0; u < UNR; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (4 * (base + u * blockDim.x + tid) + e < V && order_key(v[u][e]) >= t0) {
+          takem |= 1u << (4 * u + e);
+          ++cnt;
+        }
+    if (__ballot_sync(0xffffffffu, cnt > 0)) {
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
+      int slot0 = 0;
+      if (lane == 31) slot0 = atomicAdd(&s_nc, incl);
+      slot0 = __shfl_sync(0xffffffffu, slot0, 31);
+      int p = slot0 + incl - cnt;
+#pragma unroll
+      for (int u = 0; u < UNR; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if ((takem >> (4 * u + e)) & 1u) {
+            if (p < kTkCap) {
+              ckey[p] = order_key(v[u][e]);
+              cidx[p] = 4 * (base + u * blockDim.x + tid) + e;
+            }
+            ++p;
+          }
     }
   }
   __syncthreads();
@@ -1122,6 +1496,31 @@ static spec_status attn_launch(const spec_model_desc& d, const RowInfo& ri, cons
   return SPEC_OK;
 }
 
+template <int HDV, int MT>
+static spec_status attn_mma_launch(const spec_model_desc& d, const RowInfo& ri, const spec_rows& rows,
+                                   const void* qbuf, const spec_kv& kv, float* opart, float2* mlpart, void* attn_out,
+                                   int nsplit, int nqg, void* ws, cudaStream_t st) {
+  static int attr_dev = -1, occ = 1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  constexpr size_t smem = attn_mma_smem<HDV, MT>();
+  auto kern = attn_mma_kernel<HDV, MT>;
+  if (attr_dev != dev) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 128, smem) != cudaSuccess || occ < 1) occ = 1;
+    attr_dev = dev;
+  }
+  const int n_items = nsplit * d.n_kv_heads * rows.B * nqg;
+  const int grid = std::min(n_items, occ * sm_count());
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)d.head_dim);
+  launch_pdl(kern, dim3(grid), dim3(128), smem, st, (const __nv_bfloat16*)qbuf, kv, ri, d.n_q_heads, d.n_kv_heads,
+             d.window, nsplit, nqg, n_items, scale_log2, opart, mlpart, ws);
+  launch_pdl(attn_combine_kernel<__nv_bfloat16, HDV>, dim3(rows.M * d.n_q_heads), dim3(HDV), 0, st, opart, mlpart,
+             d.n_q_heads, nsplit, (__nv_bfloat16*)attn_out);
+  return SPEC_OK;
+}
+
 template <typename TT, int HDV>
 static spec_status attn_qdispatch(int qmax, const spec_model_desc& d, const RowInfo& ri, const spec_rows& rows,
                                   const void* qbuf, const spec_kv& kv, float* opart, float2* mlpart, void* out,
@@ -1142,10 +1541,14 @@ spec_status launch_attention(const spec_model_desc& d, const spec_rows& rows, co
   const int nqg = (rows.rows_per_req * G + qmax - 1) / qmax;
   spec_status s;
   if (d.dtype == SPEC_DTYPE_BF16) {
+    // tensor-core path: 16 or 32 query rows per item (the same groups as qmax <= 16 / 32)
+    const bool two = qmax > 16;
     if (d.head_dim == 128)
-      s = attn_qdispatch<__nv_bfloat16, 128>(qmax, d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st);
+      s = two ? attn_mma_launch<128, 2>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st)
+              : attn_mma_launch<128, 1>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st);
     else if (d.head_dim == 64)
-      s = attn_qdispatch<__nv_bfloat16, 64>(qmax, d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st);
+      s = two ? attn_mma_launch<64, 2>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st)
+              : attn_mma_launch<64, 1>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st);
     else
       return SPEC_ERR_UNSUPPORTED;
   } else {

@@ -80,3 +80,24 @@ def kv_host(dm):
 def no_device_error(dm_or_ws):
     ws = dm_or_ws.ws if hasattr(dm_or_ws, "ws") else dm_or_ws
     assert lib.spec_get_device_error(ws) == 0
+
+
+def tree_mismatch_is_near_tie(got_tok, got_par, fin, got_score=None, tol=2e-2):
+    """True if, in every request whose GPU tree differs from the oracle's, the first
+    differing node (nodes are numbered depth by depth, best score first, so later
+    differences may follow from it) sits next to a node whose oracle score is within
+    ``tol``, or where the GPU placed a candidate whose score is within ``tol`` of the
+    oracle's node there: two candidates whose ranking the two precisions may swap."""
+    got_tok, got_par = np.asarray(got_tok), np.asarray(got_par)
+    score = np.asarray(fin["score"], dtype=np.float64)
+    diff = (got_tok != fin["tok"]) | (got_par != fin["parent"])
+    for b in range(diff.shape[0]):
+        if not diff[b].any():
+            continue
+        n = int(np.argmax(diff[b]))
+        near = [abs(score[b, n] - score[b, m]) for m in (n - 1, n + 1) if 1 <= m < score.shape[1]]
+        if got_score is not None:
+            near.append(abs(float(np.asarray(got_score)[b, n]) - score[b, n]))
+        if not near or min(near) >= tol:
+            return False
+    return True
