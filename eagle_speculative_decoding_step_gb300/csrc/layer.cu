@@ -616,7 +616,7 @@ template <int HD, int MT>
 constexpr size_t attn_mma_smem() {
   using S = MmaShape<HD>;
   const size_t ring = (size_t)2 * S::STAGE;
-  const size_t red = (size_t)4 * 16 * MT * HD * 4;            // the warps' outputs after the last tile (aliases the ring)
+  const size_t red = (size_t)4 * 16 * MT * (HD + 8) * 4;      // the warps' outputs after the last tile (aliases the ring)
   return (ring > red ? ring : red) + (size_t)16 * MT * S::KP * 2 + (size_t)2 * kMmaTK * 4;
 }
 
@@ -653,7 +653,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
   constexpr size_t kRing = attn_mma_smem<HD, MT>() - (size_t)QM * KP * 2 - (size_t)2 * TK * 4;
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(mma_smem + kRing);   // [QM][KP]
   int* sCi = reinterpret_cast<int*>(sQ + QM * KP);                          // [2][TK] cache index, -1 = no slot
-  float* red = reinterpret_cast<float*>(mma_smem);                           // [4][QM][HD]
+  float* red = reinterpret_cast<float*>(mma_smem);                           // [4][QM][HD + 8]
   __shared__ float sMw[4][QM], sLw[4][QM];
   __shared__ int s_lo[QM];
   __shared__ unsigned long long s_mask[QM];
@@ -720,6 +720,8 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
     const int kbeg = min(total, s * chunk), kend = min(total, kbeg + chunk);
     const int ntiles = (kend - kbeg + TK - 1) / TK;
 
+    // stage tile j into ring slot j & 1: thread t copies half (t & 1) of the K and V
+    // rows of key t >> 1 (one page-table lookup per thread)
     auto issue = [&](int j) {
       if (j < ntiles) {
         uint8_t* st = mma_smem + (size_t)(j & 1) * Sh::STAGE;
@@ -727,27 +729,33 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
         __nv_bfloat16* sV = sK + TK * KP;
         const int t0 = kbeg + j * TK;
         const int nk = min(TK, kend - t0);
-        const int ch = tid % CH;
-        for (int kt = tid / CH; kt < TK; kt += 128 / CH) {
-          uint4* dk = reinterpret_cast<uint4*>(sK + kt * KP) + ch;
-          uint4* dv = reinterpret_cast<uint4*>(sV + kt * KP) + ch;
-          int ci = -1;
-          long long slot = -1;
-          if (kt < nk) {
-            const int kidx = t0 + kt;
-            ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
-            slot = slot_of(kv, b, ci);
-          }
-          if (slot >= 0) {
-            const size_t off = ((size_t)slot * nkv + g) * HD;
-            cp_async16(dk, reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(kv.k) + off) + ch);
-            cp_async16(dv, reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(kv.v) + off) + ch);
-          } else {
-            *dk = make_uint4(0, 0, 0, 0);
-            *dv = make_uint4(0, 0, 0, 0);
-          }
-          if (ch == 0) sCi[(j & 1) * TK + kt] = slot >= 0 ? ci : -1;
+        const int kt = tid >> 1, c0 = (tid & 1) * (CH / 2);
+        int ci = -1;
+        long long slot = -1;
+        if (kt < nk) {
+          const int kidx = t0 + kt;
+          ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
+          slot = slot_of(kv, b, ci);
         }
+        uint4* dk = reinterpret_cast<uint4*>(sK + kt * KP) + c0;
+        uint4* dv = reinterpret_cast<uint4*>(sV + kt * KP) + c0;
+        if (slot >= 0) {
+          const size_t off = ((size_t)slot * nkv + g) * HD;
+          const uint4* gk = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(kv.k) + off) + c0;
+          const uint4* gv = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(kv.v) + off) + c0;
+#pragma unroll
+          for (int c = 0; c < CH / 2; ++c) {
+            cp_async16(dk + c, gk + c);
+            cp_async16(dv + c, gv + c);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < CH / 2; ++c) {
+            dk[c] = make_uint4(0, 0, 0, 0);
+            dv[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        if ((tid & 1) == 0) sCi[(j & 1) * TK + kt] = slot >= 0 ? ci : -1;
       }
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
@@ -764,6 +772,19 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
       for (int h = 0; h < 2; ++h) { mrun[mt][h] = -INFINITY; lrun[mt][h] = 0.f; }
     }
     const uint32_t qbase = smem_u32(sQ);
+    // per-row constants of this thread's rows (m-tile mt, half h: row mt*16 + grp + 8h)
+    int rlo[MT][2];
+    unsigned long long rmask[MT][2];
+    bool rok[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int qi = mt * 16 + grp + 8 * h;
+        rok[mt][h] = qi < nQ;
+        rlo[mt][h] = s_lo[qi];
+        rmask[mt][h] = s_mask[qi];
+      }
 
     issue(0);
     for (int j = 0; j < ntiles; ++j) {
@@ -800,21 +821,22 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
         }
       }
       // mask, scale to log2 units, warp-local online softmax
+      int kci[4];                 // cache index of this thread's four keys (-1: no slot)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) kci[u] = ci_t[warp * 16 + (u >> 1) * 8 + 2 * tig + (u & 1)];
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int qi = mt * 16 + grp + 8 * h;
-          const bool qok = qi < nQ;
-          const int qlo = s_lo[qi];
-          const unsigned long long qmask = s_mask[qi];
+          const bool qok = rok[mt][h];
+          const int qlo = rlo[mt][h];
+          const unsigned long long qmask = rmask[mt][h];
           float mx = -INFINITY;
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int kt = warp * 16 + nt * 8 + 2 * tig + e;
-              const int ci = ci_t[kt];
+              const int ci = kci[2 * nt + e];
               bool ok = qok && ci >= 0;
               if (ok) ok = ci < ctx ? ci >= qlo : ((qmask >> (ci - ctx)) & 1ull) != 0;
               const float v = ok ? sc[mt][nt][2 * h + e] * scale_log2 : -INFINITY;
@@ -836,10 +858,12 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
             }
           lrun[mt][h] = lrun[mt][h] * al + ps;
           mrun[mt][h] = mnew;
+          if (al != 1.f) {
 #pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            acc[mt][n][2 * h] *= al;
-            acc[mt][n][2 * h + 1] *= al;
+            for (int n = 0; n < NT; ++n) {
+              acc[mt][n][2 * h] *= al;
+              acc[mt][n][2 * h + 1] *= al;
+            }
           }
         }
       }
@@ -879,20 +903,21 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
           sLw[warp][mt * 16 + grp + 8 * h] = l;
         }
       }
+    constexpr int RS = HD + 8;      // padded row of the merge buffer (fewer bank conflicts)
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int n = 0; n < NT; ++n)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < 2; ++h)
+        if (rok[mt][h]) {
           const int row = mt * 16 + grp + 8 * h;
-          *reinterpret_cast<float2*>(red + ((size_t)warp * QM + row) * HD + n * 8 + 2 * tig) =
-              make_float2(acc[mt][n][2 * h], acc[mt][n][2 * h + 1]);
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+            *reinterpret_cast<float2*>(red + ((size_t)warp * QM + row) * RS + n * 8 + 2 * tig) =
+                make_float2(acc[mt][n][2 * h], acc[mt][n][2 * h + 1]);
         }
     __syncthreads();
-    for (int e = tid; e < QM * HD; e += blockDim.x) {
+    for (int e = tid; e < nQ * HD; e += blockDim.x) {
       const int qi = e / HD, d = e % HD;
-      if (qi >= nQ) continue;
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < 4; ++w) M = fmaxf(M, sMw[w][qi]);
@@ -901,7 +926,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const float f = exp2f(sMw[w][qi] - M);
-          o += red[((size_t)w * QM + qi) * HD + d] * f;
+          o += red[((size_t)w * QM + qi) * RS + d] * f;
           L += sLw[w][qi] * f;
         }
       }
