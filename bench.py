@@ -129,9 +129,10 @@ def step_bytes(w):
 def launches_per_step(w):
     layer = 11                                   # prologue, 4 GEMMs, 4 epilogues, attention + combine
     head = 6 if w.rank > 0 else 2                # fused LM head + merge, or the candidate head's 6
+    verify = 4 if w.verify == "rejection" else 2  # row statistics, decisions, sampled row, emit / argmax + finalize
     if w.mode == "chain":
-        return 2 + w.K * (layer + head) + 2
-    return 2 + w.depth * (layer + head + 1) + 2  # + tree expansion per depth
+        return 2 + w.K * (layer + head) + verify
+    return 2 + w.depth * (layer + head + 1) + verify  # + tree expansion per depth
 
 
 def build_chain_step(w, dm, aux_d, root_d, device):

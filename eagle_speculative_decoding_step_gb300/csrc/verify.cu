@@ -350,26 +350,40 @@ __global__ void __launch_bounds__(1024) reject_threshold_kernel(const float* __r
 }
 
 // ---------------------------------------------------------------- rejection
+// Two streaming passes instead of one heavy one.  The accept tests need, per
+// row, only the log-sum-exp of the (filtered, tempered) target distribution;
+// the Gumbel sample is needed on one row per request: the first rejected
+// position, or row K for the bonus token.  So:
+//  1. rej_stats_kernel: every row, chunked -- max / sum-exp over the kept
+//     tokens (greedy rows: argmax);
+//  2. rej_decide_kernel: one warp per request -- merges the chunks row by row
+//     and makes the sequential accept decisions (greedy: draft == argmax),
+//     writes accept_len, the accepted drafts, -1 padding, kv_src, and for
+//     greedy requests the emitted token;
+//  3. rej_sample_kernel: the sampled row of every stochastic request, chunked
+//     -- Philox noise and the Gumbel-max key over the kept tokens, the draft
+//     token excluded on a rejected row (its records go where that request's
+//     row statistics were, no longer needed);
+//  4. rej_emit_kernel: merges the chunk keys, writes the emitted token.
 template <bool VEC>
-__global__ void __launch_bounds__(256) rejection_chunks_kernel(
-    const float* __restrict__ logits, int K, int V, int nch, int L, const int32_t* __restrict__ draft,
-    const float* __restrict__ temperature, uint2 key, uint32_t ctr_w, RejPart* __restrict__ part,
-    const Thr* __restrict__ thr) {
+__global__ void __launch_bounds__(256) rej_stats_kernel(const float* __restrict__ logits, int K, int V, int nch,
+                                                        int L, const float* __restrict__ temperature,
+                                                        RejPart* __restrict__ part, const Thr* __restrict__ thr) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[32];
   __shared__ int redi[32];
   const int row = blockIdx.y, c = blockIdx.x;
   const Thr tr = thr ? thr[row] : Thr{0u, 0x7fffffff};
-  const int b = row / (K + 1), i = row % (K + 1);
+  const int b = row / (K + 1);
   const float T = temperature[b];
   const bool greedy = !(T > 0.f);
-  const int excl = (!greedy && i < K) ? draft[(size_t)b * K + i] : -1;
+  const bool unit = T == 1.f;                 // y = l / 1 exactly: skip the division
+  const bool filt = thr != nullptr;
   const float* x = logits + (size_t)row * V;
   const int lo = c * L, hi = min(V, lo + L);
   float m = -INFINITY, s = 0.f, bk = -INFINITY;
   int bi = 0x7fffffff;
-  // every thread handles aligned groups of 4 vocabulary ids = one Philox block
   for (int j = lo + 4 * threadIdx.x; j < hi; j += 4 * blockDim.x) {
     float v[4];
     if (VEC) {
@@ -385,75 +399,151 @@ __global__ void __launch_bounds__(256) rejection_chunks_kernel(
         if (j + l < hi && better(v[l], j + l, bk, bi)) { bk = v[l]; bi = j + l; }
       continue;
     }
-    uint4 r = philox4x32_10(make_uint4((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b, ctr_w), key);
-    uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    // the group's kept values, -inf for the rest (ids past hi, filtered by top-k / top-p)
+    float y[4];
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
-      if (j + l >= hi) break;
-      float y = v[l] / T;
-      if (!kept_by(tr, okey(y), j + l)) continue;        // filtered out by top-k / top-p
-      if (y > m) { s = s * expf(m - y) + 1.f; m = y; }
-      else s += expf(y - m);
-      if (j + l == excl) continue;
-      float u = word_to_uniform(w[l]);
-      float g = y - logf(-logf(u));
-      if (better(g, j + l, bk, bi)) { bk = g; bi = j + l; }
+      y[l] = (j + l < hi) ? (unit ? v[l] : v[l] / T) : -INFINITY;
+      if (filt && y[l] > -INFINITY && !kept_by(tr, okey(y[l]), j + l)) y[l] = -INFINITY;
     }
+    // online sum of exp: one max update per group of four
+    const float gm = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
+    if (gm > m) {
+      s *= __expf(m - gm);
+      m = gm;
+    }
+    if (m > -INFINITY) s += (__expf(y[0] - m) + __expf(y[1] - m)) + (__expf(y[2] - m) + __expf(y[3] - m));
   }
-  // reduce (m, s)
-  float bm = block_max(m, red);
-  float contrib = (m == -INFINITY) ? 0.f : s * expf(m - bm);
-  float bs = block_sum(contrib, red);
+  const float bm = block_max(m, red);
+  const float contrib = (m == -INFINITY) ? 0.f : s * expf(m - bm);
+  const float bs = block_sum(contrib, red);
   block_argmax(bk, bi, red, redi);
   if (threadIdx.x == 0) part[(size_t)row * nch + c] = RejPart{bm, bs, bk, bi};
 }
 
-__global__ void __launch_bounds__(32) rejection_finalize_kernel(
+__global__ void __launch_bounds__(32) rej_decide_kernel(
     const float* __restrict__ logits, int K, int V, int nch, const RejPart* __restrict__ part,
     const int32_t* __restrict__ draft, const float* __restrict__ temperature, uint2 key, uint32_t ctr_w0,
     int32_t* __restrict__ out, int32_t* __restrict__ acc_out, int32_t* __restrict__ kv_src,
     const Thr* __restrict__ thr) {
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.x;
-  if (threadIdx.x != 0) return;
+  const int b = blockIdx.x, lane = threadIdx.x;
   const float T = temperature[b];
   const bool greedy = !(T > 0.f);
   int a = 0, emitted = -1;
   for (int i = 0; i <= K; ++i) {
     const size_t row = (size_t)b * (K + 1) + i;
-    float M = -INFINITY, S = 0.f, bk = -INFINITY;
+    // merge the row's chunk records (lane c takes chunks c, c + 32, ...)
+    float M = -INFINITY, bk = -INFINITY;
     int bi = 0x7fffffff;
-    for (int c = 0; c < nch; ++c) {
-      RejPart p = part[row * nch + c];
-      if (p.m > M) { S = S * expf(M - p.m) + p.s; M = p.m; }
-      else if (p.m > -INFINITY) S += p.s * expf(p.m - M);
+    for (int c = lane; c < nch; c += 32) {
+      const RejPart p = part[row * nch + c];
+      M = fmaxf(M, p.m);
       if (better(p.key, p.idx, bk, bi)) { bk = p.key; bi = p.idx; }
     }
-    if (i == K) { emitted = bi; break; }
+    M = warp_max(M);
+    warp_argmax(bk, bi);
+    float S = 0.f;
+    for (int c = lane; c < nch; c += 32) {
+      const RejPart p = part[row * nch + c];
+      if (p.m > -INFINITY) S += p.s * expf(p.m - M);
+    }
+    S = warp_sum(S);
+    if (i == K) {
+      if (greedy) emitted = bi;
+      break;
+    }
     const int d = draft[(size_t)b * K + i];
     bool ok;
     if (greedy) {
       ok = (d == bi);
     } else {
-      float lse = M + logf(S);
+      const float lse = M + logf(S);
       float pd = 0.f;
       if (d >= 0 && d < V) {
         const float yd = logits[row * V + d] / T;
         const Thr tr = thr ? thr[row] : Thr{0u, 0x7fffffff};
         if (kept_by(tr, okey(yd), d)) pd = expf(yd - lse);
       }
-      uint4 r = philox4x32_10(make_uint4(0u, (uint32_t)i, (uint32_t)b, ctr_w0), key);
+      const uint4 r = philox4x32_10(make_uint4(0u, (uint32_t)i, (uint32_t)b, ctr_w0), key);
       ok = word_to_uniform(r.x) <= pd;
     }
-    if (!ok) { emitted = bi; break; }
+    if (!ok) {
+      if (greedy) emitted = bi;
+      break;
+    }
     ++a;
   }
-  for (int i = 0; i <= K; ++i) {
-    out[(size_t)b * (K + 1) + i] = i < a ? draft[(size_t)b * K + i] : (i == a ? emitted : -1);
+  for (int i = lane; i <= K; i += 32) {
+    if (i != a || greedy) out[(size_t)b * (K + 1) + i] = i < a ? draft[(size_t)b * K + i] : (i == a ? emitted : -1);
     if (kv_src) kv_src[(size_t)b * (K + 1) + i] = i <= a ? i : -1;
   }
-  acc_out[b] = a;
+  if (lane == 0) acc_out[b] = a;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(256) rej_sample_kernel(const float* __restrict__ logits, int K, int V, int nchs,
+                                                         int L, int region, const int32_t* __restrict__ draft,
+                                                         const float* __restrict__ temperature, uint2 key,
+                                                         uint32_t ctr_w, const int32_t* __restrict__ acc_in,
+                                                         RejPart* __restrict__ part, const Thr* __restrict__ thr) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float red[32];
+  __shared__ int redi[32];
+  const int b = blockIdx.y, c = blockIdx.x;
+  const float T = temperature[b];
+  if (!(T > 0.f)) return;                     // greedy requests were settled by the decision kernel
+  const int i = acc_in[b];
+  const int row = b * (K + 1) + i;
+  const Thr tr = thr ? thr[row] : Thr{0u, 0x7fffffff};
+  const bool unit = T == 1.f;
+  const int excl = i < K ? draft[(size_t)b * K + i] : -1;
+  const float* x = logits + (size_t)row * V;
+  const int lo = c * L, hi = min(V, lo + L);
+  float bk = -INFINITY;
+  int bi = 0x7fffffff;
+  // every thread handles aligned groups of 4 vocabulary ids = one Philox block
+  for (int j = lo + 4 * threadIdx.x; j < hi; j += 4 * blockDim.x) {
+    float v[4];
+    if (VEC) {
+      float4 q = *reinterpret_cast<const float4*>(x + j);
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+#pragma unroll
+      for (int l = 0; l < 4; ++l) v[l] = (j + l < hi) ? x[j + l] : -INFINITY;
+    }
+    const uint4 r = philox4x32_10(make_uint4((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b, ctr_w), key);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      if (j + l >= hi) break;
+      const float y = unit ? v[l] : v[l] / T;
+      if (j + l == excl || !kept_by(tr, okey(y), j + l)) continue;
+      const float g = y - logf(-logf(word_to_uniform(w[l])));
+      if (better(g, j + l, bk, bi)) { bk = g; bi = j + l; }
+    }
+  }
+  block_argmax(bk, bi, red, redi);
+  if (threadIdx.x == 0) part[(size_t)b * region + c] = RejPart{0.f, 0.f, bk, bi};
+}
+
+__global__ void __launch_bounds__(32) rej_emit_kernel(int K, int nchs, int region, const RejPart* __restrict__ part,
+                                                      const float* __restrict__ temperature,
+                                                      const int32_t* __restrict__ acc_in, int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x, lane = threadIdx.x;
+  if (!(temperature[b] > 0.f)) return;
+  float bk = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int c = lane; c < nchs; c += 32) {
+    const RejPart p = part[(size_t)b * region + c];
+    if (better(p.key, p.idx, bk, bi)) { bk = p.key; bi = p.idx; }
+  }
+  warp_argmax(bk, bi);
+  if (lane == 0) out[(size_t)b * (K + 1) + acc_in[b]] = bi;
 }
 
 }  // namespace spec
@@ -527,16 +617,29 @@ extern "C" spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, co
     launch_pdl(reject_threshold_kernel, dim3(rows), dim3(1024), 0, stream, target_logits, K, V, temperature, top_k,
                top_p, thr);
   }
-  dim3 grid(nch, rows);
   const bool vec = (V % 4 == 0) && aligned(target_logits, 16);
   if (vec)
-    launch_pdl(rejection_chunks_kernel<true>, dim3(grid), dim3(256), 0, stream, target_logits, K, V, nch, L, draft_tok,
-               temperature, key, w0 + 1u, part, (const Thr*)thr);
+    launch_pdl(rej_stats_kernel<true>, dim3(nch, rows), dim3(256), 0, stream, target_logits, K, V, nch, L, temperature,
+               part, (const Thr*)thr);
   else
-    launch_pdl(rejection_chunks_kernel<false>, dim3(grid), dim3(256), 0, stream, target_logits, K, V, nch, L, draft_tok,
-               temperature, key, w0 + 1u, part, (const Thr*)thr);
-  launch_pdl(rejection_finalize_kernel, dim3(B), dim3(32), 0, stream, target_logits, K, V, nch, part, draft_tok,
-             temperature, key, w0, out_tok, accept_len, kv_src, (const Thr*)thr);
+    launch_pdl(rej_stats_kernel<false>, dim3(nch, rows), dim3(256), 0, stream, target_logits, K, V, nch, L,
+               temperature, part, (const Thr*)thr);
+  launch_pdl(rej_decide_kernel, dim3(B), dim3(32), 0, stream, target_logits, K, V, nch, (const RejPart*)part,
+             draft_tok, temperature, key, w0, out_tok, accept_len, kv_src, (const Thr*)thr);
+  // the sampled rows: one per request, chunked over the CTAs; each request's records
+  // take the slots of its (now consumed) row statistics
+  const int region = R * nch;
+  int nchs = std::min(region, std::max(1, (640 + B - 1) / B));
+  nchs = std::min(nchs, std::max(1, V / 2048));
+  const int Ls = chunk_len(V, nchs);
+  if (vec)
+    launch_pdl(rej_sample_kernel<true>, dim3(nchs, B), dim3(256), 0, stream, target_logits, K, V, nchs, Ls, region,
+               draft_tok, temperature, key, w0 + 1u, (const int32_t*)accept_len, part, (const Thr*)thr);
+  else
+    launch_pdl(rej_sample_kernel<false>, dim3(nchs, B), dim3(256), 0, stream, target_logits, K, V, nchs, Ls, region,
+               draft_tok, temperature, key, w0 + 1u, (const int32_t*)accept_len, part, (const Thr*)thr);
+  launch_pdl(rej_emit_kernel, dim3(B), dim3(32), 0, stream, K, nchs, region, (const RejPart*)part, temperature,
+             (const int32_t*)accept_len, out_tok);
   return last_launch();
 }
 
