@@ -802,20 +802,17 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+      const uint32_t krow = kbase + (uint32_t)((warp * 16 + 8 * (lane >> 4) + (lane & 7)) * KP +
+                                               8 * ((lane >> 3) & 1)) * 2;
+      const uint32_t qrow = qbase + (uint32_t)((8 * ((lane >> 3) & 1) + (lane & 7)) * KP + 8 * (lane >> 4)) * 2;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         uint32_t b0, b1, b2, b3;   // keys 16w + {0..7, 8..15} x dims ks*16 + {0..7, 8..15}
-        {
-          const int blk = lane >> 3, i = lane & 7;
-          const int key = warp * 16 + 8 * (blk >> 1) + i, dim = ks * 16 + 8 * (blk & 1);
-          ldsm_x4(kbase + (uint32_t)(key * KP + dim) * 2, b0, b1, b2, b3);
-        }
+        ldsm_x4(krow + (uint32_t)(ks * 16 * 2), b0, b1, b2, b3);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           uint32_t a0, a1, a2, a3;
-          const int blk = lane >> 3, i = lane & 7;
-          const int row = mt * 16 + 8 * (blk & 1) + i, dim = ks * 16 + 8 * (blk >> 1);
-          ldsm_x4(qbase + (uint32_t)(row * KP + dim) * 2, a0, a1, a2, a3);
+          ldsm_x4(qrow + (uint32_t)((mt * 16 * KP + ks * 16) * 2), a0, a1, a2, a3);
           mma_bf16(sc[mt][0], a0, a1, a2, a3, b0, b1);
           mma_bf16(sc[mt][1], a0, a1, a2, a3, b2, b3);
         }
@@ -828,6 +825,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
       for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
+          if (mt * 16 + 8 * h >= nQ) continue;     // rows of zero queries only (uniform in the warp)
           const bool qok = rok[mt][h];
           const int qlo = rlo[mt][h];
           const unsigned long long qmask = rmask[mt][h];
@@ -868,22 +866,24 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
         }
       }
       // P.V: A = P (queries x this warp's 16 keys), B = V^T via transposed ldmatrix
+      uint32_t pa[MT][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        pa[mt][0] = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
+        pa[mt][1] = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
+        pa[mt][2] = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
+        pa[mt][3] = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
+      }
+      const uint32_t vrow = vbase + (uint32_t)((warp * 16 + 8 * ((lane >> 3) & 1) + (lane & 7)) * KP +
+                                               8 * (lane >> 4)) * 2;
 #pragma unroll
       for (int n2 = 0; n2 < NT / 2; ++n2) {
         uint32_t v0, v1, v2, v3;   // keys 16w + {0..7, 8..15} x dims 16*n2 + {0..7, 8..15}
-        {
-          const int blk = lane >> 3, i = lane & 7;
-          const int key = warp * 16 + 8 * (blk & 1) + i, dim = n2 * 16 + 8 * (blk >> 1);
-          ldsm_x4_t(vbase + (uint32_t)(key * KP + dim) * 2, v0, v1, v2, v3);
-        }
+        ldsm_x4_t(vrow + (uint32_t)(n2 * 16 * 2), v0, v1, v2, v3);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          const uint32_t a0 = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
-          const uint32_t a1 = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
-          const uint32_t a2 = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
-          const uint32_t a3 = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
-          mma_bf16(acc[mt][2 * n2], a0, a1, a2, a3, v0, v1);
-          mma_bf16(acc[mt][2 * n2 + 1], a0, a1, a2, a3, v2, v3);
+          mma_bf16(acc[mt][2 * n2], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v0, v1);
+          mma_bf16(acc[mt][2 * n2 + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v2, v3);
         }
       }
       __syncthreads();     // ring slot j & 1 is refilled by the next iteration's copies
@@ -1009,24 +1009,27 @@ SPEC_DEV uint32_t order_key(float f) {
 }
 
 // The Kc largest of each row of s [M, V] (ties to the smaller id), in
-// descending order.  One CTA of 1024 threads per row, on order-preserving
-// 32-bit keys:
-//  1. every thread takes the largest key among its elements (a strided slice of
-//     the row); the Kc-th largest of these 1024 maxima, T0, is a lower bound of
-//     the row's Kc-th largest key (the Kc largest maxima are Kc distinct
-//     elements >= T0);
-//  2. a second pass copies the elements >= T0 -- typically a few hundred -- to
-//     shared memory;
-//  3. an exact radix selection over the copies gives the Kc-th key and how many
-//     of the elements equal to it are taken (smallest ids first);
-//  4. a bitonic sort of the Kc selected.
-// Both passes over the row are plain streaming reads (no atomics on shared
-// counters per element).  If more than the shared-memory capacity passes step
-// 2 (rows with huge runs of equal values), step 3 runs on the row itself, in
-// id order for the ties.
-constexpr int kTkCap = 6144;
+// descending order.  A cluster of kTkCL CTAs (1024 threads each) per row, on
+// order-preserving 32-bit keys; CTA r owns a contiguous part of the row:
+//  1. every thread takes the largest key among its elements; the Kc-th largest
+//     of its CTA's 1024 maxima is a lower bound of the row's Kc-th largest key
+//     (the Kc largest maxima are Kc distinct elements at least that large), and
+//     so is the largest of the cluster's bounds, T0 (exchanged in distributed
+//     shared memory);
+//  2. a second pass copies the CTA's elements >= T0 -- a few hundred in the
+//     whole row -- to its shared memory;
+//  3. rank 0 gathers the copies, an exact radix selection gives the Kc-th key
+//     and how many elements equal to it are taken (smallest ids first), and a
+//     bitonic sort orders the Kc selected.
+// Both passes over the row are plain streaming reads (16-byte loads, one
+// shared-counter update per warp and round).  If more elements pass step 2
+// than shared memory takes (long runs of equal values), rank 0 selects with
+// radix passes over the whole row, ties collected in id order.
+constexpr int kTkCL = 2;            // one wave at 64 rows: 128 CTAs of 1024 threads
+constexpr int kTkCap = 6144;          // copies rank 0 gathers
+constexpr int kTkCapCta = 2048;       // copies one CTA keeps
 
-size_t topk_select_smem() { return (size_t)kTkCap * 8 + 1024 * 8 + 256 * 4; }
+size_t topk_select_smem() { return (size_t)kTkCap * 8 + (size_t)kTkCapCta * 8 + 1024 * 8 + 256 * 4; }
 
 SPEC_DEV int block_excl_scan(int v, int* wsum, int* total) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -1056,7 +1059,7 @@ SPEC_DEV int block_excl_scan(int v, int* wsum, int* total) {
 // radix select over n keys (shared memory, or the float row x): the key of the
 // need-th largest, digit by digit (8 bits) from the top, and in *tie_need how
 // many elements equal to it belong to the need largest.  Lanes of a warp that
-// fall in the same digit add to the histogram once.
+// fall in the same digit add to the histogram once; warp 0 finds the digit.
 template <bool SMEM_KEYS>
 SPEC_DEV uint32_t radix_select(const float* x, const uint32_t* keys, int n, int need, int* hist, uint32_t* s_prefix,
                                int* s_need, int* tie_need) {
@@ -1084,8 +1087,8 @@ SPEC_DEV uint32_t radix_select(const float* x, const uint32_t* keys, int n, int 
     }
     __syncthreads();
     if (tid < 32) {
-      // lane l owns digits 255-8l .. 248-8l; count of elements above the lane's
-      // digits = suffix sum over the lanes before it
+      // lane l owns digits 255-8l .. 248-8l; count above the lane's digits =
+      // prefix over the lanes before it
       const int nn = *s_need;
       int hv[8], c = 0;
 #pragma unroll
@@ -1100,8 +1103,7 @@ SPEC_DEV uint32_t radix_select(const float* x, const uint32_t* keys, int n, int 
         if (lane >= o) incl += y;
       }
       const int before = incl - c;
-      const bool mine = before < nn && incl >= nn;
-      if (mine) {
+      if (before < nn && incl >= nn) {
         int acc = before, dsel = 0;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -1118,151 +1120,9 @@ SPEC_DEV uint32_t radix_select(const float* x, const uint32_t* keys, int n, int 
   return *s_prefix;
 }
 
-__global__ void __launch_bounds__(1024) topk_select_kernel(const float* __restrict__ s, int V, int Kc,
-                                                           int32_t* __restrict__ out_ids) {
-  pdl_wait();
-  pdl_trigger();
-  extern __shared__ __align__(16) uint8_t tk_smem[];
-  uint32_t* ckey = reinterpret_cast<uint32_t*>(tk_smem);              // [cap] copies
-  int* cidx = reinterpret_cast<int*>(ckey + kTkCap);                  // [cap]
-  uint32_t* skey = reinterpret_cast<uint32_t*>(cidx + kTkCap);        // [1024] maxima, then the selected
-  int* sidx = reinterpret_cast<int*>(skey + 1024);
-  int* hist = sidx + 1024;                                            // [256]
-  __shared__ int wsum[32];
-  __shared__ int s_total, s_nsel, s_nc, s_need, s_tie;
-  __shared__ uint32_t s_prefix;
-  const int m = blockIdx.x;
-  const float* x = s + (size_t)m * V;
-  const int tid = threadIdx.x, lane = tid & 31;
-  if (tid == 0) { s_nsel = 0; s_nc = 0; }
-  // The row in groups of four consecutive elements (16-byte loads), group
-  // g = base + u * 1024 + tid; UNR groups (4 * UNR loads) in flight per thread.
-  constexpr int UNR = 4;
-  const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0);
-  const int ng = (V + 3) / 4;
-  auto load4 = [&](int gi, float* v) {
-    if (gi >= ng) {
-      v[0] = v[1] = v[2] = v[3] = -INFINITY;
-    } else if (vec) {
-      const float4 q = __ldg(reinterpret_cast<const float4*>(x) + gi);
-      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = 4 * gi + e < V ? x[4 * gi + e] : -INFINITY;
-    }
-  };
-  // 1. per-thread maxima, then T0 = the Kc-th largest of them
-  uint32_t tmax = 0;
-  for (int base = 0; base < ng; base += UNR * blockDim.x) {
-    float v[UNR][4];
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) load4(base + u * blockDim.x + tid, v[u]);
-#pragma unroll
-    for (int u = 0; u < UNR; ++u)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (4 * (base + u * blockDim.x + tid) + e < V) tmax = max(tmax, order_key(v[u][e]));
-  }
-  skey[tid] = tmax;           // 0 for a thread without elements: below every key
-  __syncthreads();
-  int tie_need;
-  const uint32_t t0 = radix_select<true>(nullptr, skey, blockDim.x, Kc, hist, &s_prefix, &s_need, &tie_need);
-  // 2. copy the elements >= T0 (one shared counter update per warp and round)
-  for (int base = 0; base < ng; base += UNR * blockDim.x) {
-    float v[UNR][4];
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) load4(base + u * blockDim.x + tid, v[u]);
-    uint32_t takem = 0;
-    int cnt = 0;
-#pragma unroll
-    for (int u = 0; u < UNR; ++u)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (4 * (base + u * blockDim.x + tid) + e < V && order_key(v[u][e]) >= t0) {
-          takem |= 1u << (4 * u + e);
-          ++cnt;
-        }
-    if (__ballot_sync(0xffffffffu, cnt > 0)) {
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int slot0 = 0;
-      if (lane == 31) slot0 = atomicAdd(&s_nc, incl);
-      slot0 = __shfl_sync(0xffffffffu, slot0, 31);
-      int p = slot0 + incl - cnt;
-#pragma unroll
-      for (int u = 0; u < UNR; ++u)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if ((takem >> (4 * u + e)) & 1u) {
-            if (p < kTkCap) {
-              ckey[p] = order_key(v[u][e]);
-              cidx[p] = 4 * (base + u * blockDim.x + tid) + e;
-            }
-            ++p;
-          }
-    }
-  }
-  __syncthreads();
-  const int ncand = s_nc;
-  uint32_t kth;
-  if (ncand <= kTkCap) {
-    // 3. exact selection among the copies
-    kth = radix_select<true>(nullptr, ckey, ncand, Kc, hist, &s_prefix, &s_need, &tie_need);
-    for (int i = tid; i < ncand; i += blockDim.x) {
-      const uint32_t k = ckey[i];
-      bool take = k > kth;
-      if (k == kth) {
-        const int id = cidx[i];
-        int rank = 0;
-        for (int j = 0; j < ncand; ++j) rank += (ckey[j] == kth && cidx[j] < id);
-        take = rank < tie_need;
-      }
-      if (take) {
-        const int p = atomicAdd(&s_nsel, 1);
-        skey[p] = k;
-        sidx[p] = cidx[i];
-      }
-    }
-  } else {
-    kth = radix_select<false>(x, nullptr, V, Kc, hist, &s_prefix, &s_need, &tie_need);
-    // ordered pass over the row (ties keep the smallest ids)
-    if (tid == 0) s_tie = 0;
-    __syncthreads();
-    for (int base = 0; base < V; base += blockDim.x) {
-      const int v = base + tid;
-      uint32_t k = 0;
-      bool gt = false, eq = false;
-      if (v < V) {
-        k = order_key(x[v]);
-        gt = k > kth;
-        eq = k == kth;
-      }
-      if (gt) {
-        const int p = atomicAdd(&s_nsel, 1);
-        skey[p] = k;
-        sidx[p] = v;
-      }
-      // rank of this tie in id order: ties of earlier chunks, earlier warps, earlier lanes
-      const unsigned bal = __ballot_sync(0xffffffffu, eq);
-      const int before = block_excl_scan(lane == 0 ? __popc(bal) : 0, wsum, &s_total);
-      const int taken = s_tie;
-      const int off = __shfl_sync(0xffffffffu, before, 0);
-      if (eq && taken + off + __popc(bal & ((1u << lane) - 1u)) < tie_need) {
-        const int p = atomicAdd(&s_nsel, 1);
-        skey[p] = k;
-        sidx[p] = v;
-      }
-      __syncthreads();
-      if (tid == 0) s_tie = taken + s_total;
-      __syncthreads();
-    }
-  }
-  __syncthreads();
-  // 4. bitonic sort of the Kc selected: key descending, index ascending
+// Bitonic sort of the Kc selected (key descending, index ascending) and store.
+SPEC_DEV void sort_selected(uint32_t* skey, int* sidx, int Kc, int32_t* out) {
+  const int tid = threadIdx.x;
   int n2 = 1;
   while (n2 < Kc) n2 <<= 1;
   if (tid >= Kc && tid < n2) { skey[tid] = 0; sidx[tid] = 0x7fffffff; }
@@ -1285,7 +1145,191 @@ __global__ void __launch_bounds__(1024) topk_select_kernel(const float* __restri
       __syncthreads();
     }
   }
-  if (tid < Kc) out_ids[(size_t)m * Kc + tid] = sidx[tid];
+  if (tid < Kc) out[tid] = sidx[tid];
+}
+
+__global__ void __cluster_dims__(kTkCL, 1, 1) __launch_bounds__(1024)
+    topk_select_kernel(const float* __restrict__ s, int V, int Kc, int32_t* __restrict__ out_ids) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(16) uint8_t tk_smem[];
+  uint32_t* gkey = reinterpret_cast<uint32_t*>(tk_smem);              // [kTkCap] gathered copies (rank 0)
+  int* gidx = reinterpret_cast<int*>(gkey + kTkCap);
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(gidx + kTkCap);        // [kTkCapCta] this CTA's copies
+  int* cidx = reinterpret_cast<int*>(ckey + kTkCapCta);
+  uint32_t* skey = reinterpret_cast<uint32_t*>(cidx + kTkCapCta);     // [1024] maxima, then the selected
+  int* sidx = reinterpret_cast<int*>(skey + 1024);
+  int* hist = sidx + 1024;                                            // [256]
+  __shared__ int wsum[32];
+  __shared__ int s_total, s_nsel, s_nc, s_need, s_tie;
+  __shared__ uint32_t s_prefix, s_bound;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
+  const int m = blockIdx.x / kTkCL;
+  const float* x = s + (size_t)m * V;
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid == 0) { s_nsel = 0; s_nc = 0; }
+  // this CTA's groups of four consecutive elements (16-byte loads), UNR groups
+  // (4 * UNR loads) in flight per thread
+  constexpr int UNR = 4;
+  const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15u) == 0);
+  const int ng = (V + 3) / 4;
+  const int g0 = (int)((long long)rank * ng / kTkCL), g1 = (int)((long long)(rank + 1) * ng / kTkCL);
+  auto load4 = [&](int gi, float* v) {
+    if (gi >= g1) {
+      v[0] = v[1] = v[2] = v[3] = -INFINITY;
+    } else if (vec) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(x) + gi);
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = 4 * gi + e < V ? x[4 * gi + e] : -INFINITY;
+    }
+  };
+  // 1. per-thread maxima, the CTA's bound, the cluster's bound T0
+  uint32_t tmax = 0;
+  for (int base = g0; base < g1; base += UNR * blockDim.x) {
+    float v[UNR][4];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) load4(base + u * blockDim.x + tid, v[u]);
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int gi = base + u * blockDim.x + tid;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (gi < g1 && 4 * gi + e < V) tmax = max(tmax, order_key(v[u][e]));
+    }
+  }
+  skey[tid] = tmax;           // 0 for a thread without elements: below every key
+  __syncthreads();
+  int tie_need;
+  const uint32_t tb = radix_select<true>(nullptr, skey, blockDim.x, Kc, hist, &s_prefix, &s_need, &tie_need);
+  if (tid == 0) s_bound = tb;
+  cl.sync();
+  uint32_t t0 = 0;
+#pragma unroll
+  for (int r = 0; r < kTkCL; ++r) t0 = max(t0, *cl.map_shared_rank(&s_bound, r));
+  // 2. copy this CTA's elements >= T0
+  for (int base = g0; base < g1; base += UNR * blockDim.x) {
+    float v[UNR][4];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) load4(base + u * blockDim.x + tid, v[u]);
+    uint32_t takem = 0;
+    int cnt = 0;
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int gi = base + u * blockDim.x + tid;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (gi < g1 && 4 * gi + e < V && order_key(v[u][e]) >= t0) {
+          takem |= 1u << (4 * u + e);
+          ++cnt;
+        }
+    }
+    if (__ballot_sync(0xffffffffu, cnt > 0)) {
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int slot0 = 0;
+      if (lane == 31) slot0 = atomicAdd(&s_nc, incl);
+      slot0 = __shfl_sync(0xffffffffu, slot0, 31);
+      int p = slot0 + incl - cnt;
+#pragma unroll
+      for (int u = 0; u < UNR; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if ((takem >> (4 * u + e)) & 1u) {
+            if (p < kTkCapCta) {
+              ckey[p] = order_key(v[u][e]);
+              cidx[p] = 4 * (base + u * blockDim.x + tid) + e;
+            }
+            ++p;
+          }
+    }
+  }
+  cl.sync();                  // every CTA's copies and count are final
+  if (rank == 0) {
+    int cnt[kTkCL], total = 0;
+    bool over = false;
+#pragma unroll
+    for (int r = 0; r < kTkCL; ++r) {
+      cnt[r] = *cl.map_shared_rank(&s_nc, r);
+      over = over || cnt[r] > kTkCapCta;
+      total += cnt[r];
+    }
+    over = over || total > kTkCap;
+    uint32_t kth;
+    if (!over) {
+      // 3. gather, select, sort
+      int off = 0;
+#pragma unroll
+      for (int r = 0; r < kTkCL; ++r) {
+        const uint32_t* rk = cl.map_shared_rank(ckey, r);
+        const int* ri = cl.map_shared_rank(cidx, r);
+        for (int i = tid; i < cnt[r]; i += blockDim.x) {
+          gkey[off + i] = rk[i];
+          gidx[off + i] = ri[i];
+        }
+        off += cnt[r];
+      }
+      __syncthreads();
+      kth = radix_select<true>(nullptr, gkey, total, Kc, hist, &s_prefix, &s_need, &tie_need);
+      for (int i = tid; i < total; i += blockDim.x) {
+        const uint32_t k = gkey[i];
+        bool take = k > kth;
+        if (k == kth) {
+          const int id = gidx[i];
+          int rnk = 0;
+          for (int j = 0; j < total; ++j) rnk += (gkey[j] == kth && gidx[j] < id);
+          take = rnk < tie_need;
+        }
+        if (take) {
+          const int p = atomicAdd(&s_nsel, 1);
+          skey[p] = k;
+          sidx[p] = gidx[i];
+        }
+      }
+    } else {
+      kth = radix_select<false>(x, nullptr, V, Kc, hist, &s_prefix, &s_need, &tie_need);
+      // ordered pass over the row (ties keep the smallest ids)
+      if (tid == 0) s_tie = 0;
+      __syncthreads();
+      for (int base = 0; base < V; base += blockDim.x) {
+        const int v = base + tid;
+        uint32_t k = 0;
+        bool gt = false, eq = false;
+        if (v < V) {
+          k = order_key(x[v]);
+          gt = k > kth;
+          eq = k == kth;
+        }
+        if (gt) {
+          const int p = atomicAdd(&s_nsel, 1);
+          skey[p] = k;
+          sidx[p] = v;
+        }
+        // rank of this tie in id order: ties of earlier chunks, earlier warps, earlier lanes
+        const unsigned bal = __ballot_sync(0xffffffffu, eq);
+        const int before = block_excl_scan(lane == 0 ? __popc(bal) : 0, wsum, &s_total);
+        const int taken = s_tie;
+        const int o = __shfl_sync(0xffffffffu, before, 0);
+        if (eq && taken + o + __popc(bal & ((1u << lane) - 1u)) < tie_need) {
+          const int p = atomicAdd(&s_nsel, 1);
+          skey[p] = k;
+          sidx[p] = v;
+        }
+        __syncthreads();
+        if (tid == 0) s_tie = taken + s_total;
+        __syncthreads();
+      }
+    }
+    __syncthreads();
+    sort_selected(skey, sidx, Kc, out_ids + (size_t)m * Kc);
+  }
+  cl.sync();                  // no CTA leaves while rank 0 may still read its copies
 }
 
 // exact logits of the candidates: lm_head[cand] . hn[m]; one warp per candidate
@@ -1600,7 +1644,7 @@ void launch_topk_select(const float* s, int M, int V, int Kc, int32_t* out_ids, 
     cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)topk_select_smem());
     attr_dev = dev;
   }
-  launch_pdl(topk_select_kernel, dim3(M), dim3(1024), topk_select_smem(), st, s, V, Kc, out_ids);
+  launch_pdl(topk_select_kernel, dim3(M * kTkCL), dim3(1024), topk_select_smem(), st, s, V, Kc, out_ids);
 }
 
 void launch_rescore(int dtype, const void* hn, const void* lm_head, int H, int V, const int32_t* cand, int M, int Kc,
