@@ -126,6 +126,12 @@ def step_bytes(w):
     return total, lm_launch
 
 
+# DRAM traffic per launch of the dominant kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum from one ncu capture of the current kernel at this
+# workload's LM-head shape); workloads without a capture report null.
+LM_TRAFFIC = {"llama8b_chain": 1.086754e9 + 3.369472e6}
+
+
 def launches_per_step(w):
     layer = 11                                   # prologue, 4 GEMMs, 4 epilogues, attention + combine
     head = 6 if w.rank > 0 else 2                # fused LM head + merge, or the candidate head's 6
@@ -335,7 +341,8 @@ def run_gpu(args, w):
         "step_roofline": {"bytes": total_bytes, "t_roof_ms": total_bytes / (hbm * 1e9) * 1e3,
                           "frac": (total_bytes / (hbm * 1e9) * 1e3) / ms_step},
         "roofline": {"kernel": "tc_kernel<SchedRows, EpiStats> (LM head, fused top-k/lse)", "bound": "hbm",
-                     "achieved": lm_gbs, "peak": hbm, "unit": "GB/s", "frac": lm_gbs / hbm, "traffic": None,
+                     "achieved": lm_gbs, "peak": hbm, "unit": "GB/s", "frac": lm_gbs / hbm,
+                     "traffic": LM_TRAFFIC.get(w.name),
                      "peak_kind": kind + " (burst copy)", "ms_per_launch": lm_ms},
         "e2e": {"value": world * 1000.0 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

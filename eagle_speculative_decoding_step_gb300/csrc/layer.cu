@@ -20,6 +20,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "plan.cuh"
+#include "tc_core.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -658,13 +659,25 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
   __shared__ int s_lo[QM];
   __shared__ unsigned long long s_mask[QM];
   __shared__ int s_klo, s_nd;
+  __shared__ __align__(8) uint64_t full_bar[2];     // a ring slot's rows have landed
+  __shared__ int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = lane >> 2, tig = lane & 3;
   const int G = nq / nkv;
   const int nQall = ri.R * G;
-  // stale ring contents must be finite (P = 0 times a stale V must stay 0)
-  for (int e = tid; e < (int)(kRing / 16); e += blockDim.x) reinterpret_cast<uint4*>(mma_smem)[e] = make_uint4(0, 0, 0, 0);
+  const uint32_t bar0 = smem_u32(&full_bar[0]);
+  if (tid == 0) {
+    s_abort = 0;
+    tc::mbar_init(bar0, 128);                         // every thread arrives once per fill
+    tc::mbar_init(bar0 + 8, 128);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  volatile int* abort = &s_abort;
+  uint64_t kv_policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(kv_policy));
+  uint32_t fills = 0;                                 // ring fills consumed by this CTA before this item
+  bool ok_all = true;
 
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int s = item % nsplit;
@@ -720,44 +733,44 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
     const int kbeg = min(total, s * chunk), kend = min(total, kbeg + chunk);
     const int ntiles = (kend - kbeg + TK - 1) / TK;
 
-    // stage tile j into ring slot j & 1: thread t copies half (t & 1) of the K and V
-    // rows of key t >> 1 (one page-table lookup per thread)
+    // stage tile j into ring slot (fills + j) & 1: thread t moves one row, the K
+    // row (t < 64) or the V row (t >= 64) of key t & 63, with one bulk
+    // asynchronous copy whose bytes complete on the slot's mbarrier; keys
+    // without a slot get a zero row
     auto issue = [&](int j) {
-      if (j < ntiles) {
-        uint8_t* st = mma_smem + (size_t)(j & 1) * Sh::STAGE;
-        __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(st);
-        __nv_bfloat16* sV = sK + TK * KP;
-        const int t0 = kbeg + j * TK;
-        const int nk = min(TK, kend - t0);
-        const int kt = tid >> 1, c0 = (tid & 1) * (CH / 2);
-        int ci = -1;
-        long long slot = -1;
-        if (kt < nk) {
-          const int kidx = t0 + kt;
-          ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
-          slot = slot_of(kv, b, ci);
-        }
-        uint4* dk = reinterpret_cast<uint4*>(sK + kt * KP) + c0;
-        uint4* dv = reinterpret_cast<uint4*>(sV + kt * KP) + c0;
-        if (slot >= 0) {
-          const size_t off = ((size_t)slot * nkv + g) * HD;
-          const uint4* gk = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(kv.k) + off) + c0;
-          const uint4* gv = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(kv.v) + off) + c0;
-#pragma unroll
-          for (int c = 0; c < CH / 2; ++c) {
-            cp_async16(dk + c, gk + c);
-            cp_async16(dv + c, gv + c);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < CH / 2; ++c) {
-            dk[c] = make_uint4(0, 0, 0, 0);
-            dv[c] = make_uint4(0, 0, 0, 0);
-          }
-        }
-        if ((tid & 1) == 0) sCi[(j & 1) * TK + kt] = slot >= 0 ? ci : -1;
+      if (j >= ntiles) return;
+      const uint32_t fi = fills + (uint32_t)j;
+      uint8_t* st = mma_smem + (size_t)(fi & 1u) * Sh::STAGE;
+      const int t0 = kbeg + j * TK;
+      const int nk = min(TK, kend - t0);
+      const int kt = tid & (TK - 1);
+      const bool isv = tid >= TK;
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(st) + (isv ? TK * KP : 0) + kt * KP;
+      int ci = -1;
+      long long slot = -1;
+      if (kt < nk) {
+        const int kidx = t0 + kt;
+        ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
+        slot = slot_of(kv, b, ci);
       }
-      asm volatile("cp.async.commit_group;" ::: "memory");
+      if (!isv) sCi[(fi & 1u) * TK + kt] = slot >= 0 ? ci : -1;
+      const uint32_t bar = bar0 + 8u * (fi & 1u);
+      if (slot >= 0) {
+        // the row was last touched by ordinary loads (the previous tile, the merge
+        // buffer): order them before the copy engine's write
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc::mbar_expect_tx(bar, (uint32_t)(HD * 2));
+        const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(isv ? kv.v : kv.k) + ((size_t)slot * nkv + g) * HD;
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+            ::"r"(smem_u32(dst)), "l"(src), "r"(HD * 2), "r"(bar), "l"(kv_policy)
+            : "memory");
+      } else {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int c = 0; c < CH; ++c) d4[c] = make_uint4(0, 0, 0, 0);
+        tc::mbar_arrive(bar);
+      }
     };
 
     float acc[MT][NT][4];
@@ -789,11 +802,12 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
     issue(0);
     for (int j = 0; j < ntiles; ++j) {
       issue(j + 1);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-      __syncthreads();
-      const uint8_t* st = mma_smem + (size_t)(j & 1) * Sh::STAGE;
+      const uint32_t fi = fills + (uint32_t)j;
+      const bool ok = tc::mbar_wait(bar0 + 8u * (fi & 1u), (fi >> 1) & 1u, abort);
+      if (__syncthreads_or(!ok)) { ok_all = false; break; }
+      const uint8_t* st = mma_smem + (size_t)(fi & 1u) * Sh::STAGE;
       const uint32_t kbase = smem_u32(st), vbase = kbase + TK * KP * 2;
-      const int* ci_t = sCi + (j & 1) * TK;
+      const int* ci_t = sCi + (fi & 1u) * TK;
       // scores for this warp's 16 keys: S[mt][nt] (16 queries x 8 keys)
       float sc[MT][2][4];
 #pragma unroll
@@ -886,9 +900,10 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
           mma_bf16(acc[mt][2 * n2 + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v2, v3);
         }
       }
-      __syncthreads();     // ring slot j & 1 is refilled by the next iteration's copies
+      __syncthreads();     // this ring slot is refilled by the next iteration's copies
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (!ok_all) break;
+    fills += (uint32_t)ntiles;
     __syncthreads();
     // merge the four warps: row sums over the quad, then max / rescale through shared memory
 #pragma unroll
@@ -939,6 +954,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
     }
     __syncthreads();     // red / sQ / sMw reused by the next item
   }
+  if (!ok_all && tid == 0) report(ws, SPEC_ERR_TIMEOUT, blockIdx.x, 0);
 }
 
 template <typename T, int HD>
