@@ -607,6 +607,9 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const T* __restrict__ q
 // probabilities P (bf16) go straight from the score accumulators into the
 // P.V product's A operand; V tiles are read transposed by ldmatrix.
 constexpr int kMmaTK = 64;
+// K/V ring slots.  Two (one tile in flight ahead of the one in use) with three
+// CTAs per SM measured faster than three slots with two CTAs per SM.
+constexpr int mma_stages(int) { return 2; }
 
 template <int HD> struct MmaShape {
   static constexpr int KP = HD + 8;                         // padded bf16 row: ldmatrix rows on distinct banks
@@ -616,9 +619,9 @@ template <int HD> struct MmaShape {
 template <int HD, int MT>
 constexpr size_t attn_mma_smem() {
   using S = MmaShape<HD>;
-  const size_t ring = (size_t)2 * S::STAGE;
+  const size_t ring = (size_t)mma_stages(MT) * S::STAGE;
   const size_t red = (size_t)4 * 16 * MT * (HD + 8) * 4;      // the warps' outputs after the last tile (aliases the ring)
-  return (ring > red ? ring : red) + (size_t)16 * MT * S::KP * 2 + (size_t)2 * kMmaTK * 4;
+  return (ring > red ? ring : red) + (size_t)16 * MT * S::KP * 2 + (size_t)mma_stages(MT) * kMmaTK * 4;
 }
 
 SPEC_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -651,15 +654,16 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
   using Sh = MmaShape<HD>;
   constexpr int TK = kMmaTK, KP = Sh::KP, CH = HD / 8, QM = 16 * MT, NT = HD / 8, KS = HD / 16;
   extern __shared__ __align__(16) uint8_t mma_smem[];
-  constexpr size_t kRing = attn_mma_smem<HD, MT>() - (size_t)QM * KP * 2 - (size_t)2 * TK * 4;
+  constexpr int NS = mma_stages(MT);
+  constexpr size_t kRing = attn_mma_smem<HD, MT>() - (size_t)QM * KP * 2 - (size_t)NS * TK * 4;
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(mma_smem + kRing);   // [QM][KP]
-  int* sCi = reinterpret_cast<int*>(sQ + QM * KP);                          // [2][TK] cache index, -1 = no slot
+  int* sCi = reinterpret_cast<int*>(sQ + QM * KP);                          // [NS][TK] cache index, -1 = no slot
   float* red = reinterpret_cast<float*>(mma_smem);                           // [4][QM][HD + 8]
   __shared__ float sMw[4][QM], sLw[4][QM];
   __shared__ int s_lo[QM];
   __shared__ unsigned long long s_mask[QM];
   __shared__ int s_klo, s_nd;
-  __shared__ __align__(8) uint64_t full_bar[2];     // a ring slot's rows have landed
+  __shared__ __align__(8) uint64_t full_bar[NS];    // a ring slot's rows have landed
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -669,8 +673,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
   const uint32_t bar0 = smem_u32(&full_bar[0]);
   if (tid == 0) {
     s_abort = 0;
-    tc::mbar_init(bar0, 128);                         // every thread arrives once per fill
-    tc::mbar_init(bar0 + 8, 128);
+    for (int i = 0; i < NS; ++i) tc::mbar_init(bar0 + 8u * i, 128);   // every thread arrives once per fill
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   volatile int* abort = &s_abort;
@@ -733,14 +736,14 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
     const int kbeg = min(total, s * chunk), kend = min(total, kbeg + chunk);
     const int ntiles = (kend - kbeg + TK - 1) / TK;
 
-    // stage tile j into ring slot (fills + j) & 1: thread t moves one row, the K
+    // stage tile j into ring slot (fills + j) % NS: thread t moves one row, the K
     // row (t < 64) or the V row (t >= 64) of key t & 63, with one bulk
     // asynchronous copy whose bytes complete on the slot's mbarrier; keys
     // without a slot get a zero row
     auto issue = [&](int j) {
       if (j >= ntiles) return;
       const uint32_t fi = fills + (uint32_t)j;
-      uint8_t* st = mma_smem + (size_t)(fi & 1u) * Sh::STAGE;
+      uint8_t* st = mma_smem + (size_t)(fi % NS) * Sh::STAGE;
       const int t0 = kbeg + j * TK;
       const int nk = min(TK, kend - t0);
       const int kt = tid & (TK - 1);
@@ -753,8 +756,8 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
         ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
         slot = slot_of(kv, b, ci);
       }
-      if (!isv) sCi[(fi & 1u) * TK + kt] = slot >= 0 ? ci : -1;
-      const uint32_t bar = bar0 + 8u * (fi & 1u);
+      if (!isv) sCi[(fi % NS) * TK + kt] = slot >= 0 ? ci : -1;
+      const uint32_t bar = bar0 + 8u * (fi % NS);
       if (slot >= 0) {
         // the row was last touched by ordinary loads (the previous tile, the merge
         // buffer): order them before the copy engine's write
@@ -799,15 +802,16 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
         rmask[mt][h] = s_mask[qi];
       }
 
-    issue(0);
+#pragma unroll
+    for (int j = 0; j < NS - 1; ++j) issue(j);
     for (int j = 0; j < ntiles; ++j) {
-      issue(j + 1);
+      issue(j + NS - 1);
       const uint32_t fi = fills + (uint32_t)j;
-      const bool ok = tc::mbar_wait(bar0 + 8u * (fi & 1u), (fi >> 1) & 1u, abort);
+      const bool ok = tc::mbar_wait(bar0 + 8u * (fi % NS), (fi / NS) & 1u, abort);
       if (__syncthreads_or(!ok)) { ok_all = false; break; }
-      const uint8_t* st = mma_smem + (size_t)(fi & 1u) * Sh::STAGE;
+      const uint8_t* st = mma_smem + (size_t)(fi % NS) * Sh::STAGE;
       const uint32_t kbase = smem_u32(st), vbase = kbase + TK * KP * 2;
-      const int* ci_t = sCi + (fi & 1u) * TK;
+      const int* ci_t = sCi + (fi % NS) * TK;
       // scores for this warp's 16 keys: S[mt][nt] (16 queries x 8 keys)
       float sc[MT][2][4];
 #pragma unroll
