@@ -969,17 +969,26 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restric
   pdl_trigger();
   const int mh = blockIdx.x;          // m * nq + h
   const int d = threadIdx.x;
+  // the splits' (max, sum) pairs once into shared memory (nsplit <= 64 <= HD), the
+  // weights there too; then each thread sums its dimension over the splits with
+  // independent loads
+  __shared__ float sm_[64], sl_[64], sw[64];
+  if (d < nsplit) {
+    const float2 ml = mlpart[(size_t)mh * nsplit + d];
+    sm_[d] = ml.x;
+    sl_[d] = ml.y;
+  }
+  __syncthreads();
   float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, mlpart[(size_t)mh * nsplit + s].x);
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, sm_[s]);
+  if (d < nsplit) sw[d] = (M > -INFINITY && sm_[d] > -INFINITY) ? expf(sm_[d] - M) : 0.f;
+  __syncthreads();
   float L = 0.f, o = 0.f;
-  if (M > -INFINITY) {
-    for (int s = 0; s < nsplit; ++s) {
-      const float2 ml = mlpart[(size_t)mh * nsplit + s];
-      if (ml.x == -INFINITY) continue;
-      const float w = expf(ml.x - M);
-      L += ml.y * w;
-      o += opart[((size_t)mh * nsplit + s) * HD + d] * w;
-    }
+  const float* op = opart + (size_t)mh * nsplit * HD + d;
+#pragma unroll 4
+  for (int s = 0; s < nsplit; ++s) {
+    L += sl_[s] * sw[s];
+    o += op[(size_t)s * HD] * sw[s];
   }
   st(out + (size_t)mh * HD + d, L > 0.f ? o / L : 0.f);
 }

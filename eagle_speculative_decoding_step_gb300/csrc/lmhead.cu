@@ -188,9 +188,9 @@ struct EpiStats {
 }  // namespace tc
 
 // Merge the per-CTA records of row m: lse (whole block) and the k best (the
-// records' lists are staged in shared memory; warp 0: every lane keeps a sorted
-// top-KT of the entries it scans, then k rounds of a warp argmax over the
-// lanes' heads).
+// records' lists are staged in shared memory; every thread keeps a sorted top-KT
+// of the entries it scans, every warp takes its k best by k rounds of a warp
+// argmax over the lanes' heads, and warp 0 does the same over the warps' lists).
 constexpr int kLmMaxCtas = 256;
 
 template <int KT>
@@ -220,16 +220,17 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__
   }
   s = block_sum(s, red);      // its barriers also publish cv / ci
   const float lse = mx + logf(s);
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // every thread: a sorted top-KT of the entries it scans; every warp: its best k
+  // by k rounds of a warp argmax over the lanes' heads; warp 0: the best k of those
+  __shared__ float wv[8][KT];
+  __shared__ int wi[8][KT];
   float tv[KT];
   int ti[KT];
 #pragma unroll
   for (int q = 0; q < KT; ++q) { tv[q] = -INFINITY; ti[q] = 0x7fffffff; }
-  for (int e = lane; e < G * KT; e += 32) {
-    const float v = cv[e];
-    const int i = ci[e];
-    if (!better(v, i, tv[KT - 1], ti[KT - 1])) continue;
+  auto insert = [&](float v, int i) {
+    if (!better(v, i, tv[KT - 1], ti[KT - 1])) return;
 #pragma unroll
     for (int q = KT - 1; q >= 0; --q) {
       if (better(v, i, tv[q], ti[q])) {
@@ -242,20 +243,36 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__
         }
       }
     }
-  }
-  for (int rr = 0; rr < k; ++rr) {
-    float bv = tv[0];
-    int bi = ti[0];
-    warp_argmax(bv, bi);
-    if (ti[0] == bi) {          // the lane whose head won pops it (ids are distinct)
+  };
+  auto pop_rounds = [&](float* ov, int* oi) {     // k rounds; lane 0 receives the winners
+    for (int rr = 0; rr < k; ++rr) {
+      float bv = tv[0];
+      int bi = ti[0];
+      warp_argmax(bv, bi);
+      if (ti[0] == bi && bv == tv[0]) {           // the lane whose head won pops it
 #pragma unroll
-      for (int q = 0; q < KT - 1; ++q) { tv[q] = tv[q + 1]; ti[q] = ti[q + 1]; }
-      tv[KT - 1] = -INFINITY;
-      ti[KT - 1] = 0x7fffffff;
+        for (int q = 0; q < KT - 1; ++q) { tv[q] = tv[q + 1]; ti[q] = ti[q + 1]; }
+        tv[KT - 1] = -INFINITY;
+        ti[KT - 1] = 0x7fffffff;
+      }
+      if (lane == 0) { ov[rr] = bv; oi[rr] = bi; }
     }
-    if (lane == 0) {
-      ids[(size_t)m * ld_ids + rr] = d2t ? d2t[bi] : bi;
-      lp[(size_t)m * ld_ids + rr] = bv - lse;
+  };
+  for (int e = threadIdx.x; e < G * KT; e += blockDim.x) insert(cv[e], ci[e]);
+  pop_rounds(wv[warp], wi[warp]);
+  __syncthreads();
+  if (warp != 0) return;
+#pragma unroll
+  for (int q = 0; q < KT; ++q) { tv[q] = -INFINITY; ti[q] = 0x7fffffff; }
+  const int nw = blockDim.x >> 5;
+  for (int e = lane; e < nw * k; e += 32) insert(wv[e / k][e % k], wi[e / k][e % k]);
+  float fv[KT];
+  int fi[KT];
+  pop_rounds(fv, fi);
+  if (lane == 0) {
+    for (int rr = 0; rr < k; ++rr) {
+      ids[(size_t)m * ld_ids + rr] = d2t ? d2t[fi[rr]] : fi[rr];
+      lp[(size_t)m * ld_ids + rr] = fv[rr] - lse;
     }
   }
   if (lane == 0 && lse_out) lse_out[m] = lse;

@@ -51,12 +51,23 @@ __global__ void __launch_bounds__(256) argmax_chunks_kernel(const float* __restr
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   if (VEC) {
-    for (int j = lo + 4 * threadIdx.x; j < hi; j += 4 * blockDim.x) {
-      float4 q = *reinterpret_cast<const float4*>(x + j);
-      if (better(q.x, j, bv, bi)) { bv = q.x; bi = j; }
-      if (j + 1 < hi && better(q.y, j + 1, bv, bi)) { bv = q.y; bi = j + 1; }
-      if (j + 2 < hi && better(q.z, j + 2, bv, bi)) { bv = q.z; bi = j + 2; }
-      if (j + 3 < hi && better(q.w, j + 3, bv, bi)) { bv = q.w; bi = j + 3; }
+    // four 16-byte loads in flight per thread
+    for (int j0 = lo + 4 * threadIdx.x; j0 < hi; j0 += 16 * blockDim.x) {
+      float4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + 4 * u * blockDim.x;
+        if (j < hi) q[u] = *reinterpret_cast<const float4*>(x + j);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + 4 * u * blockDim.x;
+        if (j >= hi) break;
+        if (better(q[u].x, j, bv, bi)) { bv = q[u].x; bi = j; }
+        if (j + 1 < hi && better(q[u].y, j + 1, bv, bi)) { bv = q[u].y; bi = j + 1; }
+        if (j + 2 < hi && better(q[u].z, j + 2, bv, bi)) { bv = q[u].z; bi = j + 2; }
+        if (j + 3 < hi && better(q[u].w, j + 3, bv, bi)) { bv = q[u].w; bi = j + 3; }
+      }
     }
   } else {
     for (int j = lo + threadIdx.x; j < hi; j += blockDim.x) {
@@ -384,35 +395,48 @@ __global__ void __launch_bounds__(256) rej_stats_kernel(const float* __restrict_
   const int lo = c * L, hi = min(V, lo + L);
   float m = -INFINITY, s = 0.f, bk = -INFINITY;
   int bi = 0x7fffffff;
-  for (int j = lo + 4 * threadIdx.x; j < hi; j += 4 * blockDim.x) {
-    float v[4];
-    if (VEC) {
-      float4 q = *reinterpret_cast<const float4*>(x + j);
-      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-    } else {
+  constexpr int UNR = 4;                      // 16-byte loads in flight per thread
+  for (int j0 = lo + 4 * threadIdx.x; j0 < hi; j0 += 4 * UNR * blockDim.x) {
+    float vv[UNR][4];
 #pragma unroll
-      for (int l = 0; l < 4; ++l) v[l] = (j + l < hi) ? x[j + l] : -INFINITY;
-    }
-    if (greedy) {
+    for (int u = 0; u < UNR; ++u) {
+      const int j = j0 + 4 * u * blockDim.x;
+      if (VEC) {
+        if (j < hi) {
+          const float4 q = *reinterpret_cast<const float4*>(x + j);
+          vv[u][0] = q.x; vv[u][1] = q.y; vv[u][2] = q.z; vv[u][3] = q.w;
+        }
+      } else {
 #pragma unroll
-      for (int l = 0; l < 4; ++l)
-        if (j + l < hi && better(v[l], j + l, bk, bi)) { bk = v[l]; bi = j + l; }
-      continue;
+        for (int l = 0; l < 4; ++l) vv[u][l] = (j + l < hi) ? x[j + l] : -INFINITY;
+      }
     }
-    // the group's kept values, -inf for the rest (ids past hi, filtered by top-k / top-p)
-    float y[4];
 #pragma unroll
-    for (int l = 0; l < 4; ++l) {
-      y[l] = (j + l < hi) ? (unit ? v[l] : v[l] / T) : -INFINITY;
-      if (filt && y[l] > -INFINITY && !kept_by(tr, okey(y[l]), j + l)) y[l] = -INFINITY;
+    for (int u = 0; u < UNR; ++u) {
+      const int j = j0 + 4 * u * blockDim.x;
+      if (j >= hi) break;
+      const float* v = vv[u];
+      if (greedy) {
+#pragma unroll
+        for (int l = 0; l < 4; ++l)
+          if (j + l < hi && better(v[l], j + l, bk, bi)) { bk = v[l]; bi = j + l; }
+        continue;
+      }
+      // the group's kept values, -inf for the rest (ids past hi, filtered by top-k / top-p)
+      float y[4];
+#pragma unroll
+      for (int l = 0; l < 4; ++l) {
+        y[l] = (j + l < hi) ? (unit ? v[l] : v[l] / T) : -INFINITY;
+        if (filt && y[l] > -INFINITY && !kept_by(tr, okey(y[l]), j + l)) y[l] = -INFINITY;
+      }
+      // online sum of exp: one max update per group of four
+      const float gm = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
+      if (gm > m) {
+        s *= __expf(m - gm);
+        m = gm;
+      }
+      if (m > -INFINITY) s += (__expf(y[0] - m) + __expf(y[1] - m)) + (__expf(y[2] - m) + __expf(y[3] - m));
     }
-    // online sum of exp: one max update per group of four
-    const float gm = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
-    if (gm > m) {
-      s *= __expf(m - gm);
-      m = gm;
-    }
-    if (m > -INFINITY) s += (__expf(y[0] - m) + __expf(y[1] - m)) + (__expf(y[2] - m) + __expf(y[3] - m));
   }
   const float bm = block_max(m, red);
   const float contrib = (m == -INFINITY) ? 0.f : s * expf(m - bm);
