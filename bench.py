@@ -132,6 +132,17 @@ def step_bytes(w):
 LM_TRAFFIC = {"llama8b_chain": 1.086754e9 + 3.369472e6}
 
 
+def config_of(w):
+    """The workload as both arms report it."""
+    total_bytes, _ = step_bytes(w)
+    return {"workload": w.name, "H": w.H, "heads": [w.nq, w.nkv], "head_dim": w.hd, "I": w.I, "V": w.V,
+            "batch": w.B, "ctx": list(w.ctx_range) if w.ctx_range else w.ctx, "mode": w.mode,
+            "K": w.K if w.mode == "chain" else None,
+            "tree": [w.top_k, w.depth, w.total] if w.mode == "tree" else None,
+            "window": w.window, "rank": w.rank, "verify": w.verify,
+            "l2": "inputs larger than L2 (weights %.2f GB streamed per step)" % (total_bytes / 1e9)}
+
+
 def launches_per_step(w):
     layer = 11                                   # prologue, 4 GEMMs, 4 epilogues, attention + combine
     head = 6 if w.rank > 0 else 2                # fused LM head + merge, or the candidate head's 6
@@ -329,13 +340,7 @@ def run_gpu(args, w):
         "metric": METRIC, "value": aggregate_steps_per_s(world, ms_step), "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded random-init weights, N(0,1) aux states and context K/V)",
-        "config": {"workload": w.name, "H": w.H, "heads": [w.nq, w.nkv], "head_dim": w.hd, "I": w.I, "V": w.V,
-                   "batch": w.B, "ctx": list(w.ctx_range) if w.ctx_range else w.ctx, "mode": w.mode,
-                   "K": w.K if w.mode == "chain" else None,
-                   "tree": [w.top_k, w.depth, w.total] if w.mode == "tree" else None,
-                   "window": w.window, "rank": w.rank, "verify": w.verify,
-                   "l2": "inputs larger than L2 (weights %.2f GB streamed per step)" % (total_bytes / 1e9),
-                   "graph": "one CUDA graph per step"},
+        "config": config_of(w), "timing": "one CUDA graph per step, CUDA events on the replay stream",
         "draft_tokens_per_s": world * proposed * 1000.0 / ms_step,
         "verified_tokens_per_s": world * verified * 1000.0 / ms_step,
         "step_roofline": {"bytes": total_bytes, "t_roof_ms": total_bytes / (hbm * 1e9) * 1e3,
@@ -430,7 +435,7 @@ def main():
         print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": 1,
                           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                          "config": {"workload": w.name},
+                          "config": config_of(w),
                           "cpu_baseline": {"value": v, "unit": "steps/s", "cores": os.cpu_count(),
                                            "kind": "oracle", "sample": o.describe()},
                           "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
