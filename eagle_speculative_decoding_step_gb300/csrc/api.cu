@@ -15,7 +15,7 @@ void launch_prologue(const spec_model_desc&, const spec_rows&, const spec_weight
                      void*, cudaStream_t);
 void launch_epi_store(int, const float*, const SKPlan&, int, int, void*, int, cudaStream_t);
 void launch_epi_qkv(const spec_model_desc&, const float*, const SKPlan&, const spec_rows&, const float2*, void*,
-                    const spec_kv&, void*, cudaStream_t);
+                    const spec_kv&, int*, void*, cudaStream_t);
 void launch_epi_oproj(const spec_model_desc&, const float*, const SKPlan&, const spec_rows&, const void*,
                       const spec_weights&, float*, void*, cudaStream_t);
 void launch_epi_swiglu(const spec_model_desc&, const float*, const SKPlan&, int, void*, cudaStream_t);
@@ -32,7 +32,7 @@ int attn_splits(int B, int nkv, int nqg, int sms, int max_keys);
 int attn_splits_max(const spec_model_desc& d, int M, int sms);
 int attn_qmax(int rows_per_req, int G);
 spec_status launch_attention(const spec_model_desc&, const spec_rows&, const void*, const spec_kv&, float*, float2*,
-                             void*, int, void*, cudaStream_t);
+                             void*, int, int*, void*, cudaStream_t);
 void launch_row_stats(const float*, int, int, int, int32_t*, int, float*, float*, const int32_t*, cudaStream_t);
 void launch_topk_select(const float*, int, int, int, int32_t*, cudaStream_t);
 void launch_rescore(int, const void*, const void*, int, int, const int32_t*, int, int, float*, void*, cudaStream_t);
@@ -113,6 +113,7 @@ WsLayout ws_layout(const spec_model_desc& d, int M, int /*max_ctx*/, int sms) {
   const int smax = attn_splits_max(d, M, sms);
   L.attn_splits = smax;
   L.attn_part = take((size_t)M * nq * smax * hd * 4 + (size_t)M * nq * smax * 8);
+  L.attn_work = take(4);                       // the attention's item counter
   L.attn = take((size_t)M * nq * hd * es);
   L.r1 = take((size_t)M * H * 4);
   L.n = take((size_t)M * H * es);
@@ -306,14 +307,15 @@ extern "C" spec_status spec_draft_layer(const spec_model_desc* desc, const spec_
   if ((s = gemm(d, {w->wq, w->wk, w->wv}, {nq * hd, nkv * hd, nkv * hd}, 2 * H, x, M, part, ws, stream, &p)) !=
       SPEC_OK)
     return s;
-  launch_epi_qkv(d, part, p, r, cs, qbuf, *kv, ws, stream);
+  int* work = at<int>(ws, L.attn_work);
+  launch_epi_qkv(d, part, p, r, cs, qbuf, *kv, work, ws, stream);
   const int G = nq / nkv;
   const int qmax = attn_qmax(r.rows_per_req, G);
   const int nqg = (r.rows_per_req * G + qmax - 1) / qmax;
   int max_keys = 0;
   if (r.max_ctx > 0) max_keys = (d.window > 0 ? std::min(r.max_ctx, d.window) : r.max_ctx) + 64;
   const int nsplit = std::min(attn_splits(r.B, nkv, nqg, sm_count(), max_keys), L.attn_splits);
-  if ((s = launch_attention(d, r, qbuf, *kv, opart, mlpart, attn, nsplit, ws, stream)) != SPEC_OK) return s;
+  if ((s = launch_attention(d, r, qbuf, *kv, opart, mlpart, attn, nsplit, work, ws, stream)) != SPEC_OK) return s;
   if ((s = gemm(d, {w->wo}, {H}, nq * hd, attn, M, part, ws, stream, &p)) != SPEC_OK) return s;
   launch_epi_oproj(d, part, p, r, hid_in, *w, r1, nbuf, stream);
   if ((s = gemm(d, {w->wgate, w->wup}, {I, I}, H, nbuf, M, part, ws, stream, &p)) != SPEC_OK) return s;

@@ -146,9 +146,11 @@ __global__ void epi_store_kernel(const float* __restrict__ part, SKPlan p, int M
 // qbuf [M, nq*hd], k and v to the paged cache at entry ctx + kv_idx.
 template <typename T>
 __global__ void epi_qkv_kernel(const float* __restrict__ part, SKPlan p, RowInfo ri, int nq, int nkv, int hd,
-                               const float2* __restrict__ cs, T* __restrict__ qbuf, spec_kv kv, void* ws) {
+                               const float2* __restrict__ cs, T* __restrict__ qbuf, spec_kv kv, int* __restrict__ work,
+                               void* ws) {
   pdl_wait();
   pdl_trigger();
+  if (work != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *work = 0;   // the attention's item counter
   const int half = hd / 2;
   const int nh = nq + 2 * nkv;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -648,7 +650,8 @@ template <int HD, int MT>
 __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __restrict__ qbuf, spec_kv kv, RowInfo ri,
                                                        int nq, int nkv, int window, int nsplit, int nqg,
                                                        int n_items, float scale_log2, float* __restrict__ opart,
-                                                       float2* __restrict__ mlpart, void* ws) {
+                                                       float2* __restrict__ mlpart, int* __restrict__ work,
+                                                       void* ws) {
   pdl_wait();
   pdl_trigger();
   using Sh = MmaShape<HD>;
@@ -664,7 +667,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
   __shared__ unsigned long long s_mask[QM];
   __shared__ int s_klo, s_nd;
   __shared__ __align__(8) uint64_t full_bar[NS];    // a ring slot's rows have landed
-  __shared__ int s_abort;
+  __shared__ int s_abort, s_next;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = lane >> 2, tig = lane & 3;
@@ -682,7 +685,9 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
   uint32_t fills = 0;                                 // ring fills consumed by this CTA before this item
   bool ok_all = true;
 
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+  // items: blockIdx.x first, then the next unclaimed one from a shared counter (ragged
+  // requests make items of very different lengths; claiming balances them)
+  for (int item = blockIdx.x; item < n_items;) {
     const int s = item % nsplit;
     const int g = (item / nsplit) % nkv;
     const int bq = item / (nsplit * nkv);
@@ -717,17 +722,6 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
         s_nd = om ? 64 - __clzll((long long)om) : 0;
       }
     }
-    // queries of the item (bf16, unscaled), zero rows past nQ
-    for (int e = tid; e < QM * CH; e += blockDim.x) {
-      const int qi = e / CH, c = e % CH;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (qi < nQ) {
-        const int q = q0 + qi;
-        const int m = b * ri.R + q / G, h = g * G + q % G;
-        v = *reinterpret_cast<const uint4*>(qbuf + ((size_t)m * nq + h) * HD + c * 8);
-      }
-      *reinterpret_cast<uint4*>(sQ + qi * KP + c * 8) = v;
-    }
     __syncthreads();
     const int klo = s_klo, nd = s_nd;
     const int nctx = ctx - klo;
@@ -735,228 +729,260 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
     const int chunk = ((total + nsplit - 1) / nsplit + TK - 1) / TK * TK;
     const int kbeg = min(total, s * chunk), kend = min(total, kbeg + chunk);
     const int ntiles = (kend - kbeg + TK - 1) / TK;
-
-    // stage tile j into ring slot (fills + j) % NS: thread t moves one row, the K
-    // row (t < 64) or the V row (t >= 64) of key t & 63, with one bulk
-    // asynchronous copy whose bytes complete on the slot's mbarrier; keys
-    // without a slot get a zero row
-    auto issue = [&](int j) {
-      if (j >= ntiles) return;
-      const uint32_t fi = fills + (uint32_t)j;
-      uint8_t* st = mma_smem + (size_t)(fi % NS) * Sh::STAGE;
-      const int t0 = kbeg + j * TK;
-      const int nk = min(TK, kend - t0);
-      const int kt = tid & (TK - 1);
-      const bool isv = tid >= TK;
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(st) + (isv ? TK * KP : 0) + kt * KP;
-      int ci = -1;
-      long long slot = -1;
-      if (kt < nk) {
-        const int kidx = t0 + kt;
-        ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
-        slot = slot_of(kv, b, ci);
+    if (ntiles > 0) {
+      // queries of the item (bf16, unscaled), zero rows past nQ
+      for (int e = tid; e < QM * CH; e += blockDim.x) {
+        const int qi = e / CH, c = e % CH;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (qi < nQ) {
+          const int q = q0 + qi;
+          const int m = b * ri.R + q / G, h = g * G + q % G;
+          v = *reinterpret_cast<const uint4*>(qbuf + ((size_t)m * nq + h) * HD + c * 8);
+        }
+        *reinterpret_cast<uint4*>(sQ + qi * KP + c * 8) = v;
       }
-      if (!isv) sCi[(fi % NS) * TK + kt] = slot >= 0 ? ci : -1;
-      const uint32_t bar = bar0 + 8u * (fi % NS);
-      if (slot >= 0) {
-        // the row was last touched by ordinary loads (the previous tile, the merge
-        // buffer): order them before the copy engine's write
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc::mbar_expect_tx(bar, (uint32_t)(HD * 2));
-        const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(isv ? kv.v : kv.k) + ((size_t)slot * nkv + g) * HD;
-        asm volatile(
-            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
-            ::"r"(smem_u32(dst)), "l"(src), "r"(HD * 2), "r"(bar), "l"(kv_policy)
-            : "memory");
-      } else {
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-        for (int c = 0; c < CH; ++c) d4[c] = make_uint4(0, 0, 0, 0);
-        tc::mbar_arrive(bar);
+    } else {
+      // an empty split (a short request): its partials say "no keys"
+      for (int e = tid; e < nQ * HD; e += blockDim.x) {
+        const int qi = e / HD, d = e % HD;
+        const int q = q0 + qi;
+        const size_t base = ((size_t)(b * ri.R + q / G) * nq + g * G + q % G) * nsplit + s;
+        opart[base * HD + d] = 0.f;
+        if (d == 0) mlpart[base] = make_float2(-INFINITY, 0.f);
       }
-    };
-
-    float acc[MT][NT][4];
-    float mrun[MT][2], lrun[MT][2];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-      for (int n = 0; n < NT; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mt][n][e] = 0.f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) { mrun[mt][h] = -INFINITY; lrun[mt][h] = 0.f; }
     }
-    const uint32_t qbase = smem_u32(sQ);
-    // per-row constants of this thread's rows (m-tile mt, half h: row mt*16 + grp + 8h)
-    int rlo[MT][2];
-    unsigned long long rmask[MT][2];
-    bool rok[MT][2];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int qi = mt * 16 + grp + 8 * h;
-        rok[mt][h] = qi < nQ;
-        rlo[mt][h] = s_lo[qi];
-        rmask[mt][h] = s_mask[qi];
-      }
+    __syncthreads();
 
+    if (ntiles > 0) {
+      // stage tile j into ring slot (fills + j) % NS: thread t moves one row, the K
+      // row (t < 64) or the V row (t >= 64) of key t & 63, with one bulk
+      // asynchronous copy whose bytes complete on the slot's mbarrier; keys
+      // without a slot get a zero row
+      auto issue = [&](int j) {
+        if (j >= ntiles) return;
+        const uint32_t fi = fills + (uint32_t)j;
+        uint8_t* st = mma_smem + (size_t)(fi % NS) * Sh::STAGE;
+        const int t0 = kbeg + j * TK;
+        const int nk = min(TK, kend - t0);
+        const int kt = tid & (TK - 1);
+        const bool isv = tid >= TK;
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(st) + (isv ? TK * KP : 0) + kt * KP;
+        int ci = -1;
+        long long slot = -1;
+        if (kt < nk) {
+          const int kidx = t0 + kt;
+          ci = kidx < nctx ? klo + kidx : ctx + (kidx - nctx);
+          slot = slot_of(kv, b, ci);
+        }
+        if (!isv) sCi[(fi % NS) * TK + kt] = slot >= 0 ? ci : -1;
+        const uint32_t bar = bar0 + 8u * (fi % NS);
+        if (slot >= 0) {
+          // the row was last touched by ordinary loads (the previous tile, the merge
+          // buffer): order them before the copy engine's write
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tc::mbar_expect_tx(bar, (uint32_t)(HD * 2));
+          const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(isv ? kv.v : kv.k) + ((size_t)slot * nkv + g) * HD;
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+              ::"r"(smem_u32(dst)), "l"(src), "r"(HD * 2), "r"(bar), "l"(kv_policy)
+              : "memory");
+        } else {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-    for (int j = 0; j < NS - 1; ++j) issue(j);
-    for (int j = 0; j < ntiles; ++j) {
-      issue(j + NS - 1);
-      const uint32_t fi = fills + (uint32_t)j;
-      const bool ok = tc::mbar_wait(bar0 + 8u * (fi % NS), (fi / NS) & 1u, abort);
-      if (__syncthreads_or(!ok)) { ok_all = false; break; }
-      const uint8_t* st = mma_smem + (size_t)(fi % NS) * Sh::STAGE;
-      const uint32_t kbase = smem_u32(st), vbase = kbase + TK * KP * 2;
-      const int* ci_t = sCi + (fi % NS) * TK;
-      // scores for this warp's 16 keys: S[mt][nt] (16 queries x 8 keys)
-      float sc[MT][2][4];
+          for (int c = 0; c < CH; ++c) d4[c] = make_uint4(0, 0, 0, 0);
+          tc::mbar_arrive(bar);
+        }
+      };
+
+      float acc[MT][NT][4];
+      float mrun[MT][2], lrun[MT][2];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[mt][n][e] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) { mrun[mt][h] = -INFINITY; lrun[mt][h] = 0.f; }
+      }
+      const uint32_t qbase = smem_u32(sQ);
+      // per-row constants of this thread's rows (m-tile mt, half h: row mt*16 + grp + 8h)
+      int rlo[MT][2];
+      unsigned long long rmask[MT][2];
+      bool rok[MT][2];
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int h = 0; h < 2; ++h) {
+          const int qi = mt * 16 + grp + 8 * h;
+          rok[mt][h] = qi < nQ;
+          rlo[mt][h] = s_lo[qi];
+          rmask[mt][h] = s_mask[qi];
+        }
+
 #pragma unroll
-          for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
-      const uint32_t krow = kbase + (uint32_t)((warp * 16 + 8 * (lane >> 4) + (lane & 7)) * KP +
-                                               8 * ((lane >> 3) & 1)) * 2;
-      const uint32_t qrow = qbase + (uint32_t)((8 * ((lane >> 3) & 1) + (lane & 7)) * KP + 8 * (lane >> 4)) * 2;
+      for (int j = 0; j < NS - 1; ++j) issue(j);
+      for (int j = 0; j < ntiles; ++j) {
+        issue(j + NS - 1);
+        const uint32_t fi = fills + (uint32_t)j;
+        const bool ok = tc::mbar_wait(bar0 + 8u * (fi % NS), (fi / NS) & 1u, abort);
+        if (__syncthreads_or(!ok)) { ok_all = false; break; }
+        const uint8_t* st = mma_smem + (size_t)(fi % NS) * Sh::STAGE;
+        const uint32_t kbase = smem_u32(st), vbase = kbase + TK * KP * 2;
+        const int* ci_t = sCi + (fi % NS) * TK;
+        // scores for this warp's 16 keys: S[mt][nt] (16 queries x 8 keys)
+        float sc[MT][2][4];
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t b0, b1, b2, b3;   // keys 16w + {0..7, 8..15} x dims ks*16 + {0..7, 8..15}
-        ldsm_x4(krow + (uint32_t)(ks * 16 * 2), b0, b1, b2, b3);
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+        const uint32_t krow = kbase + (uint32_t)((warp * 16 + 8 * (lane >> 4) + (lane & 7)) * KP +
+                                                 8 * ((lane >> 3) & 1)) * 2;
+        const uint32_t qrow = qbase + (uint32_t)((8 * ((lane >> 3) & 1) + (lane & 7)) * KP + 8 * (lane >> 4)) * 2;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t b0, b1, b2, b3;   // keys 16w + {0..7, 8..15} x dims ks*16 + {0..7, 8..15}
+          ldsm_x4(krow + (uint32_t)(ks * 16 * 2), b0, b1, b2, b3);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(qrow + (uint32_t)((mt * 16 * KP + ks * 16) * 2), a0, a1, a2, a3);
+            mma_bf16(sc[mt][0], a0, a1, a2, a3, b0, b1);
+            mma_bf16(sc[mt][1], a0, a1, a2, a3, b2, b3);
+          }
+        }
+        // mask, scale to log2 units, warp-local online softmax
+        int kci[4];                 // cache index of this thread's four keys (-1: no slot)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) kci[u] = ci_t[warp * 16 + (u >> 1) * 8 + 2 * tig + (u & 1)];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(qrow + (uint32_t)((mt * 16 * KP + ks * 16) * 2), a0, a1, a2, a3);
-          mma_bf16(sc[mt][0], a0, a1, a2, a3, b0, b1);
-          mma_bf16(sc[mt][1], a0, a1, a2, a3, b2, b3);
-        }
-      }
-      // mask, scale to log2 units, warp-local online softmax
-      int kci[4];                 // cache index of this thread's four keys (-1: no slot)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) kci[u] = ci_t[warp * 16 + (u >> 1) * 8 + 2 * tig + (u & 1)];
+          for (int h = 0; h < 2; ++h) {
+            if (mt * 16 + 8 * h >= nQ) continue;     // rows of zero queries only (uniform in the warp)
+            const bool qok = rok[mt][h];
+            const int qlo = rlo[mt][h];
+            const unsigned long long qmask = rmask[mt][h];
+            float mx = -INFINITY;
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (mt * 16 + 8 * h >= nQ) continue;     // rows of zero queries only (uniform in the warp)
-          const bool qok = rok[mt][h];
-          const int qlo = rlo[mt][h];
-          const unsigned long long qmask = rmask[mt][h];
-          float mx = -INFINITY;
+              for (int e = 0; e < 2; ++e) {
+                const int ci = kci[2 * nt + e];
+                bool ok = qok && ci >= 0;
+                if (ok) ok = ci < ctx ? ci >= qlo : ((qmask >> (ci - ctx)) & 1ull) != 0;
+                const float v = ok ? sc[mt][nt][2 * h + e] * scale_log2 : -INFINITY;
+                sc[mt][nt][2 * h + e] = v;
+                mx = fmaxf(mx, v);
+              }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float mnew = fmaxf(mrun[mt][h], mx);
+            const float al = mnew == -INFINITY ? 1.f : exp2f(mrun[mt][h] - mnew);
+            float ps = 0.f;
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int ci = kci[2 * nt + e];
-              bool ok = qok && ci >= 0;
-              if (ok) ok = ci < ctx ? ci >= qlo : ((qmask >> (ci - ctx)) & 1ull) != 0;
-              const float v = ok ? sc[mt][nt][2 * h + e] * scale_log2 : -INFINITY;
-              sc[mt][nt][2 * h + e] = v;
-              mx = fmaxf(mx, v);
-            }
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const float mnew = fmaxf(mrun[mt][h], mx);
-          const float al = mnew == -INFINITY ? 1.f : exp2f(mrun[mt][h] - mnew);
-          float ps = 0.f;
+              for (int e = 0; e < 2; ++e) {
+                const float p = mnew == -INFINITY ? 0.f : exp2f(sc[mt][nt][2 * h + e] - mnew);
+                sc[mt][nt][2 * h + e] = p;
+                ps += p;
+              }
+            lrun[mt][h] = lrun[mt][h] * al + ps;
+            mrun[mt][h] = mnew;
+            if (al != 1.f) {
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float p = mnew == -INFINITY ? 0.f : exp2f(sc[mt][nt][2 * h + e] - mnew);
-              sc[mt][nt][2 * h + e] = p;
-              ps += p;
-            }
-          lrun[mt][h] = lrun[mt][h] * al + ps;
-          mrun[mt][h] = mnew;
-          if (al != 1.f) {
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-              acc[mt][n][2 * h] *= al;
-              acc[mt][n][2 * h + 1] *= al;
+              for (int n = 0; n < NT; ++n) {
+                acc[mt][n][2 * h] *= al;
+                acc[mt][n][2 * h + 1] *= al;
+              }
             }
           }
         }
-      }
-      // P.V: A = P (queries x this warp's 16 keys), B = V^T via transposed ldmatrix
-      uint32_t pa[MT][4];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        pa[mt][0] = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
-        pa[mt][1] = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
-        pa[mt][2] = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
-        pa[mt][3] = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
-      }
-      const uint32_t vrow = vbase + (uint32_t)((warp * 16 + 8 * ((lane >> 3) & 1) + (lane & 7)) * KP +
-                                               8 * (lane >> 4)) * 2;
-#pragma unroll
-      for (int n2 = 0; n2 < NT / 2; ++n2) {
-        uint32_t v0, v1, v2, v3;   // keys 16w + {0..7, 8..15} x dims 16*n2 + {0..7, 8..15}
-        ldsm_x4_t(vrow + (uint32_t)(n2 * 16 * 2), v0, v1, v2, v3);
+        // P.V: A = P (queries x this warp's 16 keys), B = V^T via transposed ldmatrix
+        uint32_t pa[MT][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          mma_bf16(acc[mt][2 * n2], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v0, v1);
-          mma_bf16(acc[mt][2 * n2 + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v2, v3);
+          pa[mt][0] = pack_bf16(sc[mt][0][0], sc[mt][0][1]);
+          pa[mt][1] = pack_bf16(sc[mt][0][2], sc[mt][0][3]);
+          pa[mt][2] = pack_bf16(sc[mt][1][0], sc[mt][1][1]);
+          pa[mt][3] = pack_bf16(sc[mt][1][2], sc[mt][1][3]);
         }
+        const uint32_t vrow = vbase + (uint32_t)((warp * 16 + 8 * ((lane >> 3) & 1) + (lane & 7)) * KP +
+                                                 8 * (lane >> 4)) * 2;
+#pragma unroll
+        for (int n2 = 0; n2 < NT / 2; ++n2) {
+          uint32_t v0, v1, v2, v3;   // keys 16w + {0..7, 8..15} x dims 16*n2 + {0..7, 8..15}
+          ldsm_x4_t(vrow + (uint32_t)(n2 * 16 * 2), v0, v1, v2, v3);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            mma_bf16(acc[mt][2 * n2], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v0, v1);
+            mma_bf16(acc[mt][2 * n2 + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], v2, v3);
+          }
+        }
+        __syncthreads();     // this ring slot is refilled by the next iteration's copies
       }
-      __syncthreads();     // this ring slot is refilled by the next iteration's copies
-    }
-    if (!ok_all) break;
-    fills += (uint32_t)ntiles;
-    __syncthreads();
-    // merge the four warps: row sums over the quad, then max / rescale through shared memory
+      if (!ok_all) break;
+      fills += (uint32_t)ntiles;
+      __syncthreads();
+      // merge the four warps: row sums over the quad, then max / rescale through shared memory
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float l = lrun[mt][h];
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        if (tig == 0) {
-          sMw[warp][mt * 16 + grp + 8 * h] = mrun[mt][h];
-          sLw[warp][mt * 16 + grp + 8 * h] = l;
+        for (int h = 0; h < 2; ++h) {
+          float l = lrun[mt][h];
+          l += __shfl_xor_sync(0xffffffffu, l, 1);
+          l += __shfl_xor_sync(0xffffffffu, l, 2);
+          if (tig == 0) {
+            sMw[warp][mt * 16 + grp + 8 * h] = mrun[mt][h];
+            sLw[warp][mt * 16 + grp + 8 * h] = l;
+          }
         }
+      constexpr int RS = HD + 8;      // padded row of the merge buffer (fewer bank conflicts)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (rok[mt][h]) {
+            const int row = mt * 16 + grp + 8 * h;
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+              *reinterpret_cast<float2*>(red + ((size_t)warp * QM + row) * RS + n * 8 + 2 * tig) =
+                  make_float2(acc[mt][n][2 * h], acc[mt][n][2 * h + 1]);
+          }
+      __syncthreads();
+      for (int e = tid; e < nQ * HD; e += blockDim.x) {
+        const int qi = e / HD, d = e % HD;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, sMw[w][qi]);
+        float o = 0.f, L = 0.f;
+        if (M > -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const float f = exp2f(sMw[w][qi] - M);
+            o += red[((size_t)w * QM + qi) * RS + d] * f;
+            L += sLw[w][qi] * f;
+          }
+        }
+        const int q = q0 + qi;
+        const int m = b * ri.R + q / G, h = g * G + q % G;
+        const size_t base = ((size_t)m * nq + h) * nsplit + s;
+        opart[base * HD + d] = o;
+        // the combine kernel takes natural-log maxima of the scaled scores
+        if (d == 0) mlpart[base] = make_float2(M == -INFINITY ? -INFINITY : M * 0.69314718055994531f, L);
       }
-    constexpr int RS = HD + 8;      // padded row of the merge buffer (fewer bank conflicts)
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        if (rok[mt][h]) {
-          const int row = mt * 16 + grp + 8 * h;
-#pragma unroll
-          for (int n = 0; n < NT; ++n)
-            *reinterpret_cast<float2*>(red + ((size_t)warp * QM + row) * RS + n * 8 + 2 * tig) =
-                make_float2(acc[mt][n][2 * h], acc[mt][n][2 * h + 1]);
-        }
-    __syncthreads();
-    for (int e = tid; e < nQ * HD; e += blockDim.x) {
-      const int qi = e / HD, d = e % HD;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) M = fmaxf(M, sMw[w][qi]);
-      float o = 0.f, L = 0.f;
-      if (M > -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float f = exp2f(sMw[w][qi] - M);
-          o += red[((size_t)w * QM + qi) * RS + d] * f;
-          L += sLw[w][qi] * f;
-        }
-      }
-      const int q = q0 + qi;
-      const int m = b * ri.R + q / G, h = g * G + q % G;
-      const size_t base = ((size_t)m * nq + h) * nsplit + s;
-      opart[base * HD + d] = o;
-      // the combine kernel takes natural-log maxima of the scaled scores
-      if (d == 0) mlpart[base] = make_float2(M == -INFINITY ? -INFINITY : M * 0.69314718055994531f, L);
     }
     __syncthreads();     // red / sQ / sMw reused by the next item
+    if (work != nullptr) {
+      if (tid == 0) s_next = (int)gridDim.x + atomicAdd(work, 1);
+      __syncthreads();
+      item = s_next;
+    } else {
+      item += gridDim.x;
+    }
   }
   if (!ok_all && tid == 0) report(ws, SPEC_ERR_TIMEOUT, blockIdx.x, 0);
 }
@@ -1490,11 +1516,11 @@ void launch_epi_store(int dtype_out, const float* part, const SKPlan& p, int M, 
 }
 
 void launch_epi_qkv(const spec_model_desc& d, const float* part, const SKPlan& p, const spec_rows& rows,
-                    const float2* cs, void* qbuf, const spec_kv& kv, void* ws, cudaStream_t st) {
+                    const float2* cs, void* qbuf, const spec_kv& kv, int* work, void* ws, cudaStream_t st) {
   RowInfo ri = to_rowinfo(rows);
   const long long n = (long long)rows.M * (d.n_q_heads + 2 * d.n_kv_heads) * (d.head_dim / 2);
   DISPATCH_T(d.dtype, launch_pdl(epi_qkv_kernel<T>, dim3(blocks_for(n, 256)), dim3(256), 0, st, 
-                          part, p, ri, d.n_q_heads, d.n_kv_heads, d.head_dim, cs, (T*)qbuf, kv, ws));
+                          part, p, ri, d.n_q_heads, d.n_kv_heads, d.head_dim, cs, (T*)qbuf, kv, work, ws));
 }
 
 void launch_epi_oproj(const spec_model_desc& d, const float* part, const SKPlan& p, const spec_rows& rows,
@@ -1597,7 +1623,7 @@ static spec_status attn_launch(const spec_model_desc& d, const RowInfo& ri, cons
 template <int HDV, int MT>
 static spec_status attn_mma_launch(const spec_model_desc& d, const RowInfo& ri, const spec_rows& rows,
                                    const void* qbuf, const spec_kv& kv, float* opart, float2* mlpart, void* attn_out,
-                                   int nsplit, int nqg, void* ws, cudaStream_t st) {
+                                   int nsplit, int nqg, int* work, void* ws, cudaStream_t st) {
   static int attr_dev = -1, occ = 1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1613,7 +1639,7 @@ static spec_status attn_mma_launch(const spec_model_desc& d, const RowInfo& ri, 
   const int grid = std::min(n_items, occ * sm_count());
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)d.head_dim);
   launch_pdl(kern, dim3(grid), dim3(128), smem, st, (const __nv_bfloat16*)qbuf, kv, ri, d.n_q_heads, d.n_kv_heads,
-             d.window, nsplit, nqg, n_items, scale_log2, opart, mlpart, ws);
+             d.window, nsplit, nqg, n_items, scale_log2, opart, mlpart, n_items > grid ? work : nullptr, ws);
   launch_pdl(attn_combine_kernel<__nv_bfloat16, HDV>, dim3(rows.M * d.n_q_heads), dim3(HDV), 0, st, opart, mlpart,
              d.n_q_heads, nsplit, (__nv_bfloat16*)attn_out);
   return SPEC_OK;
@@ -1632,7 +1658,8 @@ static spec_status attn_qdispatch(int qmax, const spec_model_desc& d, const RowI
 }
 
 spec_status launch_attention(const spec_model_desc& d, const spec_rows& rows, const void* qbuf, const spec_kv& kv,
-                             float* opart, float2* mlpart, void* attn_out, int nsplit, void* ws, cudaStream_t st) {
+                             float* opart, float2* mlpart, void* attn_out, int nsplit, int* work, void* ws,
+                             cudaStream_t st) {
   RowInfo ri = to_rowinfo(rows);
   const int G = d.n_q_heads / d.n_kv_heads;
   const int qmax = attn_qmax(rows.rows_per_req, G);
@@ -1642,11 +1669,11 @@ spec_status launch_attention(const spec_model_desc& d, const spec_rows& rows, co
     // tensor-core path: 16 or 32 query rows per item (the same groups as qmax <= 16 / 32)
     const bool two = qmax > 16;
     if (d.head_dim == 128)
-      s = two ? attn_mma_launch<128, 2>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st)
-              : attn_mma_launch<128, 1>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st);
+      s = two ? attn_mma_launch<128, 2>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st)
+              : attn_mma_launch<128, 1>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st);
     else if (d.head_dim == 64)
-      s = two ? attn_mma_launch<64, 2>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st)
-              : attn_mma_launch<64, 1>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, ws, st);
+      s = two ? attn_mma_launch<64, 2>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st)
+              : attn_mma_launch<64, 1>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st);
     else
       return SPEC_ERR_UNSUPPORTED;
   } else {
