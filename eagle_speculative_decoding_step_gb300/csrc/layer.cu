@@ -987,6 +987,418 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
   if (!ok_all && tid == 0) report(ws, SPEC_ERR_TIMEOUT, blockIdx.x, 0);
 }
 
+// ---------------------------------------------------------------- warp-specialised attention (bf16, TMA)
+// The same work items and partial results as attn_mma_kernel (up to 16 queries
+// of one request and kv head, one split of its keys), for caches whose block
+// size is a multiple of 8.  A split's keys are the cache indices [klo, ctx+nd)
+// cut into 64-key tiles aligned to multiples of 64; warp 4 produces, warps 0-3
+// consume:
+//  * the producer claims items, reads each tile's block-table entries and loads
+//    K and V by 3-D tensor copies (head dim x kv head x slot; one box is one
+//    8- or 16-slot run of a cache block and one 64-column half of the head, 128-B
+//    swizzled) and, with an item's first tile, its query rows, all completing on
+//    the ring slot's "full" barrier; runs without a valid key are not loaded;
+//  * consumer warp w owns keys 16w .. 16w+15 of every tile (scores and P.V as
+//    m16n8k16 bf16 MMAs with an online softmax, as in attn_mma_kernel), skips a
+//    tile none of whose keys is valid, zeroes the V rows of its invalid keys
+//    when some are valid (masked keys then add exact zeros), and releases the
+//    slot with one arrive per warp on its "empty" barrier;
+//  * after an item's last tile the four warps merge through that tile's slot.
+// No CTA-wide barrier runs per tile or per item; every wait is bounded.
+struct AttnTileMeta {
+  int b, g, q0, nQ, s, ctx, ci0, flags;
+  unsigned long long valid;         // bit k: key ci0 + k is attended to by some query row
+};
+constexpr int kTileFirst = 1, kTileLast = 2, kTileEnd = 4, kTileQBuf = 8;
+
+template <int HD> struct WsShape {
+  static constexpr int TK = 64, QM = 16, NS = 2, NH = HD / 64, KP = HD + 8;
+  static constexpr int HALF = TK * 128;                  // 64 keys x one 64-column half, 128-B rows
+  static constexpr int KVB = NH * HALF;                  // a K (or V) tile
+  static constexpr int STG = 2 * KVB;
+  static constexpr size_t kQ = (size_t)NS * STG;                      // [2][QM][KP] bf16 queries
+  static constexpr size_t kMeta = kQ + (size_t)2 * QM * KP * 2;      // [NS] AttnTileMeta
+  static constexpr size_t kLo = kMeta + (size_t)NS * 64;             // [2][QM] int
+  static constexpr size_t kMask = kLo + (size_t)2 * QM * 4;          // [2][QM] u64
+  static constexpr size_t kMw = kMask + (size_t)2 * QM * 8;          // [4][QM] float, then [4][QM] float
+  static constexpr size_t kBar = kMw + (size_t)2 * 4 * QM * 4;       // full[NS], empty[NS], merge
+  static constexpr size_t kMisc = kBar + (size_t)(2 * NS + 1) * 8;   // abort, consumed[4], issued
+  static constexpr size_t kBytes = kMisc + 32;
+  static constexpr size_t kSmem = kBytes + 1024;                     // + alignment of the ring to 1024 B
+  static_assert((size_t)4 * QM * HD * 4 <= (size_t)STG, "the merge reuses one ring slot");
+};
+
+SPEC_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x, int y, int z, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+template <int HD>
+__global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                         const __grid_constant__ CUtensorMap tmv,
+                                                         const __nv_bfloat16* __restrict__ qbuf, spec_kv kv,
+                                                         RowInfo ri, int nq, int nkv, int window, int nsplit,
+                                                         int nqg, int n_items, int bh, float scale_log2,
+                                                         float* __restrict__ opart, float2* __restrict__ mlpart,
+                                                         int* __restrict__ work, void* ws) {
+  pdl_wait();
+  pdl_trigger();
+  using S = WsShape<HD>;
+  constexpr int TK = S::TK, QM = S::QM, NS = S::NS, NH = S::NH, KP = S::KP, NT = HD / 8, KS = HD / 16;
+  extern __shared__ __align__(1024) uint8_t wsm_raw[];
+  uint8_t* sm = wsm_raw + ((1024u - (smem_u32(wsm_raw) & 1023u)) & 1023u);
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(sm + S::kQ);
+  AttnTileMeta* meta = reinterpret_cast<AttnTileMeta*>(sm + S::kMeta);
+  int* s_lo = reinterpret_cast<int*>(sm + S::kLo);
+  unsigned long long* s_mask = reinterpret_cast<unsigned long long*>(sm + S::kMask);
+  float* sMw = reinterpret_cast<float*>(sm + S::kMw);
+  float* sLw = sMw + 4 * QM;
+  const uint32_t full0 = smem_u32(sm + S::kBar), empty0 = full0 + 8u * NS, mbar = full0 + 16u * NS;
+  int* misc = reinterpret_cast<int*>(sm + S::kMisc);
+  volatile int* abort = misc;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = nq / nkv;
+  const int nQall = ri.R * G;
+  if (tid == 0) {
+    misc[0] = 0;
+    for (int i = 0; i < NS; ++i) {
+      tc::mbar_init(full0 + 8u * i, 1);      // the producer's arrive (+ the copies' bytes)
+      tc::mbar_init(empty0 + 8u * i, 4);     // one arrive per consumer warp
+    }
+    tc::mbar_init(mbar, 4);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    uint32_t fill = 0;
+    int qbuf_sel = 0;
+    int it = blockIdx.x;
+    bool ok = true;
+    const int ng = TK / bh;                    // block-table runs per tile
+    while (ok && it < n_items) {
+      int nxt = it;
+      if (lane == 0) nxt = work != nullptr ? (int)gridDim.x + atomicAdd(work, 1) : it + (int)gridDim.x;
+      const int s = it % nsplit;
+      const int g = (it / nsplit) % nkv;
+      const int bq = it / (nsplit * nkv);
+      const int b = bq / nqg, q0 = (bq % nqg) * QM;
+      const int nQ = min(QM, nQall - q0);
+      const int ctx = ri.ctx_len[b];
+      int lo = 0x7fffffff;
+      unsigned long long mk = 0;
+      if (lane < nQ) {
+        const int m = b * ri.R + (q0 + lane) / G;
+        const int pos = row_pos(ri, m);
+        lo = window > 0 ? max(0, pos - window + 1) : 0;
+        if (lo > ctx) lo = ctx;
+        mk = row_mask(ri, m);
+      }
+      int klo = lo;
+      unsigned long long om = mk;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        klo = min(klo, __shfl_xor_sync(0xffffffffu, klo, o));
+        om |= __shfl_xor_sync(0xffffffffu, om, o);
+      }
+      const int kend = ctx + (om ? 64 - __clzll((long long)om) : 0);   // keys: cache indices [klo, kend)
+      const int cb = klo & ~(TK - 1);
+      const int T = kend > klo ? (kend - cb + TK - 1) / TK : 0;
+      const int ct = (T + nsplit - 1) / nsplit;
+      const int t0 = s * ct;
+      const int ntiles = max(0, min(T, t0 + ct) - t0);
+      if (ntiles == 0) {
+        // an empty split: its partials say "no keys"
+        for (int e = lane; e < nQ * HD; e += 32) {
+          const int qi = e / HD, d = e % HD;
+          const int q = q0 + qi;
+          const size_t base = ((size_t)(b * ri.R + q / G) * nq + g * G + q % G) * nsplit + s;
+          opart[base * HD + d] = 0.f;
+          if (d == 0) mlpart[base] = make_float2(-INFINITY, 0.f);
+        }
+      } else {
+        // the item's row constants and queries go to buffer qbuf_sel: its previous
+        // user finished at least two fills ago (every item has a tile), and the wait
+        // for this item's first slot covers those
+        for (int j = 0; j < ntiles; ++j) {
+          const int slot = (int)(fill % NS);
+          const int ci0 = cb + (t0 + j) * TK;
+          int ent = -1;                        // lane r < ng: block-table entry of run r
+          if (lane < ng) {
+            const int ci = ci0 + lane * bh;
+            const int blk = ci / kv.block_size;
+            if (ci < kend && blk < kv.max_blocks) ent = kv.block_table[(size_t)b * kv.max_blocks + blk];
+          }
+          if (fill >= (uint32_t)NS) {
+            const bool w = tc::mbar_wait(empty0 + 8u * slot, ((fill / NS) - 1u) & 1u, abort);
+            if (__any_sync(0xffffffffu, !w)) { ok = false; break; }
+          }
+          unsigned long long valid = 0;
+#pragma unroll
+          for (int hk = 0; hk < 2; ++hk) {
+            const int kt = lane + 32 * hk;
+            const int ci = ci0 + kt;
+            const int e = __shfl_sync(0xffffffffu, ent, kt / bh);
+            bool v = ci >= klo && ci < kend && e >= 0;
+            if (v) v = (long long)e * kv.block_size + ci % kv.block_size < (long long)kv.num_slots;
+            valid |= (unsigned long long)__ballot_sync(0xffffffffu, v) << (32 * hk);
+          }
+          // lane -> one box: run r = lane / (2 NH), K or V, column half
+          const int r = lane / (2 * NH), isv = (lane / NH) & 1, hh = lane % NH;
+          const unsigned long long rmask = bh == 16 ? 0xffffull : 0xffull;
+          const int er = __shfl_sync(0xffffffffu, ent, r < ng ? r : 0);
+          const bool box = r < ng && ((valid >> (r * bh)) & rmask) != 0;
+          const uint32_t nbox = __popc(__ballot_sync(0xffffffffu, box));
+          uint32_t bytes = nbox * (uint32_t)(bh * 128);
+          if (j == 0) bytes += (uint32_t)(nQ * HD * 2);
+          if (j == 0 && lane < QM) {
+            s_lo[qbuf_sel * QM + lane] = lo;
+            s_mask[qbuf_sel * QM + lane] = mk;
+          }
+          if (lane == 0) {
+            AttnTileMeta mt;
+            mt.b = b; mt.g = g; mt.q0 = q0; mt.nQ = nQ; mt.s = s; mt.ctx = ctx; mt.ci0 = ci0;
+            mt.flags = (j == 0 ? kTileFirst : 0) | (j == ntiles - 1 ? kTileLast : 0) | (qbuf_sel ? kTileQBuf : 0);
+            mt.valid = valid;
+            meta[slot] = mt;
+          }
+          __syncwarp();
+          if (lane == 0) tc::mbar_expect_tx(full0 + 8u * slot, bytes);
+          __syncwarp();
+          const uint32_t bar = full0 + 8u * slot;
+          if (box) {
+            const int ci = ci0 + r * bh;
+            const int slot0 = er * kv.block_size + ci % kv.block_size;
+            const uint32_t dst = smem_u32(sm + (size_t)slot * S::STG + (size_t)isv * S::KVB + (size_t)hh * S::HALF +
+                                          (size_t)r * bh * 128);
+            tma_load_3d(dst, isv ? &tmv : &tmk, bar, hh * 64, g, slot0, pol);
+          }
+          if (j == 0 && lane < nQ) {
+            const int q = q0 + lane;
+            const __nv_bfloat16* src = qbuf + ((size_t)(b * ri.R + q / G) * nq + g * G + q % G) * HD;
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                ::"r"(smem_u32(sQ + ((size_t)qbuf_sel * QM + lane) * KP)), "l"(src), "r"(HD * 2), "r"(bar)
+                : "memory");
+          }
+          ++fill;
+        }
+        qbuf_sel ^= 1;
+      }
+      it = __shfl_sync(0xffffffffu, nxt, 0);
+    }
+    // end of the sequence: one more slot, without copies
+    if (ok) {
+      const int slot = (int)(fill % NS);
+      bool w = true;
+      if (fill >= (uint32_t)NS) w = tc::mbar_wait(empty0 + 8u * slot, ((fill / NS) - 1u) & 1u, abort);
+      if (!__any_sync(0xffffffffu, !w) && lane == 0) {
+        meta[slot].flags = kTileEnd;
+        tc::mbar_arrive(full0 + 8u * slot);
+      }
+    }
+    if (lane == 0) misc[5] = (int)fill;
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int grp = lane >> 2, tig = lane & 3;
+    uint32_t fill = 0, mph = 0;
+    float acc[NT][4];
+    float mrun[2], lrun[2];
+    int rlo[2], nQ = 0, qsel = 0;
+    unsigned long long rmask[2];
+    bool rok[2];
+    // this lane's ldmatrix rows: K (scores' "col" operand) and V (transposed)
+    const int key_k = warp * 16 + 8 * (lane >> 4) + (lane & 7), sel_k = (lane >> 3) & 1;
+    const int key_v = warp * 16 + 8 * ((lane >> 3) & 1) + (lane & 7), sel_v = lane >> 4;
+    const uint32_t x7 = (uint32_t)(lane & 7);
+    for (;; ++fill) {
+      const int slot = (int)(fill % NS);
+      if (!tc::mbar_wait(full0 + 8u * slot, (fill / NS) & 1u, abort)) break;
+      const AttnTileMeta mt = meta[slot];
+      if (mt.flags & kTileEnd) break;
+      if (mt.flags & kTileFirst) {
+        nQ = mt.nQ;
+        qsel = (mt.flags & kTileQBuf) ? 1 : 0;
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          mrun[h] = -INFINITY;
+          lrun[h] = 0.f;
+          const int qi = grp + 8 * h;
+          rok[h] = qi < nQ;
+          rlo[h] = s_lo[qsel * QM + qi];
+          rmask[h] = s_mask[qsel * QM + qi];
+        }
+      }
+      uint8_t* st = sm + (size_t)slot * S::STG;
+      const uint32_t vm = (uint32_t)(mt.valid >> (16 * warp)) & 0xffffu;
+      bool wrote = false;
+      if (vm != 0) {
+        if (vm != 0xffffu) {
+          // V rows of this warp's invalid keys: zeros (stale or unloaded rows may hold anything)
+          for (int e = lane; e < 16 * NH * 8; e += 32) {
+            const int kr = e / (NH * 8), c = e % (NH * 8);
+            if (!((vm >> kr) & 1u)) {
+              const int key = warp * 16 + kr;
+              *reinterpret_cast<uint4*>(st + S::KVB + (size_t)(c >> 3) * S::HALF + (size_t)key * 128 + (c & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+          }
+          wrote = true;
+          __syncwarp();
+        }
+        const uint32_t kst = smem_u32(st), vst = kst + S::KVB;
+        const uint32_t qb = smem_u32(sQ + (size_t)qsel * QM * KP);
+        const uint32_t qrow = qb + (uint32_t)((8 * ((lane >> 3) & 1) + (lane & 7)) * KP + 8 * (lane >> 4)) * 2;
+        float sc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t b0, b1, b2, b3;   // keys 16w + {0..7, 8..15} x dims ks*16 + {0..7, 8..15}
+          const uint32_t c = (uint32_t)(((ks & 3) << 1) | sel_k);
+          ldsm_x4(kst + (uint32_t)((ks >> 2) * S::HALF + key_k * 128) + ((c ^ x7) << 4), b0, b1, b2, b3);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(qrow + (uint32_t)(ks * 16 * 2), a0, a1, a2, a3);
+          mma_bf16(sc[0], a0, a1, a2, a3, b0, b1);
+          mma_bf16(sc[1], a0, a1, a2, a3, b2, b3);
+        }
+        // mask, scale to log2 units, warp-local online softmax
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (8 * h >= nQ) continue;     // rows of absent queries only (uniform in the warp)
+          float mx = -INFINITY;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int kr = nt * 8 + 2 * tig + e;
+              const int ci = mt.ci0 + warp * 16 + kr;
+              bool ok = rok[h] && ((vm >> kr) & 1u);
+              if (ok) ok = ci < mt.ctx ? ci >= rlo[h] : ((rmask[h] >> (ci - mt.ctx)) & 1ull) != 0;
+              const float v = ok ? sc[nt][2 * h + e] * scale_log2 : -INFINITY;
+              sc[nt][2 * h + e] = v;
+              mx = fmaxf(mx, v);
+            }
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const float mnew = fmaxf(mrun[h], mx);
+          const float al = mnew == -INFINITY ? 1.f : exp2f(mrun[h] - mnew);
+          float ps = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float p = mnew == -INFINITY ? 0.f : exp2f(sc[nt][2 * h + e] - mnew);
+              sc[nt][2 * h + e] = p;
+              ps += p;
+            }
+          lrun[h] = lrun[h] * al + ps;
+          mrun[h] = mnew;
+          if (al != 1.f) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              acc[n][2 * h] *= al;
+              acc[n][2 * h + 1] *= al;
+            }
+          }
+        }
+        const uint32_t pa0 = pack_bf16(sc[0][0], sc[0][1]), pa1 = pack_bf16(sc[0][2], sc[0][3]);
+        const uint32_t pa2 = pack_bf16(sc[1][0], sc[1][1]), pa3 = pack_bf16(sc[1][2], sc[1][3]);
+#pragma unroll
+        for (int n2 = 0; n2 < NT / 2; ++n2) {
+          uint32_t v0, v1, v2, v3;   // keys 16w + {0..7, 8..15} x dims 16*n2 + {0..7, 8..15}
+          const uint32_t c = (uint32_t)(((n2 & 3) << 1) | sel_v);
+          ldsm_x4_t(vst + (uint32_t)((n2 >> 2) * S::HALF + key_v * 128) + ((c ^ x7) << 4), v0, v1, v2, v3);
+          mma_bf16(acc[2 * n2], pa0, pa1, pa2, pa3, v0, v1);
+          mma_bf16(acc[2 * n2 + 1], pa0, pa1, pa2, pa3, v2, v3);
+        }
+      }
+      if (mt.flags & kTileLast) {
+        // merge the four warps through this slot (every warp is done with its K and V)
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(mbar);
+        bool okm = tc::mbar_wait(mbar, mph, abort);
+        mph ^= 1u;
+        if (!okm) break;
+        float* red = reinterpret_cast<float*>(st);     // [4][QM][HD], 8-float blocks swizzled by row
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float l = lrun[h];
+          l += __shfl_xor_sync(0xffffffffu, l, 1);
+          l += __shfl_xor_sync(0xffffffffu, l, 2);
+          const int row = grp + 8 * h;
+          if (tig == 0) {
+            sMw[warp * QM + row] = mrun[h];
+            sLw[warp * QM + row] = l;
+          }
+          if (rok[h]) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+              *reinterpret_cast<float2*>(red + ((size_t)warp * QM + row) * HD + ((n ^ (row & 7)) << 3) + 2 * tig) =
+                  make_float2(acc[n][2 * h], acc[n][2 * h + 1]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(mbar);
+        okm = tc::mbar_wait(mbar, mph, abort);
+        mph ^= 1u;
+        if (!okm) break;
+        for (int e = tid; e < nQ * HD; e += 128) {
+          const int qi = e / HD, d = e % HD;
+          const int col = (((d >> 3) ^ (qi & 7)) << 3) + (d & 7);
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) M = fmaxf(M, sMw[w * QM + qi]);
+          float o = 0.f, L = 0.f;
+          if (M > -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const float f = exp2f(sMw[w * QM + qi] - M);
+              o += red[((size_t)w * QM + qi) * HD + col] * f;
+              L += sLw[w * QM + qi] * f;
+            }
+          }
+          const int q = mt.q0 + qi;
+          const size_t base = ((size_t)(mt.b * ri.R + q / G) * nq + mt.g * G + q % G) * nsplit + mt.s;
+          opart[base * HD + d] = o;
+          // the combine kernel takes natural-log maxima of the scaled scores
+          if (d == 0) mlpart[base] = make_float2(M == -INFINITY ? -INFINITY : M * 0.69314718055994531f, L);
+        }
+        wrote = true;
+      }
+      // generic writes to the slot come before the copy engine's next fill of it
+      if (wrote) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(empty0 + 8u * slot);
+    }
+    if (lane == 0) misc[1 + warp] = (int)fill;
+  }
+  __syncthreads();
+  if (*abort) {
+    // let the copies still in flight land before the CTA's shared memory goes away
+    if (tid == 0) {
+      int c = misc[1];
+      for (int w = 2; w <= 4; ++w) c = min(c, misc[w]);
+      for (uint32_t f = (uint32_t)c; f < (uint32_t)misc[5]; ++f)
+        tc::mbar_wait(full0 + 8u * (f % NS), (f / NS) & 1u, abort, false);
+      report(ws, SPEC_ERR_TIMEOUT, blockIdx.x, 0);
+    }
+  }
+}
+
 template <typename T, int HD>
 __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restrict__ opart,
                                                           const float2* __restrict__ mlpart, int nq, int nsplit,
@@ -1645,6 +2057,61 @@ static spec_status attn_mma_launch(const spec_model_desc& d, const RowInfo& ri, 
   return SPEC_OK;
 }
 
+// K / V tensor maps of a cache, reused while the cache and its shape stay the same
+static bool kv_maps(const spec_kv& kv, int nkv, int hd, int bh, CUtensorMap* tk, CUtensorMap* tv) {
+  struct Entry {
+    const void* k;
+    const void* v;
+    int slots, nkv, hd, bh, dev;
+    CUtensorMap mk, mv;
+  };
+  static Entry e{};
+  static bool have = false;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!have || e.k != kv.k || e.v != kv.v || e.slots != kv.num_slots || e.nkv != nkv || e.hd != hd || e.bh != bh ||
+      e.dev != dev) {
+    have = false;
+    if (!tc::make_kv_map(&e.mk, kv.k, kv.num_slots, nkv, hd, bh) ||
+        !tc::make_kv_map(&e.mv, kv.v, kv.num_slots, nkv, hd, bh))
+      return false;
+    e.k = kv.k; e.v = kv.v; e.slots = kv.num_slots; e.nkv = nkv; e.hd = hd; e.bh = bh; e.dev = dev;
+    have = true;
+  }
+  *tk = e.mk;
+  *tv = e.mv;
+  return true;
+}
+
+template <int HDV>
+static spec_status attn_ws_launch(const spec_model_desc& d, const RowInfo& ri, const spec_rows& rows,
+                                  const void* qbuf, const spec_kv& kv, float* opart, float2* mlpart, void* attn_out,
+                                  int nsplit, int nqg, int* work, void* ws, cudaStream_t st) {
+  static int attr_dev = -1, occ = 1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  constexpr size_t smem = WsShape<HDV>::kSmem;
+  auto kern = attn_ws_kernel<HDV>;
+  if (attr_dev != dev) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 160, smem) != cudaSuccess || occ < 1) occ = 1;
+    attr_dev = dev;
+  }
+  const int bh = kv.block_size % 16 == 0 ? 16 : 8;
+  CUtensorMap tk, tv;
+  if (!kv_maps(kv, d.n_kv_heads, HDV, bh, &tk, &tv)) return SPEC_ERR_CUDA;
+  const int n_items = nsplit * d.n_kv_heads * rows.B * nqg;
+  const int grid = std::min(n_items, occ * sm_count());
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)d.head_dim);
+  launch_pdl(kern, dim3(grid), dim3(160), smem, st, tk, tv, (const __nv_bfloat16*)qbuf, kv, ri, d.n_q_heads,
+             d.n_kv_heads, d.window, nsplit, nqg, n_items, bh, scale_log2, opart, mlpart,
+             n_items > grid ? work : nullptr, ws);
+  launch_pdl(attn_combine_kernel<__nv_bfloat16, HDV>, dim3(rows.M * d.n_q_heads), dim3(HDV), 0, st, opart, mlpart,
+             d.n_q_heads, nsplit, (__nv_bfloat16*)attn_out);
+  return SPEC_OK;
+}
+
 template <typename TT, int HDV>
 static spec_status attn_qdispatch(int qmax, const spec_model_desc& d, const RowInfo& ri, const spec_rows& rows,
                                   const void* qbuf, const spec_kv& kv, float* opart, float2* mlpart, void* out,
@@ -1668,6 +2135,14 @@ spec_status launch_attention(const spec_model_desc& d, const spec_rows& rows, co
   if (d.dtype == SPEC_DTYPE_BF16) {
     // tensor-core path: 16 or 32 query rows per item (the same groups as qmax <= 16 / 32)
     const bool two = qmax > 16;
+    // warp-specialised kernel with tensor copies: one m-tile, cache blocks of a multiple of 8 slots,
+    // 16-byte aligned caches
+    const bool tma = !two && kv.block_size % 8 == 0 && ((reinterpret_cast<uintptr_t>(kv.k) |
+                                                          reinterpret_cast<uintptr_t>(kv.v)) & 15u) == 0;
+    if (tma && d.head_dim == 128)
+      return attn_ws_launch<128>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st);
+    if (tma && d.head_dim == 64)
+      return attn_ws_launch<64>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st);
     if (d.head_dim == 128)
       s = two ? attn_mma_launch<128, 2>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st)
               : attn_mma_launch<128, 1>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st);

@@ -41,6 +41,9 @@ template <int MPAD, int EXTRA = 0> struct Cfg {
   static constexpr size_t kSmem = (size_t)kStages * kStage + 1024 + 256 + EXTRA;
 };
 
+// 3-D tensor map of a bf16 paged K or V cache [slots][nkv][hd] (defined in tc_gemm.cu)
+bool make_kv_map(CUtensorMap* tm, const void* ptr, int slots, int nkv, int hd, int box_keys);
+
 SPEC_DEV uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 SPEC_DEV void mbar_init(uint32_t a, uint32_t n) {

@@ -57,6 +57,20 @@ bool make_map(CUtensorMap* tm, const void* ptr, int rows, int cols, int box_rows
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 paged cache [slots][nkv][hd]: box 64 columns x 1 head x box_keys slots, 128-byte swizzle
+// (rows past the last slot read as zeros).
+bool make_kv_map(CUtensorMap* tm, const void* ptr, int slots, int nkv, int hd, int box_keys) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)nkv, (cuuint64_t)slots};
+  cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)nkv * hd * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_keys};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int MPAD>
 static spec_status launch_mpad(const CUtensorMap* a, const CUtensorMap& b, const SKPlan& p, int M, float* part,
                                void* ws, cudaStream_t st) {
