@@ -76,6 +76,33 @@ def test_draft_layer_long_context(w, step):
     no_device_error(dm)
 
 
+BLOCK_CASES = [
+    replace(LONG_RAGGED, name="block8", block_size=8, B=8, seed=31),            # 8-slot runs
+    replace(LONG_RAGGED, name="block24", block_size=24, B=8, seed=32),          # runs inside 24-slot blocks
+    replace(LONG_RAGGED, name="block12", block_size=12, B=8, seed=33),          # per-row copies
+    replace(LONG_WINDOW, name="block64_window", block_size=64, B=4, ctx=3000, seed=34),
+    replace(SMALL_BF16, name="block8_hd64", block_size=8, ctx_range=(40, 300), seed=35),
+]
+
+
+@pytest.mark.parametrize("w", BLOCK_CASES, ids=lambda w: w.name)
+def test_draft_layer_block_sizes(w):
+    """Cache block sizes of 8, 24, 12 and 64 slots: the tensor-copy attention loads
+    8- or 16-slot runs of a block (12 takes the per-row copy kernel), with ragged
+    contexts or a sliding window, head dims 128 and 64."""
+    W, ctx, kv, dm = setup(w)
+    hid = synth.make_hidden(w, w.B)
+    tok = synth.integers(w.seed, 1, 0, w.V, w.B)
+    rows = {"M": w.B, "B": w.B, "R": 1, "step": 2, "ctx_len": ctx, "tok": tok}
+    ref_pre, ref_hn = od.draft_layer(w, W, rows, hid, kv)
+    pre, hn = dm.hidden(w.B), dm.hidden(w.B)
+    r = lib.make_rows(w.B, w.B, 1, dm.ctx_len, dev(tok), step=2, max_ctx=int(ctx.max()))
+    lib.spec_draft_layer(dm.desc, dm.weights, r, dev_act(hid, w), pre, hn, dm.kv, dm.ws)
+    assert_close(host(pre), ref_pre, w, "hidden_prenorm")
+    assert_close(host(hn), ref_hn, w, "hidden_normed")
+    no_device_error(dm)
+
+
 @pytest.mark.parametrize("w", [SMALL_BF16, replace(SMALL_BF16_HD128, window=64, ctx=150)], ids=lambda w: w.name)
 def test_draft_layer_tree_rows(w):
     """Frontier-style rows: several rows per request, explicit positions, draft-region
