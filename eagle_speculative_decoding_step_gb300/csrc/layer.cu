@@ -1481,13 +1481,15 @@ SPEC_DEV uint32_t order_key(float f) {
 //  1. every thread takes the largest key among its elements; the Kc-th largest
 //     of its CTA's 1024 maxima is a lower bound of the row's Kc-th largest key
 //     (the Kc largest maxima are Kc distinct elements at least that large), and
-//     so is the largest of the cluster's bounds, T0 (exchanged in distributed
-//     shared memory);
+//     so is the lower edge of its 16-bit bucket and the largest of the cluster's
+//     bounds, T0 (exchanged in distributed shared memory);
 //  2. a second pass copies the CTA's elements >= T0 -- a few hundred in the
 //     whole row -- to its shared memory;
-//  3. rank 0 gathers the copies, an exact radix selection gives the Kc-th key
-//     and how many elements equal to it are taken (smallest ids first), and a
-//     bitonic sort orders the Kc selected.
+//  3. rank 0 gathers the copies, one per thread, and each copy's rank among them
+//     (larger key first, then smaller id) is its place in the output.  With more
+//     copies than threads an exact radix selection gives the Kc-th key and how
+//     many elements equal to it are taken (smallest ids first), and a bitonic
+//     sort orders the Kc selected.
 // Both passes over the row are plain streaming reads (16-byte loads, one
 // shared-counter update per warp and round).  If more elements pass step 2
 // than shared memory takes (long runs of equal values), rank 0 selects with
@@ -1527,12 +1529,14 @@ SPEC_DEV int block_excl_scan(int v, int* wsum, int* total) {
 // need-th largest, digit by digit (8 bits) from the top, and in *tie_need how
 // many elements equal to it belong to the need largest.  Lanes of a warp that
 // fall in the same digit add to the histogram once; warp 0 finds the digit.
+// With fewer than four rounds the result is the lower edge of the need-th
+// largest key's bucket (its top 8 * rounds bits): at least `need` keys are >= it.
 template <bool SMEM_KEYS>
 SPEC_DEV uint32_t radix_select(const float* x, const uint32_t* keys, int n, int need, int* hist, uint32_t* s_prefix,
-                               int* s_need, int* tie_need) {
+                               int* s_need, int* tie_need, int rounds = 4) {
   const int tid = threadIdx.x, lane = tid & 31;
   if (tid == 0) { *s_prefix = 0u; *s_need = need; }
-  for (int lo = 24; lo >= 0; lo -= 8) {
+  for (int lo = 24; lo >= 32 - 8 * rounds; lo -= 8) {
     if (tid < 256) hist[tid] = 0;
     __syncthreads();
     const uint32_t pf = *s_prefix;
@@ -1670,7 +1674,9 @@ __global__ void __cluster_dims__(kTkCL, 1, 1) __launch_bounds__(1024)
   skey[tid] = tmax;           // 0 for a thread without elements: below every key
   __syncthreads();
   int tie_need;
-  const uint32_t tb = radix_select<true>(nullptr, skey, blockDim.x, Kc, hist, &s_prefix, &s_need, &tie_need);
+  // the bound needs no more than the top 16 bits: the lower edge of the Kc-th
+  // largest maximum's bucket still has Kc maxima at or above it
+  const uint32_t tb = radix_select<true>(nullptr, skey, blockDim.x, Kc, hist, &s_prefix, &s_need, &tie_need, 2);
   if (tid == 0) s_bound = tb;
   cl.sync();
   uint32_t t0 = 0;
@@ -1729,7 +1735,44 @@ __global__ void __cluster_dims__(kTkCL, 1, 1) __launch_bounds__(1024)
     }
     over = over || total > kTkCap;
     uint32_t kth;
-    if (!over) {
+    if (!over && total <= (int)blockDim.x) {
+      // 3. gather one copy per thread; its rank among the copies (larger key first,
+      // then smaller id) is its place in the output, and only the Kc first are kept
+      uint32_t k = 0;
+      int id = 0x7fffffff;
+      int off = 0;
+#pragma unroll
+      for (int r = 0; r < kTkCL; ++r) {
+        if (tid >= off && tid < off + cnt[r]) {
+          k = cl.map_shared_rank(ckey, r)[tid - off];
+          id = cl.map_shared_rank(cidx, r)[tid - off];
+        }
+        off += cnt[r];
+      }
+      // pad to a multiple of 8 with entries that never rank above a copy (key 0, id max)
+      const int tpad = (total + 7) & ~7;
+      if (tid < tpad) {
+        gkey[tid] = tid < total ? k : 0u;
+        gidx[tid] = tid < total ? id : 0x7fffffff;
+      }
+      __syncthreads();
+      if (tid < total) {
+        // four candidates per 16-byte load, two independent counts
+        const uint4* k4 = reinterpret_cast<const uint4*>(gkey);
+        const int4* i4 = reinterpret_cast<const int4*>(gidx);
+        int r0 = 0, r1 = 0;
+        for (int j = 0; j < tpad / 4; j += 2) {
+          const uint4 ka = k4[j], kb = k4[j + 1];
+          const int4 ia = i4[j], ib = i4[j + 1];
+          r0 += (ka.x > k || (ka.x == k && ia.x < id)) + (ka.y > k || (ka.y == k && ia.y < id)) +
+                (ka.z > k || (ka.z == k && ia.z < id)) + (ka.w > k || (ka.w == k && ia.w < id));
+          r1 += (kb.x > k || (kb.x == k && ib.x < id)) + (kb.y > k || (kb.y == k && ib.y < id)) +
+                (kb.z > k || (kb.z == k && ib.z < id)) + (kb.w > k || (kb.w == k && ib.w < id));
+        }
+        const int rnk = r0 + r1;
+        if (rnk < Kc) out_ids[(size_t)m * Kc + rnk] = id;
+      }
+    } else if (!over) {
       // 3. gather, select, sort
       int off = 0;
 #pragma unroll
@@ -1793,8 +1836,10 @@ __global__ void __cluster_dims__(kTkCL, 1, 1) __launch_bounds__(1024)
         __syncthreads();
       }
     }
-    __syncthreads();
-    sort_selected(skey, sidx, Kc, out_ids + (size_t)m * Kc);
+    if (over || total > (int)blockDim.x) {
+      __syncthreads();
+      sort_selected(skey, sidx, Kc, out_ids + (size_t)m * Kc);
+    }
   }
   cl.sync();                  // no CTA leaves while rank 0 may still read its copies
 }

@@ -164,9 +164,11 @@ def test_lm_head(w, k, M):
 LOWRANK = replace(SMALL_BF16, name="small_lowrank", rank=64, num_candidates=128, H=512, V=5000)
 
 
+@pytest.mark.parametrize("w", [LOWRANK, replace(LOWRANK, name="small_lowrank_v5024", V=5024, seed=42)],
+                         ids=lambda w: w.name)
 @pytest.mark.parametrize("M", [1, 5, 64])
-def test_lowrank_candidates(M):
-    w = LOWRANK
+def test_lowrank_candidates(M, w):
+    """Candidate head at 1, 5 and 64 rows, vocabularies of 5000 and 5024."""
     W, ctx, kv, dm = setup(w, max_rows=M)
     hn = synth.make_hidden(w, M, sub=6)
     cand_ref, exact_ref, out_ref = od.lowrank_candidates(w, W, hn, w.num_candidates, 2)
