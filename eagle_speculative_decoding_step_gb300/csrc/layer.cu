@@ -1421,13 +1421,21 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restric
   for (int s = 0; s < nsplit; ++s) M = fmaxf(M, sm_[s]);
   if (d < nsplit) sw[d] = (M > -INFINITY && sm_[d] > -INFINITY) ? expf(sm_[d] - M) : 0.f;
   __syncthreads();
-  float L = 0.f, o = 0.f;
+  float L = 0.f;
+  for (int s = 0; s < nsplit; ++s) L += sl_[s] * sw[s];
+  // sixteen splits' loads in flight per round, four partial sums
   const float* op = opart + (size_t)mh * nsplit * HD + d;
-#pragma unroll 4
-  for (int s = 0; s < nsplit; ++s) {
-    L += sl_[s] * sw[s];
-    o += op[(size_t)s * HD] * sw[s];
+  float o4[4] = {0.f, 0.f, 0.f, 0.f};
+  int s = 0;
+  for (; s + 16 <= nsplit; s += 16) {
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) v[u] = op[(size_t)(s + u) * HD];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) o4[u & 3] += v[u] * sw[s + u];
   }
+  for (; s < nsplit; ++s) o4[s & 3] += op[(size_t)s * HD] * sw[s];
+  const float o = (o4[0] + o4[1]) + (o4[2] + o4[3]);
   st(out + (size_t)mh * HD + d, L > 0.f ? o / L : 0.f);
 }
 
