@@ -137,14 +137,26 @@ def test_tree_full_size():
     torch.cuda.synchronize()
     assert dm.device_error() == 0
     tok, par = st.t_tok.cpu().numpy(), st.t_par.cpu().numpy()
-    if not (np.array_equal(tok, fin["tok"]) and np.array_equal(par, fin["parent"])):
+    if np.array_equal(tok, fin["tok"]) and np.array_equal(par, fin["parent"]):
+        np.testing.assert_array_equal(st.t_dep.cpu().numpy(), fin["depth"])
+        assert len(set(fin["parent"][0].tolist())) > 1
+    else:
+        # a score near-tie picked another (equally valid) tree: the oracle's target logits
+        # for the GPU's tree, so that its verification is still checked exactly
         assert tree_mismatch_is_near_tie(tok, par, fin, st.t_score.cpu().numpy()), \
             "tree differs away from any score near-tie"
-        pytest.skip("near-tie while drafting the tree")
-    np.testing.assert_array_equal(st.t_par.cpu().numpy(), fin["parent"])
-    np.testing.assert_array_equal(st.t_dep.cpu().numpy(), fin["depth"])
-    assert len(set(fin["parent"][0].tolist())) > 1
-    ref_out, ref_acc, _ = overify.verify_greedy_tree(target, fin["tok"], fin["parent"], w.depth)
+        mask = st.t_mask.cpu().numpy().view(np.uint64)
+        dep, pos = st.t_dep.cpu().numpy(), st.t_pos.cpu().numpy()
+        for b in range(w.B):       # the GPU's tree is a well-formed tree over its own nodes
+            assert par[b, 0] == -1 and dep[b, 0] == 0 and pos[b, 0] == ctx[b] and int(mask[b, 0]) == 1
+            for n in range(1, tok.shape[1]):
+                q = int(par[b, n])
+                assert 0 <= q < n and dep[b, n] == dep[b, q] + 1 and pos[b, n] == ctx[b] + dep[b, n]
+                assert int(mask[b, n]) == int(mask[b, q]) | (1 << n)
+        gpu_tree = {"tok": tok, "parent": par, "pos": pos, "mask": [[int(x) for x in row] for row in mask]}
+        target = ostep.tree_target(w, W64, aux, ctx, kv, gpu_tree, noise)
+        st.target.copy_(dev(target))
+    ref_out, ref_acc, _ = overify.verify_greedy_tree(target, tok, par, w.depth)
     st.verify(compact=False)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(st.out.cpu().numpy(), ref_out)

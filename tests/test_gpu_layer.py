@@ -103,11 +103,15 @@ def test_draft_layer_block_sizes(w):
     no_device_error(dm)
 
 
-@pytest.mark.parametrize("w", [SMALL_BF16, replace(SMALL_BF16_HD128, window=64, ctx=150)], ids=lambda w: w.name)
-def test_draft_layer_tree_rows(w):
+@pytest.mark.parametrize("w,k", [(SMALL_BF16, 4), (replace(SMALL_BF16_HD128, window=64, ctx=150), 4),
+                                 (replace(SMALL_BF16, name="small_bf16_k8"), 8),
+                                 (replace(SMALL_BF16, name="small_bf16_k8_block12", block_size=12), 8)],
+                         ids=["k4", "hd128_window_k4", "k8", "k8_block12"])
+def test_draft_layer_tree_rows(w, k):
     """Frontier-style rows: several rows per request, explicit positions, draft-region
-    entries, ancestor masks and gathered hidden inputs (sliding window too)."""
-    k = 4
+    entries, ancestor masks and gathered hidden inputs (sliding window too).  Eight
+    rows of four q heads are 32 queries per kv head: items of two m-tiles, with
+    16- and 12-slot cache blocks."""
     w = replace(w, mode="tree", top_k=k, depth=4, total=12, B=2)
     W, ctx, kv, dm = setup(w, max_rows=w.B * k)
     g = np.random.default_rng(3)
