@@ -64,6 +64,19 @@ SPEC_DEV void warp_argmax(float& v, int& i) {
   }
 }
 
+// The same winner as warp_argmax for non-NaN values (largest value, then smallest
+// index; -0 equals +0) from two warp-wide reductions on an order-preserving key
+// instead of five shuffle rounds; a NaN never wins here.
+SPEC_DEV void warp_argmax_redux(float& v, int& i) {
+  const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+  const uint32_t k = v != v ? 0u : ((u & 0x80000000u) ? ~u : (u | 0x80000000u));
+  const uint32_t km = __reduce_max_sync(0xffffffffu, k);
+  const int im = __reduce_min_sync(0xffffffffu, k == km ? i : 0x7fffffff);
+  const unsigned who = __ballot_sync(0xffffffffu, k == km && i == im);
+  v = __shfl_sync(0xffffffffu, v, __ffs(who) - 1);
+  i = im;
+}
+
 // block-wide sum for blockDim.x a multiple of 32 (<= 1024); all threads get the result
 SPEC_DEV float block_sum(float v, float* red) {
   int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;

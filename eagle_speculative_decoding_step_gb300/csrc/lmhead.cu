@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__
     for (int rr = 0; rr < k; ++rr) {
       float bv = tv[0];
       int bi = ti[0];
-      warp_argmax(bv, bi);
+      warp_argmax_redux(bv, bi);
       if (ti[0] == bi && bv == tv[0]) {           // the lane whose head won pops it
 #pragma unroll
         for (int q = 0; q < KT - 1; ++q) { tv[q] = tv[q + 1]; ti[q] = ti[q + 1]; }
