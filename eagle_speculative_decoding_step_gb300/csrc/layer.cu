@@ -1005,6 +1005,10 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
 //    slot with one arrive per warp on its "empty" barrier;
 //  * after an item's last tile the four warps merge through that tile's slot.
 // No CTA-wide barrier runs per tile or per item; every wait is bounded.
+// What it computes is the draft layer's attention of the file header ([NEURON]
+// "Eagle3 Draft Model Architecture"; slots from the block table as in "KV Cache
+// Sharing"; the window of [EAGLE4] Eagle4Config.sliding_window): per query,
+// softmax(q . k / sqrt(hd)) over the allowed keys, times V.
 struct AttnTileMeta {
   int b, g, q0, nQ, s, ctx, ci0, flags;
   unsigned long long valid;         // bit k: key ci0 + k is attended to by some query row
