@@ -683,6 +683,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
   uint64_t kv_policy;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(kv_policy));
   uint32_t fills = 0;                                 // ring fills consumed by this CTA before this item
+  uint32_t issued = 0, cons = 0;                      // fills issued; the fill a timed-out wait was for
   bool ok_all = true;
 
   // items: blockIdx.x first, then the next unclaimed one from a shared counter (ragged
@@ -761,6 +762,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
       auto issue = [&](int j) {
         if (j >= ntiles) return;
         const uint32_t fi = fills + (uint32_t)j;
+        issued = fi + 1;
         uint8_t* st = mma_smem + (size_t)(fi % NS) * Sh::STAGE;
         const int t0 = kbeg + j * TK;
         const int nk = min(TK, kend - t0);
@@ -826,7 +828,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
         issue(j + NS - 1);
         const uint32_t fi = fills + (uint32_t)j;
         const bool ok = tc::mbar_wait(bar0 + 8u * (fi % NS), (fi / NS) & 1u, abort);
-        if (__syncthreads_or(!ok)) { ok_all = false; break; }
+        if (__syncthreads_or(!ok)) { ok_all = false; cons = fi; break; }
         const uint8_t* st = mma_smem + (size_t)(fi % NS) * Sh::STAGE;
         const uint32_t kbase = smem_u32(st), vbase = kbase + TK * KP * 2;
         const int* ci_t = sCi + (fi % NS) * TK;
@@ -984,7 +986,11 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
       item += gridDim.x;
     }
   }
-  if (!ok_all && tid == 0) report(ws, SPEC_ERR_TIMEOUT, blockIdx.x, 0);
+  if (!ok_all) {
+    // let the copies still in flight land before the CTA's shared memory goes away
+    for (uint32_t f = cons; f < issued; ++f) tc::mbar_wait(bar0 + 8u * (f % NS), (f / NS) & 1u, abort, false);
+    if (tid == 0) report(ws, SPEC_ERR_TIMEOUT, blockIdx.x, 0);
+  }
 }
 
 // ---------------------------------------------------------------- warp-specialised attention (bf16, TMA)
