@@ -1221,7 +1221,7 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
     uint32_t fill = 0, mph = 0;
     float acc[NT][4];
     float mrun[2], lrun[2];
-    int rlo[2], nQ = 0, qsel = 0;
+    int rlo[2], nQ = 0, qsel = 0, lo_max = 0;   // lo_max: the latest window start of the item's rows
     unsigned long long rmask[2];
     bool rok[2];
     // this lane's ldmatrix rows: K (scores' "col" operand) and V (transposed)
@@ -1249,6 +1249,9 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
           rlo[h] = s_lo[qsel * QM + qi];
           rmask[h] = s_mask[qsel * QM + qi];
         }
+        lo_max = max(rok[0] ? rlo[0] : 0, rok[1] ? rlo[1] : 0);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lo_max = max(lo_max, __shfl_xor_sync(0xffffffffu, lo_max, o));
       }
       uint8_t* st = sm + (size_t)slot * S::STG;
       const uint32_t vm = (uint32_t)(mt.valid >> (16 * warp)) & 0xffffu;
@@ -1285,7 +1288,9 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
           mma_bf16(sc[0], a0, a1, a2, a3, b0, b1);
           mma_bf16(sc[1], a0, a1, a2, a3, b2, b3);
         }
-        // mask, scale to log2 units, warp-local online softmax
+        // mask, scale to log2 units, warp-local online softmax; a tile of valid context
+        // keys at or past every row's window start needs no per-key test
+        const bool open = vm == 0xffffu && mt.ci0 + TK <= mt.ctx && mt.ci0 >= lo_max;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (8 * h >= nQ) continue;     // rows of absent queries only (uniform in the warp)
@@ -1296,8 +1301,11 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
             for (int e = 0; e < 2; ++e) {
               const int kr = nt * 8 + 2 * tig + e;
               const int ci = mt.ci0 + warp * 16 + kr;
-              bool ok = rok[h] && ((vm >> kr) & 1u);
-              if (ok) ok = ci < mt.ctx ? ci >= rlo[h] : ((rmask[h] >> (ci - mt.ctx)) & 1ull) != 0;
+              bool ok = rok[h];
+              if (!open) {
+                ok = ok && ((vm >> kr) & 1u);
+                if (ok) ok = ci < mt.ctx ? ci >= rlo[h] : ((rmask[h] >> (ci - mt.ctx)) & 1ull) != 0;
+              }
               const float v = ok ? sc[nt][2 * h + e] * scale_log2 : -INFINITY;
               sc[nt][2 * h + e] = v;
               mx = fmaxf(mx, v);
