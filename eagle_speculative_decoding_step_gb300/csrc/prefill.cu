@@ -6,7 +6,7 @@
 // draft processes all target tokens of the step; its input ids are the target's
 // ids shifted by one, with the newly sampled token scattered at each request's
 // last token position; the first draft token and the recurrent state come from
-// that last position.  Reading for the row layout (stated in the design notes):
+// that last position.  The pages do not fix the row layout; the one taken here:
 // request b's R verified tokens sit at positions ctx_b .. ctx_b + R - 1, write
 // their K/V at draft-region entries 0 .. R-1 and attend causally (row j sees the
 // context and entries 0..j); rows after the last accepted one carry shifted

@@ -35,7 +35,15 @@ Pins (what each function is checked against, in ``tests/test_oracle_pins.py``):
   restatement; RoPE: norm preservation and relative-position invariance;
 * LM-head statistics: scipy logsumexp;
 * Philox4x32-10: the published known-answer vectors of the generator's authors;
-* SpecDecodeMetadata indices: the worked example printed on the Neuron page.
+* SpecDecodeMetadata indices: the worked example printed on the Neuron page;
+* batched initial pass (``step.prefill_inputs`` / ``prefill_chain_draft``): a
+  hand-worked shift-and-scatter case of the prefill phase, the causal R-row
+  pass equal to R single-row passes run in turn, one verified token reducing
+  to the chain drafter, and rows past the last accepted one ignored;
+* reduced draft vocabulary (``draft.lm_head`` with ``d2t``): the identity map
+  is the full head, a subset is the full head restricted to it;
+* candidate log-probs (``draft.lowrank_candidates(with_logprob=True)``): with
+  every token a candidate they are the full head's log-probs.
 
 Parity unpinned: none of the functions above is left without a pin; the
 absolute Philox stream beyond the three known-answer vectors is pinned only by

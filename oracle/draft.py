@@ -16,7 +16,7 @@ Sources:
   (low-rank candidate head whose retrieved candidates are rescored exactly with
   the full lm_head); ``Eagle4CandidateHeadConfig`` (rank, num_candidates).
 
-Readings where the pages are silent (each listed in the design notes):
+Readings where the pages are silent (the plainest choice each time):
 * residual of the attention block = the H-wide hidden input of the layer;
 * RMSNorm / RoPE / SwiGLU in their Llama forms (see ``numerics``);
 * attention scale 1/sqrt(head_dim); q head h uses kv head h // (nq / nkv);

@@ -5,8 +5,8 @@ Sources: [EAGLET] "Eaglet", section "Approach 1: YAML Recipe" and
 ``total_draft_tokens``; the draft model proposes candidate tokens in a tree and
 the target verifies the tree in one forward pass, page introduction).
 
-The pages give only the three parameters.  The reading used (EAGLE-2 style,
-listed in the design notes):
+The pages give only the three parameters.  The reading used (EAGLE-2 style;
+the pages fix none of the following):
 
 * the root is the last accepted token (node 0, depth 0, score 0);
 * depth 1: the root's top ``k`` tokens become nodes with score = log-prob;

@@ -688,3 +688,151 @@ def test_norm_output_recurrence_closed_form():
     np.testing.assert_array_equal(got_on, np.stack(want_on, 1))
     np.testing.assert_array_equal(got_off, np.stack(want_off, 1))
     assert (got_on[:, 0] == got_off[:, 0]).all() and (got_on != got_off).any()
+
+
+# ---------------------------------------------------------------- batched initial pass (prefill phase)
+def test_prefill_inputs_hand_worked_shift_and_scatter():
+    """[NEURON] "EagleProposer", ``propose()`` prefill phase: the input ids are
+    shifted left by one and the target's new token is scattered at each
+    request's last accepted position.  Worked by hand for two requests of four
+    verified positions (request 0 accepted everything, request 1 stopped at 1)."""
+    ids = np.array([[10, 11, 12, 13], [20, 21, 22, 23]])
+    rows, last_row = step.prefill_inputs(ids, next_token=[99, 98], last_idx=[3, 1], ctx_len=[7, 30])
+    np.testing.assert_array_equal(rows["tok"], [11, 12, 13, 99, 21, 98, 23, 0])
+    np.testing.assert_array_equal(rows["pos"], [7, 8, 9, 10, 30, 31, 32, 33])
+    np.testing.assert_array_equal(rows["kv_idx"], [0, 1, 2, 3, 0, 1, 2, 3])
+    assert rows["mask"] == [0b1, 0b11, 0b111, 0b1111] * 2          # causal over the draft region
+    np.testing.assert_array_equal(last_row, [3, 5])
+    assert rows["M"] == 8 and rows["R"] == 4 and rows["B"] == 2
+
+
+def test_prefill_causal_pass_equals_sequential_single_row_passes():
+    """One causal pass over R rows (every row's K/V written, then attention with
+    a lower-triangular draft-region mask) equals R single-row passes run one
+    after another, pass j writing entry j and attending entries 0..j: same
+    hidden states, same K/V bytes."""
+    w = replace(MICRO, dtype="f32", B=2, K=4)
+    W, ctx, kv = _setup(w)
+    R = 4
+    rng = np.random.default_rng(5)
+    ids = rng.integers(0, w.V, size=(w.B, R))
+    rows, _ = step.prefill_inputs(ids, next_token=[3, 4], last_idx=[R - 1, 2], ctx_len=ctx)
+    h0 = synth.make_hidden(w, w.B * R).astype(np.float64)
+    kv_a = copy.deepcopy(kv)
+    pre_a, hn_a = draft.draft_layer(w, W, rows, h0, kv_a)
+    kv_b = copy.deepcopy(kv)
+    tok = rows["tok"].reshape(w.B, R)
+    pre_b = np.zeros_like(pre_a)
+    hn_b = np.zeros_like(hn_a)
+    for j in range(R):
+        r = {"M": w.B, "B": w.B, "R": 1, "step": j, "ctx_len": ctx, "tok": tok[:, j]}
+        p, h = draft.draft_layer(w, W, r, h0.reshape(w.B, R, -1)[:, j], kv_b)
+        pre_b.reshape(w.B, R, -1)[:, j] = p
+        hn_b.reshape(w.B, R, -1)[:, j] = h
+    np.testing.assert_allclose(pre_a, pre_b, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(hn_a, hn_b, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(kv_a["k"], kv_b["k"], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(kv_a["v"], kv_b["v"], rtol=0, atol=1e-13)
+
+
+def test_prefill_chain_with_one_verified_token_is_the_chain_drafter():
+    """With a single verified position per request (R = 1, last index 0) the
+    prefill phase is the chain drafter's first pass on the new token at
+    position ctx, and the recurrent passes restart at context ctx + 1: the
+    drafts must equal ``chain_draft`` rooted at the new token.  An off-by-one
+    in the restart context or the recurrent step index breaks this."""
+    w = replace(MICRO, dtype="f32", B=2, K=4)
+    W, ctx, kv = _setup(w)
+    aux = synth.make_aux(w)
+    nxt = np.array([5, 17])
+    d_pre, lg_pre = step.prefill_chain_draft(w, W, aux, np.zeros((w.B, 1), dtype=np.int64), nxt, [0, 0], ctx,
+                                             copy.deepcopy(kv), w.K, keep_logits=True)
+    d_chain, lg_chain = step.chain_draft(w, W, aux, nxt, ctx, copy.deepcopy(kv), w.K, keep_logits=True)
+    np.testing.assert_array_equal(d_pre, d_chain)
+    np.testing.assert_allclose(lg_pre, lg_chain, rtol=1e-10, atol=1e-12)
+
+
+def test_prefill_rows_past_the_last_accepted_one_are_ignored():
+    """Rows after a request's last accepted position carry rejected drafts; their
+    K/V lies where the recurrent passes write before they read, so the drafts
+    equal those of a prefill over the accepted rows only."""
+    w = replace(MICRO, dtype="f32", B=1, K=3)
+    W, ctx, kv = _setup(w)
+    R, last = 4, 1
+    rng = np.random.default_rng(9)
+    ids = rng.integers(0, w.V, size=(1, R))
+    aux = synth.make_aux(w, rows=R)
+    d_full = step.prefill_chain_draft(w, W, aux, ids, [7], [last], ctx, copy.deepcopy(kv), w.K)
+    d_cut = step.prefill_chain_draft(w, W, aux[:last + 1], ids[:, :last + 1], [7], [last], ctx, copy.deepcopy(kv),
+                                     w.K)
+    np.testing.assert_array_equal(d_full, d_cut)
+    # ...while a different token in an accepted row does change them
+    ids2 = ids.copy()
+    ids2[0, 1] = (ids2[0, 1] + 1) % w.V
+    d_other, lg_o = step.prefill_chain_draft(w, W, aux, ids2, [7], [last], ctx, copy.deepcopy(kv), w.K,
+                                             keep_logits=True)
+    _, lg_f = step.prefill_chain_draft(w, W, aux, ids, [7], [last], ctx, copy.deepcopy(kv), w.K, keep_logits=True)
+    assert not np.allclose(lg_o, lg_f)
+
+
+# ---------------------------------------------------------------- reduced draft vocabulary (d2t)
+def test_lm_head_d2t_identity_map_is_the_full_head():
+    """A draft vocabulary equal to the target vocabulary with the identity map
+    must reproduce the full head exactly."""
+    w = replace(MICRO, dtype="f32")
+    W, _, _ = _setup(w)
+    hn = synth.make_hidden(w, 3).astype(np.float64)
+    ids_f, lp_f, lse_f, lg_f = draft.lm_head(w, W, hn, 5)
+    Wd = dict(W, d2t=np.arange(w.V, dtype=np.int32))
+    ids_d, lp_d, lse_d, lg_d = draft.lm_head(replace(w, draft_vocab=w.V), Wd, hn, 5)
+    np.testing.assert_array_equal(ids_d, ids_f)
+    np.testing.assert_array_equal(lp_d, lp_f)
+    np.testing.assert_array_equal(lse_d, lse_f)
+
+
+def test_lm_head_d2t_subset_is_the_full_head_restricted():
+    """A draft vocabulary S (lm_head rows = the full head's rows at S, d2t = S)
+    gives the full head's logits restricted to S: the emitted ids are the
+    target ids of the best entries of S, the log-probs normalise over S only."""
+    w = replace(MICRO, dtype="f32")
+    W, _, _ = _setup(w)
+    hn = synth.make_hidden(w, 4).astype(np.float64)
+    _, _, _, full = draft.lm_head(w, W, hn, 1)
+    S = np.sort(np.random.default_rng(3).choice(w.V, size=23, replace=False)).astype(np.int32)
+    Wd = dict(W, lm_head=W["lm_head"][S], d2t=S)
+    ids, lp, lse, lg = draft.lm_head(replace(w, draft_vocab=len(S)), Wd, hn, 4)
+    for m in range(4):
+        sub = full[m, S]
+        order = sorted(range(len(S)), key=lambda i: (-np.float32(sub[i]), i))[:4]   # brute force
+        np.testing.assert_array_equal(ids[m], S[order])
+        z = np.log(np.sum(np.exp(sub - sub.max()))) + sub.max()
+        np.testing.assert_allclose(lse[m], z, rtol=1e-13)
+        np.testing.assert_allclose(lp[m], sub[order] - z, rtol=1e-12, atol=1e-13)
+        assert set(ids[m].tolist()) <= set(S.tolist())
+
+
+# ---------------------------------------------------------------- candidate log-probs
+def test_lowrank_candidate_logprobs_with_every_token_a_candidate():
+    """With num_candidates = V every token is a candidate whatever the low-rank
+    scores are (rank 4 here, far from exact), so the softmax over the
+    candidates is the full softmax: the candidate head's top-k ids and
+    log-probs equal the full head's."""
+    w = replace(MICRO, dtype="f32", rank=4, num_candidates=MICRO.V)
+    W, _, _ = _setup(w)
+    W["lr_down"], W["lr_up"] = synth.lowrank_factors(W["lm_head"], 4, "f32")
+    hn = synth.make_hidden(w, 3).astype(np.float64)
+    ids_f, lp_f, _, _ = draft.lm_head(w, W, hn, 6)
+    cand, exact, out, out_lp = draft.lowrank_candidates(w, W, hn, w.V, 6, with_logprob=True)
+    np.testing.assert_array_equal(np.sort(cand, axis=1), np.tile(np.arange(w.V), (3, 1)))
+    np.testing.assert_array_equal(out, ids_f)
+    np.testing.assert_allclose(out_lp, lp_f, rtol=1e-12, atol=1e-13)
+    # with fewer candidates the log-probs normalise over the candidates only: they
+    # are at least the full log-probs, and exp sums to <= 1 over the kept ones
+    _, ex_s, out_s, lp_s = draft.lowrank_candidates(replace(w, num_candidates=10), W, hn, 10, 3,
+                                                     with_logprob=True)
+    for m in range(3):
+        np.testing.assert_allclose(np.exp(ex_s[m] - scipy.special.logsumexp(ex_s[m])).sum(), 1.0)
+        full_lp = dict(zip(range(w.V), (hn[m] @ W["lm_head"].astype(np.float64).T
+                                        - scipy.special.logsumexp(hn[m] @ W["lm_head"].astype(np.float64).T))))
+        for t, l in zip(out_s[m], lp_s[m]):
+            assert l >= full_lp[int(t)] - 1e-12
