@@ -91,7 +91,10 @@ class ChainStep:
         self.top_k, self.top_p = top_k, top_p
         self.vws = torch.zeros(lib.spec_verify_workspace_bytes(B, K + 1, V), dtype=torch.uint8, device=dev)
 
-    def draft(self):
+    def draft(self, trace=None):
+        """Issue the drafting calls.  ``trace(i, tensors)``, if given, is called on
+        the host after pass i is issued (tensors: that pass's hn, pre-norm state
+        and draft ids); it must synchronise before reading them."""
         dm, w, B, K = self.dm, self.dm.w, self.B, self.K
         lib.spec_fc_fuse(dm.desc, dm.weights, self.aux, self.h0, B, dm.ws)
         hid = self.h0
@@ -111,6 +114,8 @@ class ChainStep:
             else:
                 lib.spec_lm_head(dm.desc, dm.weights, hn, B, 1, ids, self.lp.data_ptr() + 4 * i, ws=dm.ws,
                                  ids_ld=K)
+            if trace is not None:
+                trace(i, {"hn": hn, "pre": out, "ids": self.drafts[:, i]})
             hid = hn if w.norm_output else out
 
     def verify(self):
@@ -164,21 +169,33 @@ class TreeStep:
         self.kv_src = torch.zeros(B, D + 1, **i32)
         self.vws = torch.zeros(lib.spec_verify_workspace_bytes(B, N + 1, V), dtype=torch.uint8, device=dev)
 
-    def draft(self):
+    def draft(self, trace=None):
+        """Issue the drafting calls.  ``trace(d, tensors)``, if given, is called on
+        the host after depth d's pass and head are issued (tensors: the pass's hn,
+        pre-norm state, top-k ids and log-probs); it must synchronise before
+        reading them.  The frontier rows of pass d + 1 are the ``f_*`` buffers once
+        the following expansion has run."""
         dm, B, k, D, N = self.dm, self.B, self.k, self.D, self.N
         lib.spec_fc_fuse(dm.desc, dm.weights, self.aux, self.h0, B, dm.ws)
         rows = lib.make_rows(B, B, 1, dm.ctx_len, self.root, step=0, max_ctx=dm.w.max_ctx)
         no = dm.w.norm_output          # EAGLE-3.1: children take the parent's normalised state
         lib.spec_draft_layer(dm.desc, dm.weights, rows, self.h0, self.pre[0], self.hns[0], dm.kv, dm.ws)
         self._head(B, self.hns[0])
+        if trace is not None:
+            trace(1, {"hn": self.hns[0][:B], "pre": self.pre[0][:B], "ids": self.ids[:B], "lp": self.lp[:B]})
         lib.spec_tree_expand(B, k, 1, D, N, dm.ctx_len, self.root, self.ids, self.lp, self.state, self.io)
         for d in range(2, D + 1):
+            if trace is not None:
+                trace(("rows", d), {"tok": self.f_tok, "pos": self.f_pos, "kv_idx": self.f_kv, "mask": self.f_mask,
+                                    "hid_src": self.f_src})
             rows = lib.make_rows(B * k, B, k, dm.ctx_len, self.f_tok, pos=self.f_pos, kv_idx=self.f_kv,
                                  mask=self.f_mask, hid_src=self.f_src, max_ctx=dm.w.max_ctx)
             src, dst = self.pre[d % 2], self.pre[(d + 1) % 2]
             hsrc, hdst = self.hns[d % 2], self.hns[(d + 1) % 2]
             lib.spec_draft_layer(dm.desc, dm.weights, rows, hsrc if no else src, dst, hdst, dm.kv, dm.ws)
             self._head(B * k, hdst)
+            if trace is not None:
+                trace(d, {"hn": hdst, "pre": dst, "ids": self.ids, "lp": self.lp})
             lib.spec_tree_expand(B, k, d, D, N, dm.ctx_len, self.root, self.ids, self.lp, self.state, self.io)
 
     def _head(self, M, hn):
