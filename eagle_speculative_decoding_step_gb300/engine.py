@@ -94,7 +94,8 @@ class ChainStep:
     def draft(self, trace=None):
         """Issue the drafting calls.  ``trace(i, tensors)``, if given, is called on
         the host after pass i is issued (tensors: that pass's hn, pre-norm state
-        and draft ids); it must synchronise before reading them."""
+        and draft ids, and the FC-fused feature h0); it must synchronise before
+        reading them."""
         dm, w, B, K = self.dm, self.dm.w, self.B, self.K
         lib.spec_fc_fuse(dm.desc, dm.weights, self.aux, self.h0, B, dm.ws)
         hid = self.h0
@@ -115,7 +116,7 @@ class ChainStep:
                 lib.spec_lm_head(dm.desc, dm.weights, hn, B, 1, ids, self.lp.data_ptr() + 4 * i, ws=dm.ws,
                                  ids_ld=K)
             if trace is not None:
-                trace(i, {"hn": hn, "pre": out, "ids": self.drafts[:, i]})
+                trace(i, {"hn": hn, "pre": out, "ids": self.drafts[:, i], "h0": self.h0})
             hid = hn if w.norm_output else out
 
     def verify(self):
@@ -172,8 +173,8 @@ class TreeStep:
     def draft(self, trace=None):
         """Issue the drafting calls.  ``trace(d, tensors)``, if given, is called on
         the host after depth d's pass and head are issued (tensors: the pass's hn,
-        pre-norm state, top-k ids and log-probs); it must synchronise before
-        reading them.  The frontier rows of pass d + 1 are the ``f_*`` buffers once
+        pre-norm state, top-k ids and log-probs, and at depth 1 the FC-fused
+        feature h0); it must synchronise before reading them.  The frontier rows of pass d + 1 are the ``f_*`` buffers once
         the following expansion has run."""
         dm, B, k, D, N = self.dm, self.B, self.k, self.D, self.N
         lib.spec_fc_fuse(dm.desc, dm.weights, self.aux, self.h0, B, dm.ws)
@@ -182,7 +183,8 @@ class TreeStep:
         lib.spec_draft_layer(dm.desc, dm.weights, rows, self.h0, self.pre[0], self.hns[0], dm.kv, dm.ws)
         self._head(B, self.hns[0])
         if trace is not None:
-            trace(1, {"hn": self.hns[0][:B], "pre": self.pre[0][:B], "ids": self.ids[:B], "lp": self.lp[:B]})
+            trace(1, {"hn": self.hns[0][:B], "pre": self.pre[0][:B], "ids": self.ids[:B], "lp": self.lp[:B],
+                      "h0": self.h0})
         lib.spec_tree_expand(B, k, 1, D, N, dm.ctx_len, self.root, self.ids, self.lp, self.state, self.io)
         for d in range(2, D + 1):
             if trace is not None:

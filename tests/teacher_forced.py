@@ -5,8 +5,11 @@ different token changes every later pass.  So instead of comparing two
 independent runs, the oracle follows the GPU's own decisions pass by pass:
 
 * every oracle pass runs on the rows the GPU ran (its token ids, positions,
-  draft-region entries, masks, hidden-state sources), with the oracle's own
-  hidden states carried from its previous pass; the pass's hidden states are
+  draft-region entries, masks, hidden-state sources) and on the GPU's own
+  hidden inputs (its FC-fused feature for the first pass, its previous pass's
+  recurrent state after that -- the same bf16 values), so each pass is
+  compared on its own and rounding differences do not accumulate along the
+  chain; the pass's hidden states, and the FC-fused feature itself, are
   compared with the GPU's within the bf16 tolerance;
 * every head decision is recomputed by the oracle on the GPU's own normalised
   state (the same bf16 values), so the GPU's ids must equal the oracle's except
@@ -58,10 +61,13 @@ def decision_tie(a, b):
     return abs(a - b) < DECISION_REL * max(1.0, abs(a), abs(b))
 
 
-def check_hidden(w, got, ref, what):
+def check_hidden(w, got, ref, what, stats=None):
     atol, rtol = _tol(w)
-    np.testing.assert_allclose(np.asarray(got, np.float64), np.asarray(ref, np.float64), atol=atol, rtol=rtol,
-                               err_msg=what)
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    np.testing.assert_allclose(got, ref, atol=atol, rtol=rtol, err_msg=what)
+    if stats is not None:
+        rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True)) + 1e-30
+        stats["max_err_over_rms"] = max(stats.get("max_err_over_rms", 0.0), float(np.max(np.abs(got - ref) / rms)))
 
 
 def check_full_head(w, W, hn, ids, lp, what, stats):
@@ -169,7 +175,8 @@ def chain(w, W, aux, root, ctx, kv, recs, drafts, lib=None, dm=None, stats=None,
     stats = stats if stats is not None else new_stats()
     B, K = drafts.shape
     passes = K + 1 if passes is None else passes
-    hid = od.fc_fuse(w, W, aux)
+    check_hidden(w, recs[0]["h0"], od.fc_fuse(w, W, aux), "h0 (FC fuse)", stats)
+    hid = recs[0]["h0"]
     tok = np.asarray(root, np.int64)
     logits = []
     Wl = np.asarray(W["lm_head"], np.float64)
@@ -178,8 +185,8 @@ def chain(w, W, aux, root, ctx, kv, recs, drafts, lib=None, dm=None, stats=None,
         pre, hn = od.draft_layer(w, W, rows, hid, kv)
         if i < K:
             r = recs[i]
-            check_hidden(w, r["hn"], hn, "pass %d hidden_normed" % i)
-            check_hidden(w, r["pre"], pre, "pass %d hidden_prenorm" % i)
+            check_hidden(w, r["hn"], hn, "pass %d hidden_normed" % i, stats)
+            check_hidden(w, r["pre"], pre, "pass %d hidden_prenorm" % i, stats)
             got = r["ids"].reshape(B, 1)
             if w.rank > 0:
                 cand, again = gpu_candidates(lib, dm, r["hn"], B, 1)
@@ -195,7 +202,8 @@ def chain(w, W, aux, root, ctx, kv, recs, drafts, lib=None, dm=None, stats=None,
         else:
             lg = hn @ Wl.T
         logits.append(lg)
-        hid = od.recurrent_state(w, pre, hn)
+        g = recs[min(i, K - 1)]                 # the GPU's recurrent state out of this pass
+        hid = g["hn"] if getattr(w, "norm_output", False) else g["pre"]
         if i < K:
             tok = drafts[:, i].astype(np.int64)
     return np.stack(logits, axis=1), stats
@@ -206,10 +214,10 @@ def tree(w, W, aux, root, ctx, kv, recs, gpu_tree, lib=None, dm=None, stats=None
     GPU's ids / log-probs; checks every pass and the final tree bit for bit."""
     stats = stats if stats is not None else new_stats()
     B, k, D, N = w.B, w.top_k, w.depth, w.total
-    h0 = od.fc_fuse(w, W, aux)
+    check_hidden(w, recs[1]["h0"], od.fc_fuse(w, W, aux), "h0 (FC fuse)", stats)
     st = otree.tree_init(B, k, D, N, root, ctx)
     rows = {"M": B, "B": B, "R": 1, "step": 0, "ctx_len": ctx, "tok": np.asarray(root, np.int64)}
-    hid_in = h0
+    hid_in = recs[1]["h0"]
     fin = None
     for d in range(1, D + 1):
         if d >= 2:
@@ -220,8 +228,8 @@ def tree(w, W, aux, root, ctx, kv, recs, gpu_tree, lib=None, dm=None, stats=None
         pre, hn = od.draft_layer(w, W, rows, hid_in, kv)
         r = recs[d]
         M = rows["M"]
-        check_hidden(w, r["hn"][:M], hn, "depth %d hidden_normed" % d)
-        check_hidden(w, r["pre"][:M], pre, "depth %d hidden_prenorm" % d)
+        check_hidden(w, r["hn"][:M], hn, "depth %d hidden_normed" % d, stats)
+        check_hidden(w, r["pre"][:M], pre, "depth %d hidden_prenorm" % d, stats)
         ids, lp = r["ids"][:M], r["lp"][:M]
         if w.rank > 0:
             cand, again = gpu_candidates(lib, dm, r["hn"][:M], M, k)
@@ -231,7 +239,9 @@ def tree(w, W, aux, root, ctx, kv, recs, gpu_tree, lib=None, dm=None, stats=None
             check_full_head(w, W, r["hn"][:M], ids, lp, "depth %d" % d, stats)
         res = otree.tree_expand(st, d, ids, lp)
         if d < D:
-            rows, hid_in = res, od.recurrent_state(w, pre, hn)
+            # the next pass takes the GPU's recurrent state of this pass's rows
+            rows = res
+            hid_in = (r["hn"] if getattr(w, "norm_output", False) else r["pre"])[:M]
         else:
             fin = res
     for key, gkey in (("tok", "tok"), ("parent", "par"), ("depth", "dep"), ("pos", "pos")):
