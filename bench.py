@@ -193,7 +193,7 @@ def config_of(w):
 def launches_per_step(w):
     layer = 11                                   # prologue, 4 GEMMs, 4 epilogues, attention + combine
     head = 6 if w.rank > 0 else 2                # fused LM head + merge, or the candidate head's 6
-    verify = 4 if w.verify == "rejection" else 2  # row statistics, decisions, sampled row, emit / argmax + finalize
+    verify = 1                                   # one verifier kernel (greedy or rejection, no top-k / top-p)
     if w.mode == "chain":
         return 2 + w.K * (layer + head) + verify
     return 2 + w.depth * (layer + head + 1) + verify  # + tree expansion per depth

@@ -90,6 +90,9 @@ EXPORTS = {
     "spec_gather_rows": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp]),
     "spec_verify_greedy_static": (c_i32, [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_vp,
                                           ctypes.POINTER(ModelDesc), ctypes.POINTER(KV), c_vp, c_vp]),
+    "spec_verify_greedy_static_capacity": (c_size, []),
+    "spec_verify_greedy_static_bytes": (c_size, [c_i32, c_i32, c_i32]),
+    "spec_verify_greedy_static_error": (c_i32, [ctypes.POINTER(c_i32), c_vp]),
 }
 
 _LIB = None
@@ -245,6 +248,20 @@ def spec_verify_greedy_static(B, R, V, target_logits, draft_tok, out_tok, accept
                                             ctypes.byref(desc) if desc is not None else None,
                                             ctypes.byref(kv) if kv is not None else None, _p(ctx_len), _stream()),
            "spec_verify_greedy_static")
+
+
+def spec_verify_greedy_static_capacity():
+    return _lib().spec_verify_greedy_static_capacity()
+
+
+def spec_verify_greedy_static_bytes(B, R, V):
+    return _lib().spec_verify_greedy_static_bytes(B, R, V)
+
+
+def spec_verify_greedy_static_error():
+    v = c_i32(0)
+    _check(_lib().spec_verify_greedy_static_error(ctypes.byref(v), _stream()), "spec_verify_greedy_static_error")
+    return v.value
 
 
 def spec_decode_metadata(R, cu_num_scheduled, num_draft, cu_num_draft, logits_indices, target_logits_indices,

@@ -37,54 +37,57 @@ static int verify_chunks(int rows, int V) {
 }
 static int chunk_len(int V, int nch) { int L = (V + nch - 1) / nch; return (L + 3) & ~3; }
 
-// ---------------------------------------------------------------- greedy argmax
-template <bool VEC>
-__global__ void __launch_bounds__(256) argmax_chunks_kernel(const float* __restrict__ logits, int V,
-                                                           int nch, int L, ArgPart* __restrict__ part) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ float rv[32];
-  __shared__ int ri[32];
-  const int row = blockIdx.y, c = blockIdx.x;
-  const float* x = logits + (size_t)row * V;
-  const int lo = c * L, hi = min(V, lo + L);
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
-  if (VEC) {
-    // four 16-byte loads in flight per thread
-    for (int j0 = lo + 4 * threadIdx.x; j0 < hi; j0 += 16 * blockDim.x) {
-      float4 q[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = j0 + 4 * u * blockDim.x;
-        if (j < hi) q[u] = *reinterpret_cast<const float4*>(x + j);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = j0 + 4 * u * blockDim.x;
-        if (j >= hi) break;
-        if (better(q[u].x, j, bv, bi)) { bv = q[u].x; bi = j; }
-        if (j + 1 < hi && better(q[u].y, j + 1, bv, bi)) { bv = q[u].y; bi = j + 1; }
-        if (j + 2 < hi && better(q[u].z, j + 2, bv, bi)) { bv = q[u].z; bi = j + 2; }
-        if (j + 3 < hi && better(q[u].w, j + 3, bv, bi)) { bv = q[u].w; bi = j + 3; }
-      }
-    }
-  } else {
-    for (int j = lo + threadIdx.x; j < hi; j += blockDim.x) {
-      float q = x[j];
-      if (better(q, j, bv, bi)) { bv = q; bi = j; }
-    }
+// ---------------------------------------------------------------- control words
+// After the header, a verifier workspace holds its completion counters (zero
+// when idle; every kernel that raises one sets it back to zero before it
+// finishes, so a zero-filled workspace stays ready for the next call):
+//   ticket, finished  -- rejection: start-order tickets / finished CTAs;
+//   cnt[B]            -- chunk CTAs of request b that finished their statistics;
+//   scnt[B]           -- sampling CTAs of request b that finished;
+//   decided[B]        -- rejection: request b's decision is published.
+// Header bytes 64..71 are two knobs a caller may set (zero = default): the
+// bound on a sampling CTA's wait in microseconds, and a test hook that keeps
+// request (value - 1)'s decision unpublished so its waits run out.
+struct VerifyCtl { int ticket, finished; };
+constexpr size_t kKnobWait = 64, kKnobWithhold = 68;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;     // 2 s
+
+static size_t ctl_bytes(int B) { return align_up(sizeof(VerifyCtl) + (size_t)B * 3 * sizeof(int), 256); }
+
+SPEC_DEV int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+SPEC_DEV void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Thread 0 of a CTA that finished its share of request b: true for the last of
+// `total` CTAs of that request (the counter is reset by the caller of this when
+// it is done).  Every earlier CTA's writes are visible to the last one.
+__device__ bool last_arrival(int* counter, int total, int* s_flag) {
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int n = atomicAdd(counter, 1);
+    *s_flag = (n == total - 1);
+    if (*s_flag) __threadfence();
   }
-  block_argmax(bv, bi, rv, ri);
-  if (threadIdx.x == 0) part[(size_t)row * nch + c] = ArgPart{bv, bi};
+  __syncthreads();
+  return *s_flag != 0;
 }
 
+// ---------------------------------------------------------------- greedy
+// One launch: CTA (c, row) reduces chunk c of a logits row to its argmax; the
+// last CTA of a request to finish (completion counter, no waiting) merges the
+// request's chunk records, makes the sequential accept decisions, writes the
+// outputs and moves the accepted K/V.
 __device__ int merged_argmax(const ArgPart* part, int row, int nch) {
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   for (int c = 0; c < nch; ++c) {
-    ArgPart p = part[(size_t)row * nch + c];
-    if (better(p.v, p.i, bv, bi)) { bv = p.v; bi = p.i; }
+    const float v = __ldcg(&part[(size_t)row * nch + c].v);
+    const int i = __ldcg(&part[(size_t)row * nch + c].i);
+    if (better(v, i, bv, bi)) { bv = v; bi = i; }
   }
   return bi;
 }
@@ -112,34 +115,91 @@ __device__ void compact_path(const spec_kv& kv, int b, int ctx, const int* src, 
   }
 }
 
-__global__ void __launch_bounds__(128) verify_greedy_finalize_kernel(
-    int R, int nch, const ArgPart* __restrict__ part, const int32_t* __restrict__ draft,
-    const int32_t* __restrict__ parent, int max_depth, int32_t* __restrict__ out,
-    int32_t* __restrict__ acc_out, int32_t* __restrict__ kv_src, spec_kv kv, int has_kv,
-    int row_elems, int elem_bytes, const int32_t* __restrict__ ctx_len, void* ws) {
+struct GreedyArgs {
+  const float* logits;
+  int V, R, nch, L;
+  ArgPart* part;
+  long long part_cap;        // chunk records the scratch holds (a larger index is not written)
+  int* cnt;
+  const int32_t* draft;
+  const int32_t* parent;
+  int max_depth;
+  int32_t* out;
+  int32_t* acc_out;
+  int32_t* kv_src;
+  spec_kv kv;
+  int has_kv, row_elems, elem_bytes;
+  const int32_t* ctx_len;
+  void* ws;
+};
+
+template <bool VEC>
+__global__ void __launch_bounds__(256) verify_greedy_kernel(GreedyArgs g) {
   pdl_wait();
   pdl_trigger();
+  __shared__ float rv[32];
+  __shared__ int ri[32];
   __shared__ int t[64];
   __shared__ int path[65];
-  __shared__ int s_a;
-  const int b = blockIdx.x;
-  for (int n = threadIdx.x; n < R; n += blockDim.x) t[n] = merged_argmax(part, b * R + n, nch);
+  __shared__ int s_a, s_last;
+  const int row = blockIdx.y, c = blockIdx.x;
+  const int V = g.V, R = g.R;
+  const float* x = g.logits + (size_t)row * V;
+  const int lo = c * g.L, hi = min(V, lo + g.L);
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  if (VEC) {
+    // four 16-byte loads in flight per thread
+    for (int j0 = lo + 4 * threadIdx.x; j0 < hi; j0 += 16 * blockDim.x) {
+      float4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + 4 * u * blockDim.x;
+        if (j < hi) q[u] = __ldcs(reinterpret_cast<const float4*>(x + j));
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + 4 * u * blockDim.x;
+        if (j >= hi) break;
+        if (better(q[u].x, j, bv, bi)) { bv = q[u].x; bi = j; }
+        if (j + 1 < hi && better(q[u].y, j + 1, bv, bi)) { bv = q[u].y; bi = j + 1; }
+        if (j + 2 < hi && better(q[u].z, j + 2, bv, bi)) { bv = q[u].z; bi = j + 2; }
+        if (j + 3 < hi && better(q[u].w, j + 3, bv, bi)) { bv = q[u].w; bi = j + 3; }
+      }
+    }
+  } else {
+    for (int j = lo + threadIdx.x; j < hi; j += blockDim.x) {
+      float q = x[j];
+      if (better(q, j, bv, bi)) { bv = q; bi = j; }
+    }
+  }
+  block_argmax(bv, bi, rv, ri);
+  if (threadIdx.x == 0) {
+    const long long at = (long long)row * g.nch + c;
+    if (at < g.part_cap) g.part[at] = ArgPart{bv, bi};
+    else report(g.ws, SPEC_ERR_CAPACITY, row, c);
+  }
+  const int b = row / R;
+  if (!last_arrival(&g.cnt[b], R * g.nch, &s_last)) return;
+
+  // ---- the request's last CTA: decisions, outputs, K/V compaction
+  for (int n = threadIdx.x; n < R; n += blockDim.x) t[n] = merged_argmax(g.part, b * R + n, g.nch);
   __syncthreads();
-  const int W = (parent == nullptr) ? R : max_depth + 1;
+  const int W = (g.parent == nullptr) ? R : g.max_depth + 1;
   if (threadIdx.x == 0) {
     int a = 0;
-    if (parent == nullptr) {
+    if (g.parent == nullptr) {
       const int K = R - 1;
-      const int32_t* d = draft + (size_t)b * K;
+      const int32_t* d = g.draft + (size_t)b * K;
       while (a < K && d[a] == t[a]) ++a;
       for (int i = 0; i < W; ++i) {
-        out[(size_t)b * W + i] = i < a ? d[i] : (i == a ? t[a] : -1);
-        if (kv_src) kv_src[(size_t)b * W + i] = i <= a ? i : -1;
+        g.out[(size_t)b * W + i] = i < a ? d[i] : (i == a ? t[a] : -1);
+        if (g.kv_src) g.kv_src[(size_t)b * W + i] = i <= a ? i : -1;
       }
       path[0] = 0;
     } else {
-      const int32_t* tok = draft + (size_t)b * R;
-      const int32_t* par = parent + (size_t)b * R;
+      const int32_t* tok = g.draft + (size_t)b * R;
+      const int32_t* par = g.parent + (size_t)b * R;
       unsigned long long accepted = 1ull;   // R <= 64
       int depth[64];
       depth[0] = 0;
@@ -147,7 +207,7 @@ __global__ void __launch_bounds__(128) verify_greedy_finalize_kernel(
       for (int n = 1; n < R; ++n) {
         int p = par[n];
         if (p < 0 || p >= n) {
-          report(ws, SPEC_ERR_DEVICE, b, n);
+          report(g.ws, SPEC_ERR_DEVICE, b, n);
           depth[n] = 0;
           continue;
         }
@@ -158,9 +218,9 @@ __global__ void __launch_bounds__(128) verify_greedy_finalize_kernel(
         }
       }
       a = depth[best];
-      if (a > max_depth) {
-        report(ws, SPEC_ERR_DEVICE, b, a);
-        a = max_depth;
+      if (a > g.max_depth) {
+        report(g.ws, SPEC_ERR_DEVICE, b, a);
+        a = g.max_depth;
       }
       int n = best;
       for (int dd = depth[best]; dd > 0; --dd) {
@@ -172,20 +232,21 @@ __global__ void __launch_bounds__(128) verify_greedy_finalize_kernel(
         int o = -1;
         if (i < a) o = tok[path[i + 1]];
         else if (i == a) o = t[best];
-        out[(size_t)b * W + i] = o;
-        if (kv_src) kv_src[(size_t)b * W + i] = i <= a ? path[i] : -1;
+        g.out[(size_t)b * W + i] = o;
+        if (g.kv_src) g.kv_src[(size_t)b * W + i] = i <= a ? path[i] : -1;
       }
     }
-    acc_out[b] = a;
+    g.acc_out[b] = a;
     s_a = a;
+    g.cnt[b] = 0;                              // ready for the next call
   }
   __syncthreads();
-  if (parent != nullptr && has_kv) {
-    const int ctx = ctx_len[b];
-    if (elem_bytes == 2)
-      compact_path<__nv_bfloat16>(kv, b, ctx, path, s_a, row_elems, ws);
+  if (g.parent != nullptr && g.has_kv) {
+    const int ctx = g.ctx_len[b];
+    if (g.elem_bytes == 2)
+      compact_path<__nv_bfloat16>(g.kv, b, ctx, path, s_a, g.row_elems, g.ws);
     else
-      compact_path<float>(kv, b, ctx, path, s_a, row_elems, ws);
+      compact_path<float>(g.kv, b, ctx, path, s_a, g.row_elems, g.ws);
   }
 }
 
@@ -361,38 +422,60 @@ __global__ void __launch_bounds__(1024) reject_threshold_kernel(const float* __r
 }
 
 // ---------------------------------------------------------------- rejection
-// Two streaming passes instead of one heavy one.  The accept tests need, per
-// row, only the log-sum-exp of the (filtered, tempered) target distribution;
-// the Gumbel sample is needed on one row per request: the first rejected
-// position, or row K for the bonus token.  So:
-//  1. rej_stats_kernel: every row, chunked -- max / sum-exp over the kept
-//     tokens (greedy rows: argmax);
-//  2. rej_decide_kernel: one warp per request -- merges the chunks row by row
-//     and makes the sequential accept decisions (greedy: draft == argmax),
-//     writes accept_len, the accepted drafts, -1 padding, kv_src, and for
-//     greedy requests the emitted token;
-//  3. rej_sample_kernel: the sampled row of every stochastic request, chunked
-//     -- Philox noise and the Gumbel-max key over the kept tokens, the draft
-//     token excluded on a rejected row (its records go where that request's
-//     row statistics were, no longer needed);
-//  4. rej_emit_kernel: merges the chunk keys, writes the emitted token.
+// One launch, two roles, in start order.  The accept tests need, per row, only
+// the log-sum-exp of the (filtered, tempered) target distribution; the Gumbel
+// sample is needed on one row per request: the first rejected position, or
+// row K for the bonus token.  So:
+//  * statistics CTAs (the first rows*nch tickets): chunk c of a row -- max /
+//    sum-exp over the kept tokens (greedy rows: argmax); the last of a
+//    request's statistics CTAs merges the chunks row by row, makes the
+//    sequential accept decisions, writes accept_len, the accepted drafts, -1
+//    padding, kv_src (greedy requests: also the emitted token) and publishes
+//    the decision;
+//  * sampling CTAs (the next B*nchs tickets): chunk c of request b's sampled
+//    row -- they wait (bounded) for the decision, then Philox noise and the
+//    Gumbel-max key over the kept tokens, the draft token excluded on a
+//    rejected row; the last of them writes the emitted token.
+// Tickets are taken when a CTA starts, so every statistics CTA had started
+// before any sampling CTA waits, and none of them waits on anything: the waits
+// end.  They are bounded all the same (SPEC_ERR_TIMEOUT).
+// a chunk record written by another CTA of this launch (read past L1)
+SPEC_DEV RejPart ld_rejpart(const RejPart* p) {
+  const float4 q = __ldcg(reinterpret_cast<const float4*>(p));
+  return RejPart{q.x, q.y, q.z, __float_as_int(q.w)};
+}
+
+struct RejArgs {
+  const float* logits;
+  int K, V, nch, L, nchs, Ls, nstat, ncta;
+  const float* temperature;
+  const Thr* thr;
+  const int32_t* draft;
+  uint2 key;
+  uint32_t w0;
+  RejPart* part;      // [rows, nch] statistics records
+  RejPart* spart;     // [B, nchs] sampling records
+  VerifyCtl* ctl;
+  int* cnt;
+  int* scnt;
+  int* decided;
+  int32_t* out;
+  int32_t* acc_out;
+  int32_t* kv_src;
+  void* ws;
+};
+
 template <bool VEC>
-__global__ void __launch_bounds__(256) rej_stats_kernel(const float* __restrict__ logits, int K, int V, int nch,
-                                                        int L, const float* __restrict__ temperature,
-                                                        RejPart* __restrict__ part, const Thr* __restrict__ thr) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ float red[32];
-  __shared__ int redi[32];
-  const int row = blockIdx.y, c = blockIdx.x;
-  const Thr tr = thr ? thr[row] : Thr{0u, 0x7fffffff};
+__device__ void rej_stats(const RejArgs& g, int row, int c, float* red, int* redi) {
+  const int K = g.K, V = g.V;
+  const Thr tr = g.thr ? g.thr[row] : Thr{0u, 0x7fffffff};
   const int b = row / (K + 1);
-  const float T = temperature[b];
+  const float T = g.temperature[b];
   const bool greedy = !(T > 0.f);
   const bool unit = T == 1.f;                 // y = l / 1 exactly: skip the division
-  const bool filt = thr != nullptr;
-  const float* x = logits + (size_t)row * V;
-  const int lo = c * L, hi = min(V, lo + L);
+  const bool filt = g.thr != nullptr;
+  const float* x = g.logits + (size_t)row * V;
+  const int lo = c * g.L, hi = min(V, lo + g.L);
   float m = -INFINITY, s = 0.f, bk = -INFINITY;
   int bi = 0x7fffffff;
   constexpr int UNR = 4;                      // 16-byte loads in flight per thread
@@ -442,18 +525,13 @@ __global__ void __launch_bounds__(256) rej_stats_kernel(const float* __restrict_
   const float contrib = (m == -INFINITY) ? 0.f : s * expf(m - bm);
   const float bs = block_sum(contrib, red);
   block_argmax(bk, bi, red, redi);
-  if (threadIdx.x == 0) part[(size_t)row * nch + c] = RejPart{bm, bs, bk, bi};
+  if (threadIdx.x == 0) g.part[(size_t)row * g.nch + c] = RejPart{bm, bs, bk, bi};
 }
 
-__global__ void __launch_bounds__(32) rej_decide_kernel(
-    const float* __restrict__ logits, int K, int V, int nch, const RejPart* __restrict__ part,
-    const int32_t* __restrict__ draft, const float* __restrict__ temperature, uint2 key, uint32_t ctr_w0,
-    int32_t* __restrict__ out, int32_t* __restrict__ acc_out, int32_t* __restrict__ kv_src,
-    const Thr* __restrict__ thr) {
-  pdl_wait();
-  pdl_trigger();
-  const int b = blockIdx.x, lane = threadIdx.x;
-  const float T = temperature[b];
+// The request's sequential accept decisions, by one warp, from the chunk records.
+__device__ void rej_decide(const RejArgs& g, int b) {
+  const int K = g.K, V = g.V, nch = g.nch, lane = threadIdx.x & 31;
+  const float T = g.temperature[b];
   const bool greedy = !(T > 0.f);
   int a = 0, emitted = -1;
   for (int i = 0; i <= K; ++i) {
@@ -462,7 +540,7 @@ __global__ void __launch_bounds__(32) rej_decide_kernel(
     float M = -INFINITY, bk = -INFINITY;
     int bi = 0x7fffffff;
     for (int c = lane; c < nch; c += 32) {
-      const RejPart p = part[row * nch + c];
+      const RejPart p = ld_rejpart(&g.part[row * nch + c]);
       M = fmaxf(M, p.m);
       if (better(p.key, p.idx, bk, bi)) { bk = p.key; bi = p.idx; }
     }
@@ -470,7 +548,7 @@ __global__ void __launch_bounds__(32) rej_decide_kernel(
     warp_argmax(bk, bi);
     float S = 0.f;
     for (int c = lane; c < nch; c += 32) {
-      const RejPart p = part[row * nch + c];
+      const RejPart p = ld_rejpart(&g.part[row * nch + c]);
       if (p.m > -INFINITY) S += p.s * expf(p.m - M);
     }
     S = warp_sum(S);
@@ -478,7 +556,7 @@ __global__ void __launch_bounds__(32) rej_decide_kernel(
       if (greedy) emitted = bi;
       break;
     }
-    const int d = draft[(size_t)b * K + i];
+    const int d = g.draft[(size_t)b * K + i];
     bool ok;
     if (greedy) {
       ok = (d == bi);
@@ -486,11 +564,11 @@ __global__ void __launch_bounds__(32) rej_decide_kernel(
       const float lse = M + logf(S);
       float pd = 0.f;
       if (d >= 0 && d < V) {
-        const float yd = logits[row * V + d] / T;
-        const Thr tr = thr ? thr[row] : Thr{0u, 0x7fffffff};
+        const float yd = g.logits[row * V + d] / T;
+        const Thr tr = g.thr ? g.thr[row] : Thr{0u, 0x7fffffff};
         if (kept_by(tr, okey(yd), d)) pd = expf(yd - lse);
       }
-      const uint4 r = philox4x32_10(make_uint4(0u, (uint32_t)i, (uint32_t)b, ctr_w0), key);
+      const uint4 r = philox4x32_10(make_uint4(0u, (uint32_t)i, (uint32_t)b, g.w0), g.key);
       ok = word_to_uniform(r.x) <= pd;
     }
     if (!ok) {
@@ -500,32 +578,22 @@ __global__ void __launch_bounds__(32) rej_decide_kernel(
     ++a;
   }
   for (int i = lane; i <= K; i += 32) {
-    if (i != a || greedy) out[(size_t)b * (K + 1) + i] = i < a ? draft[(size_t)b * K + i] : (i == a ? emitted : -1);
-    if (kv_src) kv_src[(size_t)b * (K + 1) + i] = i <= a ? i : -1;
+    if (i != a || greedy) g.out[(size_t)b * (K + 1) + i] = i < a ? g.draft[(size_t)b * K + i] : (i == a ? emitted : -1);
+    if (g.kv_src) g.kv_src[(size_t)b * (K + 1) + i] = i <= a ? i : -1;
   }
-  if (lane == 0) acc_out[b] = a;
+  if (lane == 0) g.acc_out[b] = a;
 }
 
 template <bool VEC>
-__global__ void __launch_bounds__(256) rej_sample_kernel(const float* __restrict__ logits, int K, int V, int nchs,
-                                                         int L, int region, const int32_t* __restrict__ draft,
-                                                         const float* __restrict__ temperature, uint2 key,
-                                                         uint32_t ctr_w, const int32_t* __restrict__ acc_in,
-                                                         RejPart* __restrict__ part, const Thr* __restrict__ thr) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ float red[32];
-  __shared__ int redi[32];
-  const int b = blockIdx.y, c = blockIdx.x;
-  const float T = temperature[b];
-  if (!(T > 0.f)) return;                     // greedy requests were settled by the decision kernel
-  const int i = acc_in[b];
+__device__ void rej_sample(const RejArgs& g, int b, int c, int i, float* red, int* redi) {
+  const int K = g.K, V = g.V;
+  const float T = g.temperature[b];
   const int row = b * (K + 1) + i;
-  const Thr tr = thr ? thr[row] : Thr{0u, 0x7fffffff};
+  const Thr tr = g.thr ? g.thr[row] : Thr{0u, 0x7fffffff};
   const bool unit = T == 1.f;
-  const int excl = i < K ? draft[(size_t)b * K + i] : -1;
-  const float* x = logits + (size_t)row * V;
-  const int lo = c * L, hi = min(V, lo + L);
+  const int excl = i < K ? g.draft[(size_t)b * K + i] : -1;
+  const float* x = g.logits + (size_t)row * V;
+  const int lo = c * g.Ls, hi = min(V, lo + g.Ls);
   float bk = -INFINITY;
   int bi = 0x7fffffff;
   // every thread handles aligned groups of 4 vocabulary ids = one Philox block
@@ -538,47 +606,184 @@ __global__ void __launch_bounds__(256) rej_sample_kernel(const float* __restrict
 #pragma unroll
       for (int l = 0; l < 4; ++l) v[l] = (j + l < hi) ? x[j + l] : -INFINITY;
     }
-    const uint4 r = philox4x32_10(make_uint4((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b, ctr_w), key);
+    const uint4 r = philox4x32_10(make_uint4((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b, g.w0 + 1u), g.key);
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
       if (j + l >= hi) break;
       const float y = unit ? v[l] : v[l] / T;
       if (j + l == excl || !kept_by(tr, okey(y), j + l)) continue;
-      const float g = y - logf(-logf(word_to_uniform(w[l])));
-      if (better(g, j + l, bk, bi)) { bk = g; bi = j + l; }
+      const float gk = y - logf(-logf(word_to_uniform(w[l])));
+      if (better(gk, j + l, bk, bi)) { bk = gk; bi = j + l; }
     }
   }
   block_argmax(bk, bi, red, redi);
-  if (threadIdx.x == 0) part[(size_t)b * region + c] = RejPart{0.f, 0.f, bk, bi};
+  if (threadIdx.x == 0) g.spart[(size_t)b * g.nchs + c] = RejPart{0.f, 0.f, bk, bi};
 }
 
-__global__ void __launch_bounds__(32) rej_emit_kernel(int K, int nchs, int region, const RejPart* __restrict__ part,
-                                                      const float* __restrict__ temperature,
-                                                      const int32_t* __restrict__ acc_in, int32_t* __restrict__ out) {
+template <bool VEC>
+__global__ void __launch_bounds__(256) verify_rejection_kernel(RejArgs g) {
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.x, lane = threadIdx.x;
-  if (!(temperature[b] > 0.f)) return;
-  float bk = -INFINITY;
-  int bi = 0x7fffffff;
-  for (int c = lane; c < nchs; c += 32) {
-    const RejPart p = part[(size_t)b * region + c];
-    if (better(p.key, p.idx, bk, bi)) { bk = p.key; bi = p.idx; }
+  __shared__ float red[32];
+  __shared__ int redi[32];
+  __shared__ int s_t, s_flag, s_ok, s_i;
+  const int nstat = g.nstat;
+  if (threadIdx.x == 0) s_t = atomicAdd(&g.ctl->ticket, 1);
+  __syncthreads();
+  const int t = s_t;
+  const int K = g.K;
+  if (t < nstat) {
+    const int row = t / g.nch, c = t % g.nch, b = row / (K + 1);
+    rej_stats<VEC>(g, row, c, red, redi);
+    if (last_arrival(&g.cnt[b], (K + 1) * g.nch, &s_flag)) {
+      if (threadIdx.x < 32) rej_decide(g, b);
+      if (threadIdx.x == 0) {
+        g.cnt[b] = 0;
+        const int hold = *reinterpret_cast<const int*>(static_cast<const char*>(g.ws) + kKnobWithhold);
+        if (g.temperature[b] > 0.f && hold != b + 1) {
+          __threadfence();
+          st_release(&g.decided[b], 1);
+        }
+      }
+    }
+  } else {
+    const int sidx = t - nstat, b = sidx / g.nchs, c = sidx % g.nchs;
+    if (g.temperature[b] > 0.f) {              // greedy requests were settled by their decision
+      if (threadIdx.x == 0) {
+        const int lim_us = *reinterpret_cast<const int*>(static_cast<const char*>(g.ws) + kKnobWait);
+        const unsigned long long lim = lim_us > 0 ? (unsigned long long)lim_us * 1000ull : kDefaultWaitNs;
+        const unsigned long long t0 = globaltimer_ns();
+        int ok = 0;
+        for (unsigned it = 0; it < (1u << 24); ++it) {      // the timer ends it; the count bounds it too
+          if (ld_acquire(&g.decided[b]) != 0) { ok = 1; break; }
+          if ((it & 15u) == 0 && globaltimer_ns() - t0 > lim) break;
+          __nanosleep(256);
+        }
+        if (!ok) report(g.ws, SPEC_ERR_TIMEOUT, b, c);
+        const int i = ok ? __ldcg(&g.acc_out[b]) : 0;
+        s_ok = ok && i >= 0 && i <= g.K;
+        s_i = i;
+      }
+      __syncthreads();
+      if (s_ok) {
+        rej_sample<VEC>(g, b, c, s_i, red, redi);
+      } else if (threadIdx.x == 0) {
+        g.spart[(size_t)b * g.nchs + c] = RejPart{0.f, 0.f, -INFINITY, 0x7fffffff};
+      }
+      if (last_arrival(&g.scnt[b], g.nchs, &s_flag)) {
+        if (threadIdx.x < 32) {
+          const int lane = threadIdx.x;
+          float bk = -INFINITY;
+          int bi = 0x7fffffff;
+          for (int cc = lane; cc < g.nchs; cc += 32) {
+            const RejPart p = ld_rejpart(&g.spart[(size_t)b * g.nchs + cc]);
+            if (better(p.key, p.idx, bk, bi)) { bk = p.key; bi = p.idx; }
+          }
+          warp_argmax(bk, bi);
+          if (lane == 0) {
+            const int i = __ldcg(&g.acc_out[b]);
+            if (i >= 0 && i <= K) g.out[(size_t)b * (K + 1) + i] = (bi == 0x7fffffff) ? -1 : bi;
+            else report(g.ws, SPEC_ERR_DEVICE, b, i);
+            g.scnt[b] = 0;
+            g.decided[b] = 0;
+          }
+        }
+      }
+    }
   }
-  warp_argmax(bk, bi);
-  if (lane == 0) out[(size_t)b * (K + 1) + acc_in[b]] = bi;
+  // the last CTA of the grid rewinds the ticket counter for the next call
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int n = atomicAdd(&g.ctl->finished, 1);
+    if (n == g.ncta - 1) {
+      g.ctl->ticket = 0;
+      g.ctl->finished = 0;
+    }
+  }
 }
 
+}  // namespace spec
+
+namespace spec {
+// Verifier workspace: header | control words | chunk records | sampling records
+// | top-k / top-p thresholds.  The greedy verifier uses the first three regions
+// only (8-byte records).
+struct VLayout {
+  size_t ctl, part, spart, thr, total, greedy_total;
+  int nch, nchs;
+};
+static int sample_chunks(int B, int V) {
+  int n = std::max(1, (640 + B - 1) / B);
+  return std::min(n, std::max(1, V / 2048));
+}
+static VLayout vlayout(int B, int R, int V) {
+  VLayout L{};
+  const int rows = B * R;
+  L.nch = verify_chunks(rows, V);
+  L.nchs = sample_chunks(B, V);
+  L.ctl = kWsHeader;
+  L.part = L.ctl + ctl_bytes(B);
+  L.greedy_total = L.part + align_up((size_t)rows * L.nch * sizeof(ArgPart), 256);
+  L.spart = L.part + align_up((size_t)rows * L.nch * sizeof(RejPart), 256);
+  L.thr = L.spart + align_up((size_t)B * L.nchs * sizeof(RejPart), 256);
+  L.total = L.thr + align_up((size_t)rows * sizeof(Thr), 256);
+  return L;
+}
+
+static spec_status greedy_args(int32_t B, int32_t R, int32_t V, const float* target_logits, const int32_t* draft_tok,
+                               const int32_t* parent, int32_t max_depth, int32_t* out_tok, int32_t* accept_len,
+                               int32_t* kv_src, const spec_model_desc* desc, const spec_kv* kv,
+                               const int32_t* ctx_len, GreedyArgs* g) {
+  if (B <= 0 || R <= 0 || V <= 0) return SPEC_ERR_SHAPE;
+  if (!target_logits || !draft_tok || !out_tok || !accept_len) return SPEC_ERR_ARG;
+  if (R > 64) return SPEC_ERR_CAPACITY;
+  if (parent == nullptr && R < 2) return SPEC_ERR_SHAPE;
+  if (parent != nullptr && (max_depth < 0 || max_depth >= 64)) return SPEC_ERR_SHAPE;
+  *g = GreedyArgs{};
+  if (parent != nullptr && kv != nullptr) {
+    if (!desc || !ctx_len || !kv->k || !kv->v || !kv->block_table) return SPEC_ERR_ARG;
+    if (kv->block_size <= 0 || kv->max_blocks <= 0 || kv->num_slots <= 0) return SPEC_ERR_SHAPE;
+    g->has_kv = 1;
+    g->kv = *kv;
+    g->row_elems = desc->n_kv_heads * desc->head_dim;
+    g->elem_bytes = desc->dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  }
+  g->logits = target_logits;
+  g->V = V;
+  g->R = R;
+  g->draft = draft_tok;
+  g->parent = parent;
+  g->max_depth = max_depth;
+  g->out = out_tok;
+  g->acc_out = accept_len;
+  g->kv_src = kv_src;
+  g->ctx_len = ctx_len;
+  return SPEC_OK;
+}
+
+static spec_status launch_greedy(GreedyArgs g, int B, void* ws, const VLayout& L, cudaStream_t stream) {
+  g.nch = L.nch;
+  g.L = chunk_len(g.V, L.nch);
+  g.part = reinterpret_cast<ArgPart*>(static_cast<char*>(ws) + L.part);
+  g.part_cap = (long long)B * g.R * L.nch;
+  g.cnt = reinterpret_cast<int*>(static_cast<char*>(ws) + L.ctl + sizeof(VerifyCtl));
+  g.ws = ws;
+  const dim3 grid(L.nch, B * g.R);
+  const bool vec = (g.V % 4 == 0) && aligned(g.logits, 16);
+  if (vec)
+    launch_pdl(verify_greedy_kernel<true>, grid, dim3(256), 0, stream, g);
+  else
+    launch_pdl(verify_greedy_kernel<false>, grid, dim3(256), 0, stream, g);
+  return last_launch();
+}
 }  // namespace spec
 
 using namespace spec;
 
 extern "C" size_t spec_verify_workspace_bytes(int32_t B, int32_t R, int32_t V) {
   if (B <= 0 || R <= 0 || V <= 0) return 0;
-  int rows = B * R;
-  int nch = verify_chunks(rows, V);
-  return kWsHeader + align_up((size_t)rows * nch * sizeof(RejPart), 256) + align_up((size_t)rows * sizeof(Thr), 256);
+  return vlayout(B, R, V).total;
 }
 
 extern "C" spec_status spec_verify_greedy(int32_t B, int32_t R, int32_t V, const float* target_logits,
@@ -587,36 +792,12 @@ extern "C" spec_status spec_verify_greedy(int32_t B, int32_t R, int32_t V, const
                                           int32_t* kv_src, const spec_model_desc* desc,
                                           const spec_kv* kv, const int32_t* ctx_len, void* ws,
                                           size_t ws_bytes, spec_stream_t stream) {
-  if (B <= 0 || R <= 0 || V <= 0) return SPEC_ERR_SHAPE;
-  if (!target_logits || !draft_tok || !out_tok || !accept_len) return SPEC_ERR_ARG;
-  if (R > 64) return SPEC_ERR_CAPACITY;
-  if (parent == nullptr && R < 2) return SPEC_ERR_SHAPE;
-  if (parent != nullptr && (max_depth < 0 || max_depth >= 64)) return SPEC_ERR_SHAPE;
+  GreedyArgs g;
+  spec_status s = greedy_args(B, R, V, target_logits, draft_tok, parent, max_depth, out_tok, accept_len, kv_src,
+                              desc, kv, ctx_len, &g);
+  if (s != SPEC_OK) return s;
   if (!ws || !aligned(ws, 256) || ws_bytes < spec_verify_workspace_bytes(B, R, V)) return SPEC_ERR_WORKSPACE;
-  int has_kv = 0, row_elems = 0, elem_bytes = 4;
-  spec_kv kvv{};
-  if (parent != nullptr && kv != nullptr) {
-    if (!desc || !ctx_len || !kv->k || !kv->v || !kv->block_table) return SPEC_ERR_ARG;
-    if (kv->block_size <= 0 || kv->max_blocks <= 0 || kv->num_slots <= 0) return SPEC_ERR_SHAPE;
-    has_kv = 1;
-    kvv = *kv;
-    row_elems = desc->n_kv_heads * desc->head_dim;
-    elem_bytes = desc->dtype == SPEC_DTYPE_BF16 ? 2 : 4;
-  }
-  const int rows = B * R;
-  const int nch = verify_chunks(rows, V);
-  const int L = chunk_len(V, nch);
-  ArgPart* part = reinterpret_cast<ArgPart*>(static_cast<char*>(ws) + kWsHeader);
-  dim3 grid(nch, rows);
-  const bool vec = (V % 4 == 0) && aligned(target_logits, 16);
-  if (vec)
-    launch_pdl(argmax_chunks_kernel<true>, dim3(grid), dim3(256), 0, stream, target_logits, V, nch, L, part);
-  else
-    launch_pdl(argmax_chunks_kernel<false>, dim3(grid), dim3(256), 0, stream, target_logits, V, nch, L, part);
-  launch_pdl(verify_greedy_finalize_kernel, dim3(B), dim3(128), 0, stream, R, nch, part, draft_tok, parent, max_depth, out_tok,
-                                                       accept_len, kv_src, kvv, has_kv, row_elems, elem_bytes,
-                                                       ctx_len, ws);
-  return last_launch();
+  return launch_greedy(g, B, ws, vlayout(B, R, V), stream);
 }
 
 extern "C" spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, const float* target_logits,
@@ -629,41 +810,44 @@ extern "C" spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, co
   if (!target_logits || !draft_tok || !temperature || !out_tok || !accept_len) return SPEC_ERR_ARG;
   const int R = K + 1;
   if (!ws || !aligned(ws, 256) || ws_bytes < spec_verify_workspace_bytes(B, R, V)) return SPEC_ERR_WORKSPACE;
+  const VLayout L = vlayout(B, R, V);
   const int rows = B * R;
-  const int nch = verify_chunks(rows, V);
-  const int L = chunk_len(V, nch);
-  RejPart* part = reinterpret_cast<RejPart*>(static_cast<char*>(ws) + kWsHeader);
-  uint2 key = make_uint2((uint32_t)(seed & 0xffffffffull), (uint32_t)(seed >> 32));
-  uint32_t w0 = (uint32_t)((2ull * step_offset) & 0xffffffffull);
-  Thr* thr = nullptr;
+  char* base = static_cast<char*>(ws);
+  RejArgs g{};
+  g.logits = target_logits;
+  g.K = K;
+  g.V = V;
+  g.nch = L.nch;
+  g.L = chunk_len(V, L.nch);
+  g.nchs = L.nchs;
+  g.Ls = chunk_len(V, L.nchs);
+  g.nstat = rows * L.nch;
+  g.ncta = g.nstat + B * L.nchs;
+  g.temperature = temperature;
+  g.draft = draft_tok;
+  g.key = make_uint2((uint32_t)(seed & 0xffffffffull), (uint32_t)(seed >> 32));
+  g.w0 = (uint32_t)((2ull * step_offset) & 0xffffffffull);
+  g.part = reinterpret_cast<RejPart*>(base + L.part);
+  g.spart = reinterpret_cast<RejPart*>(base + L.spart);
+  g.ctl = reinterpret_cast<VerifyCtl*>(base + L.ctl);
+  g.cnt = reinterpret_cast<int*>(base + L.ctl + sizeof(VerifyCtl));
+  g.scnt = g.cnt + B;
+  g.decided = g.cnt + 2 * B;
+  g.out = out_tok;
+  g.acc_out = accept_len;
+  g.kv_src = kv_src;
+  g.ws = ws;
   if (top_k || top_p) {
-    thr = reinterpret_cast<Thr*>(reinterpret_cast<char*>(part) + align_up((size_t)rows * nch * sizeof(RejPart), 256));
+    Thr* thr = reinterpret_cast<Thr*>(base + L.thr);
     launch_pdl(reject_threshold_kernel, dim3(rows), dim3(1024), 0, stream, target_logits, K, V, temperature, top_k,
                top_p, thr);
+    g.thr = thr;
   }
   const bool vec = (V % 4 == 0) && aligned(target_logits, 16);
   if (vec)
-    launch_pdl(rej_stats_kernel<true>, dim3(nch, rows), dim3(256), 0, stream, target_logits, K, V, nch, L, temperature,
-               part, (const Thr*)thr);
+    launch_pdl(verify_rejection_kernel<true>, dim3(g.ncta), dim3(256), 0, stream, g);
   else
-    launch_pdl(rej_stats_kernel<false>, dim3(nch, rows), dim3(256), 0, stream, target_logits, K, V, nch, L,
-               temperature, part, (const Thr*)thr);
-  launch_pdl(rej_decide_kernel, dim3(B), dim3(32), 0, stream, target_logits, K, V, nch, (const RejPart*)part,
-             draft_tok, temperature, key, w0, out_tok, accept_len, kv_src, (const Thr*)thr);
-  // the sampled rows: one per request, chunked over the CTAs; each request's records
-  // take the slots of its (now consumed) row statistics
-  const int region = R * nch;
-  int nchs = std::min(region, std::max(1, (640 + B - 1) / B));
-  nchs = std::min(nchs, std::max(1, V / 2048));
-  const int Ls = chunk_len(V, nchs);
-  if (vec)
-    launch_pdl(rej_sample_kernel<true>, dim3(nchs, B), dim3(256), 0, stream, target_logits, K, V, nchs, Ls, region,
-               draft_tok, temperature, key, w0 + 1u, (const int32_t*)accept_len, part, (const Thr*)thr);
-  else
-    launch_pdl(rej_sample_kernel<false>, dim3(nchs, B), dim3(256), 0, stream, target_logits, K, V, nchs, Ls, region,
-               draft_tok, temperature, key, w0 + 1u, (const int32_t*)accept_len, part, (const Thr*)thr);
-  launch_pdl(rej_emit_kernel, dim3(B), dim3(32), 0, stream, K, nchs, region, (const RejPart*)part, temperature,
-             (const int32_t*)accept_len, out_tok);
+    launch_pdl(verify_rejection_kernel<false>, dim3(g.ncta), dim3(256), 0, stream, g);
   return last_launch();
 }
 
@@ -676,14 +860,15 @@ extern "C" spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, co
 // that is part of the loaded library (every GPU that loads the library holds it
 // until the process exits).
 namespace spec {
-constexpr size_t kStaticVerifyScratch = 256 * 1024;     // header + chunk partials
+constexpr size_t kStaticVerifyScratch = 256 * 1024;     // header + control words + chunk records
 static __device__ __align__(256) unsigned char g_verify_scratch[kStaticVerifyScratch];
 constexpr int kStaticMaxDevices = 64;
 static void* g_verify_scratch_addr[kStaticMaxDevices];
 static std::mutex g_verify_scratch_mu;
 
 // Device address of the scratch array on the current device (looked up once per
-// device, with that device current).  nullptr if the lookup fails.
+// device, with that device current; the cached address does not survive a
+// cudaDeviceReset of that device).  nullptr if the lookup fails.
 static void* static_verify_scratch() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStaticMaxDevices) return nullptr;
@@ -697,45 +882,41 @@ static void* static_verify_scratch() {
 }
 }  // namespace spec
 
+extern "C" size_t spec_verify_greedy_static_capacity(void) { return kStaticVerifyScratch; }
+
+extern "C" size_t spec_verify_greedy_static_bytes(int32_t B, int32_t R, int32_t V) {
+  if (B <= 0 || R <= 0 || V <= 0) return 0;
+  return vlayout(B, R, V).greedy_total;
+}
+
 extern "C" spec_status spec_verify_greedy_static(int32_t B, int32_t R, int32_t V, const float* target_logits,
                                                  const int32_t* draft_tok, const int32_t* parent,
                                                  int32_t max_depth, int32_t* out_tok, int32_t* accept_len,
                                                  int32_t* kv_src, const spec_model_desc* desc, const spec_kv* kv,
                                                  const int32_t* ctx_len, spec_stream_t stream) {
-  if (B <= 0 || R <= 0 || V <= 0) return SPEC_ERR_SHAPE;
-  if (!target_logits || !draft_tok || !out_tok || !accept_len) return SPEC_ERR_ARG;
-  if (R > 64) return SPEC_ERR_CAPACITY;
-  if (parent == nullptr && R < 2) return SPEC_ERR_SHAPE;
-  if (parent != nullptr && (max_depth < 0 || max_depth >= 64)) return SPEC_ERR_SHAPE;
-  // the same scratch layout as the workspace version must fit the fixed array
-  if (spec_verify_workspace_bytes(B, R, V) > kStaticVerifyScratch) return SPEC_ERR_CAPACITY;
-  int has_kv = 0, row_elems = 0, elem_bytes = 4;
-  spec_kv kvv{};
-  if (parent != nullptr && kv != nullptr) {
-    if (!desc || !ctx_len || !kv->k || !kv->v || !kv->block_table) return SPEC_ERR_ARG;
-    if (kv->block_size <= 0 || kv->max_blocks <= 0 || kv->num_slots <= 0) return SPEC_ERR_SHAPE;
-    has_kv = 1;
-    kvv = *kv;
-    row_elems = desc->n_kv_heads * desc->head_dim;
-    elem_bytes = desc->dtype == SPEC_DTYPE_BF16 ? 2 : 4;
-  }
+  GreedyArgs g;
+  spec_status s = greedy_args(B, R, V, target_logits, draft_tok, parent, max_depth, out_tok, accept_len, kv_src,
+                              desc, kv, ctx_len, &g);
+  if (s != SPEC_OK) return s;
+  // the greedy layout (header, control words, 8-byte chunk records) must fit the array
+  const VLayout L = vlayout(B, R, V);
+  if (L.greedy_total > kStaticVerifyScratch) return SPEC_ERR_CAPACITY;
   void* ws = static_verify_scratch();
   if (ws == nullptr) return SPEC_ERR_CUDA;
-  // the array keeps the previous call's contents: the error header starts at zero;
-  // every chunk partial is rewritten before it is read
-  if (cudaMemsetAsync(ws, 0, kWsHeader, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  const int rows = B * R;
-  const int nch = verify_chunks(rows, V);
-  const int L = chunk_len(V, nch);
-  ArgPart* part = reinterpret_cast<ArgPart*>(static_cast<char*>(ws) + kWsHeader);
-  dim3 grid(nch, rows);
-  const bool vec = (V % 4 == 0) && aligned(target_logits, 16);
-  if (vec)
-    launch_pdl(argmax_chunks_kernel<true>, dim3(grid), dim3(256), 0, stream, target_logits, V, nch, L, part);
-  else
-    launch_pdl(argmax_chunks_kernel<false>, dim3(grid), dim3(256), 0, stream, target_logits, V, nch, L, part);
-  launch_pdl(verify_greedy_finalize_kernel, dim3(B), dim3(128), 0, stream, R, nch, part, draft_tok, parent, max_depth, out_tok,
-                                                       accept_len, kv_src, kvv, has_kv, row_elems, elem_bytes,
-                                                       ctx_len, ws);
-  return last_launch();
+  // the array keeps the previous call's contents: the error header and the
+  // completion counters start at zero; every chunk record is rewritten before it
+  // is read
+  if (cudaMemsetAsync(ws, 0, L.part, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  return launch_greedy(g, B, ws, L, stream);
+}
+
+extern "C" spec_status spec_verify_greedy_static_error(int32_t* code_out, spec_stream_t stream) {
+  if (!code_out) return SPEC_ERR_ARG;
+  void* ws = static_verify_scratch();
+  if (ws == nullptr) return SPEC_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  *code_out = v;
+  return SPEC_OK;
 }

@@ -292,10 +292,25 @@ spec_status spec_tree_expand(int32_t B, int32_t top_k, int32_t depth_idx, int32_
 /* ------------------------------------------------------------------ */
 /* Verification.                                                       */
 
-/* Workspace bytes for the verifiers over B requests of R rows of V logits. */
+/* Workspace bytes for the verifiers over B requests of R rows of V logits.
+ * Layout: the 256-byte header (error word first), the verifiers' completion
+ * counters, chunk records, sampling records, top-k / top-p thresholds.  The
+ * workspace must be zero-filled before its first use (the counters start at
+ * zero; every call leaves them at zero again).  Header bytes 64..71 hold two
+ * optional int32 settings, zero for the defaults: the bound in microseconds on
+ * the wait of spec_verify_rejection's sampling CTAs for their request's
+ * decision (default 2 s; when it runs out the error word becomes
+ * SPEC_ERR_TIMEOUT and that request's emitted token is -1), and a test hook --
+ * a value k > 0 keeps request k-1's decision unpublished, so its waits run out.
+ * Both verifiers are one kernel launch each (spec_verify_rejection adds one for
+ * top-k / top-p thresholds); calls sharing a workspace must not overlap on the
+ * GPU. */
 size_t spec_verify_workspace_bytes(int32_t B, int32_t R, int32_t V);
 
-/* Greedy verification.  [NEURON] "Rejection Sampling", on-device sampler:
+/* Greedy verification, one kernel: chunk CTAs reduce the target rows to their
+ * argmax; the last CTA of a request to finish (a completion counter, no
+ * waiting) makes the request's decisions and moves its K/V.
+ * [NEURON] "Rejection Sampling", on-device sampler:
  * t = argmax(target) per row (ties to the smaller id); accept drafts in order
  * until the first mismatch, emit the target token there, or a bonus token when
  * all match; -1 after.  [NEURON] "What is Speculative Decoding?" (bit-exact
@@ -319,7 +334,10 @@ spec_status spec_verify_greedy(int32_t B, int32_t R, int32_t V, const float *tar
                                const spec_kv *kv, const int32_t *ctx_len,
                                void *ws, size_t ws_bytes, spec_stream_t stream);
 
-/* Stochastic verification of a greedy-drafted chain.  [NEURON] "Rejection
+/* Stochastic verification of a greedy-drafted chain, one kernel: statistics
+ * CTAs (max / sum-exp per row chunk), the last of a request's making its
+ * accept decisions, then sampling CTAs of the request's one sampled row, which
+ * wait (bounded) for that decision.  [NEURON] "Rejection
  * Sampling", CPU sampler (arXiv:2211.17192): p = softmax(target / T); accept
  * draft d at position i when u <= p(d) (draft prob 1); at the first rejection
  * emit argmax_x p(x) / E_x over x != d (Gumbel-max with exponential noise
@@ -400,18 +418,35 @@ spec_status spec_gather_rows(const void *src, int32_t n_src, int32_t row_bytes, 
  * ws / ws_bytes.  Its scratch is a fixed 256 KiB array of device memory inside
  * the library (held on every GPU that loads the library until the process
  * exits); requests whose scratch (spec_verify_workspace_bytes(B, R, V)) exceeds
- * it return SPEC_ERR_CAPACITY without launching.  The first call on a device
- * looks up the array's device address with that device current; make that first
- * call before any stream capture.  All calls share the one array, so calls that
- * overlap on the GPU (different streams, no ordering) race; calls ordered on
- * one stream are safe.  Each call clears the array's error header; device-side
- * index errors of this variant are not reported back (offending accesses are
- * skipped as in the workspace version).  It allocates nothing. */
+ * it return SPEC_ERR_CAPACITY without launching; the scratch a request needs is
+ * spec_verify_greedy_static_bytes(B, R, V) (256-byte header, B completion
+ * counters, 8 bytes per chunk record: about B*R*ceil(640/(B*R))*8 bytes for
+ * large vocabularies) and the array's size is
+ * spec_verify_greedy_static_capacity().  The first call on a device looks up
+ * the array's device address with that device current and keeps it (it does
+ * not survive a cudaDeviceReset of that device); make that first call before
+ * any stream capture.  All calls share the one array, so calls that overlap on
+ * the GPU (different streams, no ordering) race; calls ordered on one stream
+ * are safe.  Each call clears the array's error header and counters;
+ * spec_verify_greedy_static_error reads the error word the last call left
+ * (device-side index errors, as in the workspace version).  It allocates
+ * nothing. */
 spec_status spec_verify_greedy_static(int32_t B, int32_t R, int32_t V, const float *target_logits,
                                       const int32_t *draft_tok, const int32_t *parent,
                                       int32_t max_depth, int32_t *out_tok, int32_t *accept_len,
                                       int32_t *kv_src, const spec_model_desc *desc,
                                       const spec_kv *kv, const int32_t *ctx_len, spec_stream_t stream);
+
+/* Size in bytes of spec_verify_greedy_static's fixed scratch array, and the
+ * scratch one call over B requests of R rows of V logits needs (the paper has
+ * no counterpart; see spec_verify_greedy_static). */
+size_t spec_verify_greedy_static_capacity(void);
+size_t spec_verify_greedy_static_bytes(int32_t B, int32_t R, int32_t V);
+
+/* The error word spec_verify_greedy_static's last call on the current device
+ * left in its fixed scratch array (0 = none, else a spec_status code), read
+ * after synchronising ``stream`` (the paper has no counterpart). */
+spec_status spec_verify_greedy_static_error(int32_t *code_out, spec_stream_t stream);
 
 #ifdef __cplusplus
 }

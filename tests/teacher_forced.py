@@ -62,12 +62,26 @@ def decision_tie(a, b):
 
 
 def check_hidden(w, got, ref, what, stats=None):
+    """Hidden states within the bf16 tolerance, its absolute part taken at the
+    row's scale: |gpu - oracle| <= atol * max(1, rms(row)) + rtol * |oracle|.
+    The residual stream (hidden_prenorm) grows to an RMS of 3-13 in these
+    workloads, and its differences scale with it: besides bf16 storage, the
+    attention's second product takes the softmax weights as bf16 operands (a
+    relative error up to 2^-9 per weight, against the oracle's exact weights),
+    which moves the attention output, and through the output projection the
+    whole row, in proportion to the row's magnitude."""
     atol, rtol = _tol(w)
     got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
-    np.testing.assert_allclose(got, ref, atol=atol, rtol=rtol, err_msg=what)
+    rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
+    lim = atol * np.maximum(1.0, rms) + rtol * np.abs(ref)
+    bad = np.abs(got - ref) > lim
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError("%s: %d of %d elements outside tolerance; first at %s: gpu %.6g oracle %.6g "
+                             "(row rms %.4g)" % (what, int(bad.sum()), bad.size, i, got[i], ref[i], rms[i[:-1]][0]))
     if stats is not None:
-        rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True)) + 1e-30
-        stats["max_err_over_rms"] = max(stats.get("max_err_over_rms", 0.0), float(np.max(np.abs(got - ref) / rms)))
+        stats["max_err_over_rms"] = max(stats.get("max_err_over_rms", 0.0),
+                                        float(np.max(np.abs(got - ref) / (rms + 1e-30))))
 
 
 def check_full_head(w, W, hn, ids, lp, what, stats):

@@ -15,7 +15,7 @@ from eagle_speculative_decoding_step_gb300 import binding as lib, configs, engin
 from oracle import step as ostep, verify as overify
 import teacher_forced as tf
 from gpu_helpers import dev, dev_act
-from test_gpu_step import check_rejection
+from test_gpu_step import TEST_SIGMA, check_rejection
 
 pytestmark = pytest.mark.gpu
 
@@ -66,10 +66,12 @@ def test_chain_full_size(name, sample):
     lg, stats = tf.chain(w, W64, aux[idx], root[idx], ctx[idx], _sub_kv(kv, idx), sub, drafts_all[idx], lib=lib,
                          dm=dm)
     # target logits: the oracle's logits for the GPU's drafts + noise on the sampled
-    # requests, noise elsewhere; then the whole step in the bench's launch form
+    # requests (greedy: small noise, so some drafts are accepted and the accept path
+    # runs), the workload's noise elsewhere; then the whole step in the bench's launch form
     noise = synth.noise(w, (w.B, w.K + 1, w.V))
     target = noise.copy()
-    target[idx] = (lg + noise[idx]).astype(np.float32)
+    small = noise[idx] * (TEST_SIGMA / w.sigma) if w.verify == "greedy" else noise[idx]
+    target[idx] = (lg + small).astype(np.float32)
     st.target.copy_(dev(target))
     st.run()
     torch.cuda.synchronize()
@@ -118,7 +120,7 @@ def test_tree_full_size():
     assert dm.device_error() == 0
     for key in ("tok", "par", "dep", "pos", "score", "mask"):
         np.testing.assert_array_equal(tf.gpu_tree_of(st)[key], gt[key])
-    noise = synth.noise(w, (w.B, w.total + 1, w.V))
+    noise = synth.noise(w, (w.B, w.total + 1, w.V)) * (TEST_SIGMA / w.sigma)
     target = ostep.tree_target(w, W64, aux, ctx, kv, fin, noise)
     st.target = dev(target)
     ref_out, ref_acc, _ = overify.verify_greedy_tree(target, fin["tok"], fin["parent"], w.depth)

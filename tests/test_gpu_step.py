@@ -29,6 +29,13 @@ def check_rejection(out, acc, ref_out, ref_acc, info, stats):
         stats["decision_ties"] += 1
 
 
+# The step tests draw target logits as the oracle's draft logits + N(0, 0.05): close
+# enough to the drafts that requests accept some drafts, so verification is
+# exercised past the first position (the workloads' own noise, sigma >= 0.5, lets
+# almost nothing through at these vocabulary sizes).
+TEST_SIGMA = 0.05
+
+
 def run_chain_teacher_forced(w, target_noise=True):
     W, ctx, kv, dm = setup(w)
     aux = synth.make_aux(w)
@@ -41,7 +48,7 @@ def run_chain_teacher_forced(w, target_noise=True):
     torch.cuda.synchronize()
     drafts = st.drafts.cpu().numpy()
     lg, stats = tf.chain(w, W, aux, root, ctx, copy.deepcopy(kv), recs, drafts, lib=lib, dm=dm)
-    noise = synth.noise(w, (w.B, w.K + 1, w.V))
+    noise = synth.noise(replace(w, sigma=TEST_SIGMA), (w.B, w.K + 1, w.V))
     target = ((lg if target_noise else 0.0) + noise).astype(np.float32)
     st.target.copy_(dev(target))
     st.verify()
@@ -69,6 +76,8 @@ def run_chain_teacher_forced(w, target_noise=True):
 def test_chain_step(w):
     stats, acc = run_chain_teacher_forced(w)
     assert stats["decision_ties"] + stats["boundary_ties"] <= w.B * w.K
+    if w.verify == "greedy":
+        assert acc.max() >= 1                     # some drafts accepted: the accept path ran
 
 
 def test_chain_step_reduced_draft_vocabulary():
@@ -92,7 +101,7 @@ def run_tree_teacher_forced(w):
     # one), target logits = the oracle's draft pass over that tree + noise; the GPU's
     # cache gets the K/V of that same pass
     kv_t = copy.deepcopy(kv)
-    noise = synth.noise(w, (w.B, w.total + 1, w.V))
+    noise = synth.noise(replace(w, sigma=TEST_SIGMA), (w.B, w.total + 1, w.V))
     target = ostep.tree_target(w, W, aux, ctx, kv_t, fin, noise)
     st.target = dev(target)
     dm.tkv["k"].copy_(engine.to_device(kv_t["k"], w.dtype, "cuda"))

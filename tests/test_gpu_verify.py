@@ -175,3 +175,30 @@ def test_verify_rejection_top_k_top_p(B, K, V):
         row = target[b, a].astype(np.float64) / temp[b]
         kept, _ = verify.kept_set(row, top_k[b], float(top_p[b]))
         assert kept[out[b, a]]
+
+
+def test_verifiers_reuse_their_workspace():
+    """Each verifier is one launch whose completion counters return to zero: calls
+    in a row on one workspace (alternating greedy and rejection, different batch
+    sizes within it) all match the oracle."""
+    B, K, V = 9, 4, 20000
+    ws = torch.zeros(lib.spec_verify_workspace_bytes(B, K + 1, V), dtype=torch.uint8, device="cuda")
+    for call in range(4):
+        b = B - call
+        target, drafts = _chain_inputs(b, K, V, seed=40 + call, plant=[0, K, 2, 1])
+        out = torch.zeros(b, K + 1, dtype=torch.int32, device="cuda")
+        acc = torch.zeros(b, dtype=torch.int32, device="cuda")
+        if call % 2 == 0:
+            ref_out, ref_acc, _ = verify.verify_greedy_chain(target, drafts)
+            lib.spec_verify_greedy(b, K + 1, V, dev(target), dev(drafts), out, acc, ws=ws)
+        else:
+            temp = np.full(b, 0.8, dtype=np.float32)
+            ref_out, ref_acc, info = verify.verify_rejection(target, drafts, temp, 5, call)
+            lib.spec_verify_rejection(b, K, V, dev(target), dev(drafts), dev(temp), 5, call, out, acc, ws=ws)
+        torch.cuda.synchronize()
+        got_out, got_acc = out.cpu().numpy(), acc.cpu().numpy()
+        for r in range(b):
+            if not (np.array_equal(got_out[r], ref_out[r]) and got_acc[r] == ref_acc[r]):
+                assert call % 2 == 1 and ((np.abs(info["accept_margin"][r]) < 1e-5).any()
+                                          or info["sample_gap"][r] < 1e-4), "call %d request %d" % (call, r)
+        assert lib.spec_get_device_error(ws) == 0

@@ -99,8 +99,68 @@ def test_static_scratch_tree_with_compaction_matches_workspace_version_twice():
         assert int(results[0][1].max()) >= 1
 
 
+def _greedy_pair(B, R, V, seed):
+    g = np.random.default_rng(seed)
+    target = torch.randn(B, R, V, generator=torch.Generator().manual_seed(seed)).cuda()
+    t = target.argmax(-1).cpu().numpy()
+    drafts = g.integers(0, V, size=(B, R - 1))
+    for b in range(B):
+        a = int(g.integers(0, R))
+        drafts[b, :a] = t[b, :a]
+    return target, torch.from_numpy(drafts.astype(np.int32)).cuda()
+
+
+def test_static_scratch_at_its_capacity_edge():
+    """The largest batch whose scratch fits the array runs and matches the workspace
+    version; one request more is refused with SPEC_ERR_CAPACITY, and nothing is
+    launched (outputs untouched)."""
+    cap = lib.spec_verify_greedy_static_capacity()
+    R, V = 8, 1024
+    B = 1
+    while lib.spec_verify_greedy_static_bytes(B + 1, R, V) <= cap:
+        B += 1
+    assert lib.spec_verify_greedy_static_bytes(B + 1, R, V) > cap
+    target, drafts = _greedy_pair(B + 1, R, V, 5)
+    want = _run_chain(False, B, R - 1, V, target[:B].contiguous(), drafts[:B].contiguous())
+    got = _run_chain(True, B, R - 1, V, target[:B].contiguous(), drafts[:B].contiguous())
+    for a, b in zip(got, want):
+        assert torch.equal(a, b)
+    out = torch.full((B + 1, R), -7, dtype=torch.int32, device="cuda")
+    acc = torch.full((B + 1,), -7, dtype=torch.int32, device="cuda")
+    with pytest.raises(lib.SpecError) as e:
+        lib.spec_verify_greedy_static(B + 1, R, V, target, drafts, out, acc)
+    assert e.value.status == -4
+    torch.cuda.synchronize()
+    assert int(out.min()) == -7 and int(out.max()) == -7 and int(acc.max()) == -7
+
+
 def test_static_scratch_rejects_oversized_request_without_launch():
-    FAKE = 4096        # never dereferenced: the size check fails first
-    st = lib.load().spec_verify_greedy_static(1000, 64, 1 << 20, FAKE, FAKE, None, 0, FAKE, FAKE, None, None, None,
-                                              None, None)
-    assert st == -4    # SPEC_ERR_CAPACITY
+    """Real, correctly sized device buffers whose scratch need exceeds the array:
+    refused with SPEC_ERR_CAPACITY before any launch."""
+    B, R, V = 1000, 40, 16
+    assert lib.spec_verify_greedy_static_bytes(B, R, V) > lib.spec_verify_greedy_static_capacity()
+    target, drafts = _greedy_pair(B, R, V, 3)
+    out = torch.full((B, R), -7, dtype=torch.int32, device="cuda")
+    acc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    with pytest.raises(lib.SpecError) as e:
+        lib.spec_verify_greedy_static(B, R, V, target, drafts, out, acc)
+    assert e.value.status == -4
+    torch.cuda.synchronize()
+    assert int(out.max()) == -7 and int(acc.max()) == -7
+
+
+def test_static_scratch_error_word_is_readable():
+    """A tree whose node 2 names node 3 as its parent (a parent must precede its
+    node) sets the array's error word to SPEC_ERR_DEVICE; the next valid call
+    clears it."""
+    B, N, V = 1, 4, 512
+    target = torch.randn(B, N + 1, V, generator=torch.Generator().manual_seed(4)).cuda()
+    tok = torch.zeros(B, N + 1, dtype=torch.int32, device="cuda")
+    par = torch.tensor([[-1, 0, 3, 0, 1]], dtype=torch.int32, device="cuda")
+    out = torch.zeros(B, 4, dtype=torch.int32, device="cuda")
+    acc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    lib.spec_verify_greedy_static(B, N + 1, V, target, tok, out, acc, parent=par, max_depth=3)
+    assert lib.spec_verify_greedy_static_error() == -6
+    par_ok = torch.tensor([[-1, 0, 0, 1, 2]], dtype=torch.int32, device="cuda")
+    lib.spec_verify_greedy_static(B, N + 1, V, target, tok, out, acc, parent=par_ok, max_depth=3)
+    assert lib.spec_verify_greedy_static_error() == 0
