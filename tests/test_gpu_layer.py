@@ -141,7 +141,15 @@ def test_draft_layer_tree_rows(w, k):
 @pytest.mark.parametrize("k,M", [(1, 3), (8, 8), (1, 64), (8, 1)])
 def test_lm_head(w, k, M):
     if w.dtype == "f32" and M > 32:
-        pytest.skip("fp32 path serves at most 32 rows")
+        # the fp32 path serves at most 32 rows: the call is refused before any launch
+        W, ctx, kv, dm = setup(w, max_rows=32)
+        hn = torch.zeros(M, w.H, dtype=torch.float32, device="cuda")
+        ids = torch.zeros(M, k, dtype=torch.int32, device="cuda")
+        lp = torch.zeros(M, k, dtype=torch.float32, device="cuda")
+        with pytest.raises(lib.SpecError) as e:
+            lib.spec_lm_head(dm.desc, dm.weights, hn, M, k, ids, lp, ws=dm.ws)
+        assert e.value.status == -2
+        return
     W, ctx, kv, dm = setup(w, max_rows=M)
     hn = synth.make_hidden(w, M, sub=5)
     ref_ids, ref_lp, ref_lse, ref_logits = od.lm_head(w, W, hn, k)

@@ -76,8 +76,10 @@ def run_chain_teacher_forced(w, target_noise=True):
 def test_chain_step(w):
     stats, acc = run_chain_teacher_forced(w)
     assert stats["decision_ties"] + stats["boundary_ties"] <= w.B * w.K
-    if w.verify == "greedy":
-        assert acc.max() >= 1                     # some drafts accepted: the accept path ran
+    if w.verify == "greedy" and w.rank == 0:
+        # some drafts accepted: the accept path ran (the candidate head's drafts need
+        # not be the full head's argmax, so its chains may all be rejected)
+        assert acc.max() >= 1
 
 
 def test_chain_step_reduced_draft_vocabulary():
