@@ -1021,8 +1021,12 @@ struct AttnTileMeta {
 };
 constexpr int kTileFirst = 1, kTileLast = 2, kTileEnd = 4, kTileQBuf = 8;
 
-template <int HD> struct WsShape {
-  static constexpr int TK = 64, QM = 16, NS = 2, NH = HD / 64, KP = HD + 8;
+// MT query m-tiles of 16 per item: the four consumer warps split an item's 64
+// keys into 4 / MT blocks of 16 * MT keys; warp w serves m-tile w / (4 / MT)
+// with key block w % (4 / MT), so every K / V row is read from shared memory
+// once per m-tile and the merge combines the 4 / MT warps of an m-tile.
+template <int HD, int MT = 1> struct WsShape {
+  static constexpr int TK = 64, QM = 16 * MT, NS = 2, NH = HD / 64, KP = HD + 8;
   static constexpr int HALF = TK * 128;                  // 64 keys x one 64-column half, 128-B rows
   static constexpr int KVB = NH * HALF;                  // a K (or V) tile
   static constexpr int STG = 2 * KVB;
@@ -1035,7 +1039,8 @@ template <int HD> struct WsShape {
   static constexpr size_t kMisc = kBar + (size_t)(2 * NS + 1) * 8;   // abort, consumed[4], issued
   static constexpr size_t kBytes = kMisc + 32;
   static constexpr size_t kSmem = kBytes + 1024;                     // + alignment of the ring to 1024 B
-  static_assert((size_t)4 * QM * HD * 4 <= (size_t)STG, "the merge reuses one ring slot");
+  static_assert((size_t)4 * 16 * HD * 4 <= (size_t)STG, "the merge reuses one ring slot");
+  static_assert(MT == 1 || MT == 2, "one or two m-tiles");
 };
 
 SPEC_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x, int y, int z, uint64_t pol) {
@@ -1046,8 +1051,8 @@ SPEC_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int
       : "memory");
 }
 
-template <int HD>
-__global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__ CUtensorMap tmk,
+template <int HD, int MT>
+__global__ void __launch_bounds__(160, MT == 1 ? 3 : 2) attn_ws_kernel(const __grid_constant__ CUtensorMap tmk,
                                                          const __grid_constant__ CUtensorMap tmv,
                                                          const __nv_bfloat16* __restrict__ qbuf, spec_kv kv,
                                                          RowInfo ri, int nq, int nkv, int window, int nsplit,
@@ -1056,8 +1061,9 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
                                                          int* __restrict__ work, void* ws) {
   pdl_wait();
   pdl_trigger();
-  using S = WsShape<HD>;
+  using S = WsShape<HD, MT>;
   constexpr int TK = S::TK, QM = S::QM, NS = S::NS, NH = S::NH, KP = S::KP, NT = HD / 8, KS = HD / 16;
+  constexpr int WPM = 4 / MT, KPW = TK / WPM;   // warps per m-tile, keys per warp
   extern __shared__ __align__(1024) uint8_t wsm_raw[];
   uint8_t* sm = wsm_raw + ((1024u - (smem_u32(wsm_raw) & 1023u)) & 1023u);
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(sm + S::kQ);
@@ -1218,16 +1224,19 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
   } else {
     // ------------------------------------------------------------ consumers
     const int grp = lane >> 2, tig = lane & 3;
+    const int mtile = MT == 1 ? 0 : warp / WPM, kbase = (warp % WPM) * KPW;   // this warp's m-tile and keys
     uint32_t fill = 0, mph = 0;
     float acc[NT][4];
     float mrun[2], lrun[2];
-    int rlo[2], nQ = 0, qsel = 0, lo_max = 0;   // lo_max: the latest window start of the item's rows
+    int rlo[2], nQ = 0, qsel = 0, lo_max = 0;   // lo_max: the latest window start of the warp's rows
     unsigned long long rmask[2];
     bool rok[2];
-    // this lane's ldmatrix rows: K (scores' "col" operand) and V (transposed)
-    const int key_k = warp * 16 + 8 * (lane >> 4) + (lane & 7), sel_k = (lane >> 3) & 1;
-    const int key_v = warp * 16 + 8 * ((lane >> 3) & 1) + (lane & 7), sel_v = lane >> 4;
+    // this lane's ldmatrix rows (relative to the warp's first key): K (scores' "col"
+    // operand) and V (transposed)
+    const int key_k = 8 * (lane >> 4) + (lane & 7), sel_k = (lane >> 3) & 1;
+    const int key_v = 8 * ((lane >> 3) & 1) + (lane & 7), sel_v = lane >> 4;
     const uint32_t x7 = (uint32_t)(lane & 7);
+    constexpr uint32_t kFull = KPW == 32 ? 0xffffffffu : ((1u << KPW) - 1u);
     for (;; ++fill) {
       const int slot = (int)(fill % NS);
       if (!tc::mbar_wait(full0 + 8u * slot, (fill / NS) & 1u, abort)) break;
@@ -1244,7 +1253,7 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
         for (int h = 0; h < 2; ++h) {
           mrun[h] = -INFINITY;
           lrun[h] = 0.f;
-          const int qi = grp + 8 * h;
+          const int qi = 16 * mtile + grp + 8 * h;
           rok[h] = qi < nQ;
           rlo[h] = s_lo[qsel * QM + qi];
           rmask[h] = s_mask[qsel * QM + qi];
@@ -1254,15 +1263,16 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
         for (int o = 16; o > 0; o >>= 1) lo_max = max(lo_max, __shfl_xor_sync(0xffffffffu, lo_max, o));
       }
       uint8_t* st = sm + (size_t)slot * S::STG;
-      const uint32_t vm = (uint32_t)(mt.valid >> (16 * warp)) & 0xffffu;
+      const uint32_t vm = (uint32_t)(mt.valid >> kbase) & kFull;
       bool wrote = false;
-      if (vm != 0) {
-        if (vm != 0xffffu) {
-          // V rows of this warp's invalid keys: zeros (stale or unloaded rows may hold anything)
-          for (int e = lane; e < 16 * NH * 8; e += 32) {
+      if (vm != 0 && 16 * mtile < nQ) {
+        if (vm != kFull) {
+          // V rows of this warp's invalid keys: zeros (stale or unloaded rows may hold
+          // anything); a warp of the other m-tile may write the same zeros
+          for (int e = lane; e < KPW * NH * 8; e += 32) {
             const int kr = e / (NH * 8), c = e % (NH * 8);
             if (!((vm >> kr) & 1u)) {
-              const int key = warp * 16 + kr;
+              const int key = kbase + kr;
               *reinterpret_cast<uint4*>(st + S::KVB + (size_t)(c >> 3) * S::HALF + (size_t)key * 128 + (c & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
             }
@@ -1271,36 +1281,43 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
           __syncwarp();
         }
         const uint32_t kst = smem_u32(st), vst = kst + S::KVB;
-        const uint32_t qb = smem_u32(sQ + (size_t)qsel * QM * KP);
+        const uint32_t qb = smem_u32(sQ + (size_t)qsel * QM * KP + (size_t)mtile * 16 * KP);
         const uint32_t qrow = qb + (uint32_t)((8 * ((lane >> 3) & 1) + (lane & 7)) * KP + 8 * (lane >> 4)) * 2;
-        float sc[2][4];
+        float sc[2 * MT][4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2 * MT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
 #pragma unroll
+        const uint32_t krow = kst + (uint32_t)((kbase + key_k) * 128);
         for (int ks = 0; ks < KS; ++ks) {
-          uint32_t b0, b1, b2, b3;   // keys 16w + {0..7, 8..15} x dims ks*16 + {0..7, 8..15}
           const uint32_t c = (uint32_t)(((ks & 3) << 1) | sel_k);
-          ldsm_x4(kst + (uint32_t)((ks >> 2) * S::HALF + key_k * 128) + ((c ^ x7) << 4), b0, b1, b2, b3);
+          uint32_t b[MT][4];         // keys kbase + 16j + {0..7, 8..15} x dims ks*16 + {0..7, 8..15}
+#pragma unroll
+          for (int j = 0; j < MT; ++j)
+            ldsm_x4(krow + (uint32_t)((ks >> 2) * S::HALF + 16 * j * 128) + ((c ^ x7) << 4), b[j][0], b[j][1],
+                    b[j][2], b[j][3]);
           uint32_t a0, a1, a2, a3;
           ldsm_x4(qrow + (uint32_t)(ks * 16 * 2), a0, a1, a2, a3);
-          mma_bf16(sc[0], a0, a1, a2, a3, b0, b1);
-          mma_bf16(sc[1], a0, a1, a2, a3, b2, b3);
+#pragma unroll
+          for (int j = 0; j < MT; ++j) {
+            mma_bf16(sc[2 * j], a0, a1, a2, a3, b[j][0], b[j][1]);
+            mma_bf16(sc[2 * j + 1], a0, a1, a2, a3, b[j][2], b[j][3]);
+          }
         }
         // mask, scale to log2 units, warp-local online softmax; a tile of valid context
         // keys at or past every row's window start needs no per-key test
-        const bool open = vm == 0xffffu && mt.ci0 + TK <= mt.ctx && mt.ci0 >= lo_max;
+        const bool open = vm == kFull && mt.ci0 + TK <= mt.ctx && mt.ci0 >= lo_max;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          if (8 * h >= nQ) continue;     // rows of absent queries only (uniform in the warp)
+          if (16 * mtile + 8 * h >= nQ) continue;     // rows of absent queries only (uniform in the warp)
           float mx = -INFINITY;
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+          for (int nt = 0; nt < 2 * MT; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int kr = nt * 8 + 2 * tig + e;
-              const int ci = mt.ci0 + warp * 16 + kr;
+              const int ci = mt.ci0 + kbase + kr;
               bool ok = rok[h];
               if (!open) {
                 ok = ok && ((vm >> kr) & 1u);
@@ -1316,7 +1333,7 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
           const float al = mnew == -INFINITY ? 1.f : exp2f(mrun[h] - mnew);
           float ps = 0.f;
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+          for (int nt = 0; nt < 2 * MT; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const float p = mnew == -INFINITY ? 0.f : exp2f(sc[nt][2 * h + e] - mnew);
@@ -1333,25 +1350,31 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
             }
           }
         }
-        const uint32_t pa0 = pack_bf16(sc[0][0], sc[0][1]), pa1 = pack_bf16(sc[0][2], sc[0][3]);
-        const uint32_t pa2 = pack_bf16(sc[1][0], sc[1][1]), pa3 = pack_bf16(sc[1][2], sc[1][3]);
+        const uint32_t vrow = vst + (uint32_t)((kbase + key_v) * 128);
 #pragma unroll
-        for (int n2 = 0; n2 < NT / 2; ++n2) {
-          uint32_t v0, v1, v2, v3;   // keys 16w + {0..7, 8..15} x dims 16*n2 + {0..7, 8..15}
-          const uint32_t c = (uint32_t)(((n2 & 3) << 1) | sel_v);
-          ldsm_x4_t(vst + (uint32_t)((n2 >> 2) * S::HALF + key_v * 128) + ((c ^ x7) << 4), v0, v1, v2, v3);
-          mma_bf16(acc[2 * n2], pa0, pa1, pa2, pa3, v0, v1);
-          mma_bf16(acc[2 * n2 + 1], pa0, pa1, pa2, pa3, v2, v3);
+        for (int j = 0; j < MT; ++j) {
+          // P of keys kbase + 16j .. + 15 as the A operand (bf16)
+          const uint32_t pa0 = pack_bf16(sc[2 * j][0], sc[2 * j][1]), pa1 = pack_bf16(sc[2 * j][2], sc[2 * j][3]);
+          const uint32_t pa2 = pack_bf16(sc[2 * j + 1][0], sc[2 * j + 1][1]);
+          const uint32_t pa3 = pack_bf16(sc[2 * j + 1][2], sc[2 * j + 1][3]);
+#pragma unroll
+          for (int n2 = 0; n2 < NT / 2; ++n2) {
+            uint32_t v0, v1, v2, v3;   // keys kbase + 16j + {0..7, 8..15} x dims 16*n2 + {0..7, 8..15}
+            const uint32_t c = (uint32_t)(((n2 & 3) << 1) | sel_v);
+            ldsm_x4_t(vrow + (uint32_t)((n2 >> 2) * S::HALF + 16 * j * 128) + ((c ^ x7) << 4), v0, v1, v2, v3);
+            mma_bf16(acc[2 * n2], pa0, pa1, pa2, pa3, v0, v1);
+            mma_bf16(acc[2 * n2 + 1], pa0, pa1, pa2, pa3, v2, v3);
+          }
         }
       }
       if (mt.flags & kTileLast) {
-        // merge the four warps through this slot (every warp is done with its K and V)
+        // merge the warps of each m-tile through this slot (every warp is done with its K and V)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(mbar);
         bool okm = tc::mbar_wait(mbar, mph, abort);
         mph ^= 1u;
         if (!okm) break;
-        float* red = reinterpret_cast<float*>(st);     // [4][QM][HD], 8-float blocks swizzled by row
+        float* red = reinterpret_cast<float*>(st);     // [4 warps][16][HD], 8-float blocks swizzled by row
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           float l = lrun[h];
@@ -1359,13 +1382,13 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
           l += __shfl_xor_sync(0xffffffffu, l, 2);
           const int row = grp + 8 * h;
           if (tig == 0) {
-            sMw[warp * QM + row] = mrun[h];
-            sLw[warp * QM + row] = l;
+            sMw[warp * 16 + row] = mrun[h];
+            sLw[warp * 16 + row] = l;
           }
           if (rok[h]) {
 #pragma unroll
             for (int n = 0; n < NT; ++n)
-              *reinterpret_cast<float2*>(red + ((size_t)warp * QM + row) * HD + ((n ^ (row & 7)) << 3) + 2 * tig) =
+              *reinterpret_cast<float2*>(red + ((size_t)warp * 16 + row) * HD + ((n ^ (row & 7)) << 3) + 2 * tig) =
                   make_float2(acc[n][2 * h], acc[n][2 * h + 1]);
           }
         }
@@ -1376,17 +1399,18 @@ __global__ void __launch_bounds__(160, 3) attn_ws_kernel(const __grid_constant__
         if (!okm) break;
         for (int e = tid; e < nQ * HD; e += 128) {
           const int qi = e / HD, d = e % HD;
-          const int col = (((d >> 3) ^ (qi & 7)) << 3) + (d & 7);
+          const int r = qi & 15, w0 = (qi >> 4) * WPM;
+          const int col = (((d >> 3) ^ (r & 7)) << 3) + (d & 7);
           float M = -INFINITY;
 #pragma unroll
-          for (int w = 0; w < 4; ++w) M = fmaxf(M, sMw[w * QM + qi]);
+          for (int w = 0; w < WPM; ++w) M = fmaxf(M, sMw[(w0 + w) * 16 + r]);
           float o = 0.f, L = 0.f;
           if (M > -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const float f = exp2f(sMw[w * QM + qi] - M);
-              o += red[((size_t)w * QM + qi) * HD + col] * f;
-              L += sLw[w * QM + qi] * f;
+            for (int w = 0; w < WPM; ++w) {
+              const float f = exp2f(sMw[(w0 + w) * 16 + r] - M);
+              o += red[((size_t)(w0 + w) * 16 + r) * HD + col] * f;
+              L += sLw[(w0 + w) * 16 + r] * f;
             }
           }
           const int q = mt.q0 + qi;
@@ -2154,15 +2178,15 @@ static bool kv_maps(const spec_kv& kv, int nkv, int hd, int bh, CUtensorMap* tk,
   return true;
 }
 
-template <int HDV>
+template <int HDV, int MT>
 static spec_status attn_ws_launch(const spec_model_desc& d, const RowInfo& ri, const spec_rows& rows,
                                   const void* qbuf, const spec_kv& kv, float* opart, float2* mlpart, void* attn_out,
                                   int nsplit, int nqg, int* work, void* ws, cudaStream_t st) {
   static int attr_dev = -1, occ = 1;
   int dev = 0;
   cudaGetDevice(&dev);
-  constexpr size_t smem = WsShape<HDV>::kSmem;
-  auto kern = attn_ws_kernel<HDV>;
+  constexpr size_t smem = WsShape<HDV, MT>::kSmem;
+  auto kern = attn_ws_kernel<HDV, MT>;
   if (attr_dev != dev) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return SPEC_ERR_CUDA;
@@ -2206,14 +2230,16 @@ spec_status launch_attention(const spec_model_desc& d, const spec_rows& rows, co
   if (d.dtype == SPEC_DTYPE_BF16) {
     // tensor-core path: 16 or 32 query rows per item (the same groups as qmax <= 16 / 32)
     const bool two = qmax > 16;
-    // warp-specialised kernel with tensor copies: one m-tile, cache blocks of a multiple of 8 slots,
-    // 16-byte aligned caches
-    const bool tma = !two && kv.block_size % 8 == 0 && ((reinterpret_cast<uintptr_t>(kv.k) |
-                                                          reinterpret_cast<uintptr_t>(kv.v)) & 15u) == 0;
+    // warp-specialised kernel with tensor copies: one or two m-tiles, cache blocks of a
+    // multiple of 8 slots, 16-byte aligned caches
+    const bool tma = kv.block_size % 8 == 0 && ((reinterpret_cast<uintptr_t>(kv.k) |
+                                                 reinterpret_cast<uintptr_t>(kv.v)) & 15u) == 0;
     if (tma && d.head_dim == 128)
-      return attn_ws_launch<128>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st);
+      return two ? attn_ws_launch<128, 2>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st)
+                 : attn_ws_launch<128, 1>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st);
     if (tma && d.head_dim == 64)
-      return attn_ws_launch<64>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st);
+      return two ? attn_ws_launch<64, 2>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st)
+                 : attn_ws_launch<64, 1>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st);
     if (d.head_dim == 128)
       s = two ? attn_mma_launch<128, 2>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st)
               : attn_mma_launch<128, 1>(d, ri, rows, qbuf, kv, opart, mlpart, attn_out, nsplit, nqg, work, ws, st);

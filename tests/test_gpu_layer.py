@@ -103,15 +103,26 @@ def test_draft_layer_block_sizes(w):
     no_device_error(dm)
 
 
+LONG_TREE = replace(configs.WORKLOADS["qwen4b_tree"], name="long_tree", H=512, I=1000, V=3000, B=2, ctx=0,
+                    ctx_range=(3000, 4096), seed=28)
+
+
 @pytest.mark.parametrize("w,k", [(SMALL_BF16, 4), (replace(SMALL_BF16_HD128, window=64, ctx=150), 4),
                                  (replace(SMALL_BF16, name="small_bf16_k8"), 8),
-                                 (replace(SMALL_BF16, name="small_bf16_k8_block12", block_size=12), 8)],
-                         ids=["k4", "hd128_window_k4", "k8", "k8_block12"])
+                                 (replace(SMALL_BF16, name="small_bf16_k8_block12", block_size=12), 8),
+                                 (replace(SMALL_BF16_HD128, name="hd128_k8", ctx=333), 8),
+                                 (replace(SMALL_BF16_HD128, name="hd128_k8_window", window=128, ctx=700), 8),
+                                 (replace(SMALL_BF16_HD128, name="hd128_k6", ctx=200), 6),
+                                 (LONG_TREE, 8)],
+                         ids=["k4", "hd128_window_k4", "k8", "k8_block12", "hd128_k8", "hd128_k8_window", "hd128_k6",
+                              "long_tree_32_8_heads"])
 def test_draft_layer_tree_rows(w, k):
     """Frontier-style rows: several rows per request, explicit positions, draft-region
     entries, ancestor masks and gathered hidden inputs (sliding window too).  Eight
-    rows of four q heads are 32 queries per kv head: items of two m-tiles, with
-    16- and 12-slot cache blocks."""
+    rows of four q heads are 32 queries per kv head: items of two m-tiles (six rows:
+    24 queries, the second m-tile half empty), with 16- and 12-slot cache blocks,
+    head dims 64 and 128, and the tree workload's attention shape (32 / 8 heads,
+    contexts of 3000-4096 keys: many tiles per item)."""
     w = replace(w, mode="tree", top_k=k, depth=4, total=12, B=2)
     W, ctx, kv, dm = setup(w, max_rows=w.B * k)
     g = np.random.default_rng(3)
