@@ -143,6 +143,68 @@ struct EpiStore {
   SPEC_DEV void finish(int, int) {}
 };
 
+// order-preserving 32-bit key of a float (larger float, larger key)
+SPEC_DEV uint32_t sort_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Candidate retrieval without writing the outputs: an output (row m, feature n)
+// whose key reaches the row's threshold tau[m] is appended to row m's list
+// (keys and feature ids, cap entries per row; the count keeps growing past cap so
+// the reader sees the overflow).  Row-range schedule: every tile is complete in
+// one CTA, and [lo, hi) keeps the shifted last tile's overlap from being taken twice.
+template <int MPAD>
+struct EpiFilter {
+  struct Params {
+    int M;
+    int cap;
+    const uint32_t* tau;
+    uint32_t* keys;
+    int* ids;
+    int* count;
+  };
+  const Params& P;
+  static constexpr int kScratch = 0;
+  static SPEC_DEV void init(uint8_t*) {}
+  SPEC_DEV EpiFilter(const Params& pp, int, uint8_t*, volatile int*) : P(pp) {}
+  SPEC_DEV bool after(const Seg&, int, int) { return true; }
+  SPEC_DEV bool segment(const Seg& s, uint32_t tb, int warp, int lane) {
+    const int n = s.row0 + warp * 32 + lane;
+    const bool valid = n >= s.lo && n < s.hi;
+#pragma unroll
+    for (int c16 = 0; c16 < MPAD / 16; ++c16) {
+      if (c16 * 16 >= P.M) break;
+      uint32_t r[16];
+      tmem_ld16(tb + (uint32_t)(c16 * 16), r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int m = c16 * 16 + q;
+        if (m >= P.M) break;
+        const uint32_t key = sort_key(__uint_as_float(r[q]));
+        const bool take = valid && key >= __ldg(P.tau + m);
+        const unsigned bal = __ballot_sync(0xffffffffu, take);
+        if (bal != 0u) {
+          const int lead = __ffs(bal) - 1;
+          int base = 0;
+          if (lane == lead) base = atomicAdd(P.count + m, __popc(bal));
+          base = __shfl_sync(0xffffffffu, base, lead);
+          if (take) {
+            const int at = base + __popc(bal & ((1u << lane) - 1u));
+            if (at < P.cap) {
+              P.keys[(size_t)m * P.cap + at] = key;
+              P.ids[(size_t)m * P.cap + at] = n;
+            }
+          }
+        }
+      }
+    }
+    return true;
+  }
+  SPEC_DEV void finish(int, int) {}
+};
+
 // ---------------------------------------------------------------- kernel
 template <int MPAD, class Sched, class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
