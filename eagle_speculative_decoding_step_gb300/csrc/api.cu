@@ -37,13 +37,14 @@ void launch_row_stats(const float*, int, int, int, int32_t*, int, float*, float*
 void launch_topk_select(const float*, int, int, int, int32_t*, cudaStream_t);
 void launch_rescore(int, const void*, const void*, int, int, const int32_t*, int, int, float*, void*, cudaStream_t);
 void launch_cand_best(const float*, const int32_t*, int, int, int, int32_t*, int, float*, cudaStream_t);
-void launch_lr_threshold(const float*, const SKPlan&, int, int, void*, const void*, int, int, uint32_t*, int*,
+void launch_lr_threshold(const float*, const SKPlan&, int, int, void*, const void*, int, int, uint32_t*,
                          cudaStream_t);
-void launch_lr_select(const uint32_t*, const int*, const int*, int, int, int, int, const void*, const void*, float*,
-                      int32_t*, cudaStream_t);
-int lr_list_cap();
+void launch_lr_select(const uint32_t*, const int*, const int*, int, int, int, int, int, const void*, const void*,
+                      float*, int32_t*, cudaStream_t);
+int lr_list_slots();
+int tc_filter_ctas(int N);
 spec_status launch_tc_gemm_filter(const void* W, int N, int K, const void* X, int M, const uint32_t* tau,
-                                  uint32_t* keys, int* ids, int* count, int cap, void* ws, cudaStream_t st);
+                                  uint32_t* keys, int* ids, int* count, int slots, void* ws, cudaStream_t st);
 spec_status launch_lm_head_fused(const spec_model_desc&, const void*, const void*, int, int, int32_t*, int, float*,
                                  float*, const int32_t*, void*, size_t, cudaStream_t);
 size_t lm_fused_ws_bytes(int M, int sms);
@@ -147,13 +148,14 @@ WsLayout ws_layout(const spec_model_desc& d, int M, int /*max_ctx*/, int sms) {
   L.z = take((size_t)M * (r > 0 ? r : 1) * es);
   const int Kc = d.num_candidates > 0 ? d.num_candidates : 1;
   L.cand = take((size_t)M * Kc * 8);
-  // threshold-filtered candidate lists of the bf16 candidate head
-  const bool lr = r > 0 && d.dtype == SPEC_DTYPE_BF16;
-  const size_t cap = lr ? (size_t)lr_list_cap() : 0;
+  // threshold-filtered candidate lists of the bf16 candidate head: one per (CTA of
+  // the score GEMM, epilogue warp, row)
+  const bool lr = r > 0 && d.dtype == SPEC_DTYPE_BF16 && M <= 64;
+  const size_t nlist = lr ? (size_t)4 * tc_filter_ctas(V) * M : 0;
   L.lr_tau = take((size_t)M * 4);
-  L.lr_cnt = take((size_t)M * 4);
-  L.lr_keys = take((size_t)M * cap * 4);
-  L.lr_ids = take((size_t)M * cap * 4);
+  L.lr_cnt = take(nlist * 4);
+  L.lr_keys = take(nlist * lr_list_slots() * 4);
+  L.lr_ids = take(nlist * lr_list_slots() * 4);
   L.total = o;
   return L;
 }
@@ -405,11 +407,12 @@ extern "C" spec_status spec_lowrank_candidates(const spec_model_desc* desc, cons
     int* cnt = at<int>(ws, L.lr_cnt);
     uint32_t* keys = at<uint32_t>(ws, L.lr_keys);
     int* ids = at<int>(ws, L.lr_ids);
-    launch_lr_threshold(part, p, M, d.rank, z, w->lr_up, d.vocab, Kc, tau, cnt, stream);
-    if ((s = launch_tc_gemm_filter(w->lr_up, d.vocab, d.rank, z, M, tau, keys, ids, cnt, lr_list_cap(), ws,
+    launch_lr_threshold(part, p, M, d.rank, z, w->lr_up, d.vocab, Kc, tau, stream);
+    if ((s = launch_tc_gemm_filter(w->lr_up, d.vocab, d.rank, z, M, tau, keys, ids, cnt, lr_list_slots(), ws,
                                    stream)) != SPEC_OK)
       return s;
-    launch_lr_select(keys, ids, cnt, M, d.vocab, Kc, d.rank, z, w->lr_up, sc, cand, stream);
+    launch_lr_select(keys, ids, cnt, 4 * tc_filter_ctas(d.vocab), M, d.vocab, Kc, d.rank, z, w->lr_up, sc, cand,
+                     stream);
     launch_rescore(d.dtype, hn, w->lm_head, d.hidden, d.vocab, cand, M, Kc, exact, ws, stream);
     launch_cand_best(exact, cand, M, Kc, k_out, out_ids, out_ld, out_logprob, stream);
     return last_launch();

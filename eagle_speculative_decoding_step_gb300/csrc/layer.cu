@@ -1971,12 +1971,14 @@ __global__ void __cluster_dims__(kTkCL, 1, 1) __launch_bounds__(1024)
 // The bf16 candidate head retrieves the Kc best low-rank scores of a row
 // without writing the [M, V] score matrix: a threshold per row that about
 // kLrWant scores reach is taken from a systematic sample of the vocabulary,
-// the score GEMM appends every (key, id) at or above it to the row's list as
-// it drains its accumulators, and the list's Kc best are the exact top-Kc as
-// long as the list holds at least Kc entries (every score above the Kc-th is
-// then above the threshold too).  A list shorter than Kc or longer than its
-// capacity sends the row to an exact fallback over recomputed scores.
-constexpr int kLrCap = 8192;        // list entries kept per row
+// the score GEMM keeps every (key, id) at or above it in lists private to each
+// (CTA, epilogue warp, row) as it drains its accumulators, and the lists' Kc
+// best are the exact top-Kc as long as they hold at least Kc entries together
+// (every score above the Kc-th is then above the threshold too).  Lists that
+// hold fewer than Kc, or dropped entries, send the row to an exact fallback
+// over recomputed scores.
+constexpr int kLrCap = 8192;        // entries the selection takes per row
+constexpr int kLrSlots = 32;        // entries per (CTA, epilogue warp, row) list
 constexpr int kLrSample = 2048;     // about this many ids sampled per row
 constexpr int kLrWant = 2048;       // list length the threshold aims at (16 Kc for Kc = 128)
 
@@ -1998,14 +2000,15 @@ inline LrSample lr_sample(int V, int Kc) {
 
 // Row m: z = bf16(sum of the stream-K partials) (the rank-r projection), the
 // sample's scores z . up[v] for v = 0, stride, 2 stride, ..., and the key of
-// their J-th largest as the row's threshold; the row's list count starts at 0.
+// their J-th largest as the row's threshold.
+template <int R8>
 __global__ void __launch_bounds__(512) lr_threshold_kernel(const float* __restrict__ part, SKPlan p, int r,
                                                           __nv_bfloat16* __restrict__ z,
                                                           const __nv_bfloat16* __restrict__ up, LrSample smp,
-                                                          uint32_t* __restrict__ tau, int* __restrict__ count) {
+                                                          uint32_t* __restrict__ tau) {
   pdl_wait();
   pdl_trigger();
-  __shared__ __align__(16) float zs[256];
+  __shared__ __align__(16) float zs[8 * R8];
   __shared__ uint32_t skeys[kLrSample];
   __shared__ int hist[256];
   __shared__ uint32_t s_prefix;
@@ -2018,41 +2021,37 @@ __global__ void __launch_bounds__(512) lr_threshold_kernel(const float* __restri
   }
   __syncthreads();
   for (int i = tid; i < smp.nsub; i += blockDim.x) {
+    // one sampled row of up: all its 16-byte pieces in flight at once
     const uint4* u4 = reinterpret_cast<const uint4*>(up + (size_t)i * smp.stride * r);
+    uint4 q[R8];
+#pragma unroll
+    for (int e = 0; e < R8; ++e) q[e] = __ldg(u4 + e);
     float acc = 0.f;
-    for (int c = 0; c < r / 8; c += 4) {
-      uint4 q[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (c + e < r / 8) q[e] = __ldg(u4 + c + e);
+    for (int e = 0; e < R8; ++e) {
+      float f[8];
+      unpack16<__nv_bfloat16>(q[e], f);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (c + e < r / 8) {
-          float f[8];
-          unpack16<__nv_bfloat16>(q[e], f);
-#pragma unroll
-          for (int t = 0; t < 8; ++t) acc = fmaf(zs[8 * (c + e) + t], f[t], acc);
-        }
+      for (int t = 0; t < 8; ++t) acc = fmaf(zs[8 * e + t], f[t], acc);
     }
     skeys[i] = order_key(acc);
   }
   __syncthreads();
   int tie_need;
   const uint32_t t = radix_select<true>(nullptr, skeys, smp.nsub, smp.J, hist, &s_prefix, &s_need, &tie_need);
-  if (tid == 0) {
-    tau[m] = t;
-    count[m] = 0;
-  }
+  if (tid == 0) tau[m] = t;
 }
 
 size_t lr_select_smem() { return (size_t)kLrCap * 8 + 1024 * 8 + 256 * 4; }
 
-// Row m's Kc best list entries, in descending order (ties to the smaller id).  A
-// list shorter than Kc or past its capacity: the row's scores are recomputed
+// Row m's Kc best list entries, in descending order (ties to the smaller id).
+// nseg = 4 x the filter GEMM's CTAs lists per row, gathered in list order.  Too
+// few entries, or a list that dropped some: the row's scores are recomputed
 // (z . up[v] in fp32) into the scratch row and selected exactly.
 __global__ void __launch_bounds__(1024) lr_select_kernel(const uint32_t* __restrict__ keys,
                                                         const int* __restrict__ ids, const int* __restrict__ count,
-                                                        int V, int Kc, int r, const __nv_bfloat16* __restrict__ z,
+                                                        int nseg, int M, int V, int Kc, int r,
+                                                        const __nv_bfloat16* __restrict__ z,
                                                         const __nv_bfloat16* __restrict__ up,
                                                         float* __restrict__ scratch, int32_t* __restrict__ out_ids) {
   pdl_wait();
@@ -2064,15 +2063,22 @@ __global__ void __launch_bounds__(1024) lr_select_kernel(const uint32_t* __restr
   int* sidx = reinterpret_cast<int*>(skey + 1024);                  // [1024]
   int* hist = sidx + 1024;                                          // [256]
   __shared__ int wsum[32];
-  __shared__ int s_total, s_nsel, s_need, s_tie;
+  __shared__ int s_total, s_nsel, s_need, s_tie, s_over;
   __shared__ uint32_t s_prefix;
   const int m = blockIdx.x, tid = threadIdx.x;
-  const int n = count[m];
-  if (tid == 0) s_nsel = 0;
-  if (n >= Kc && n <= kLrCap) {
-    for (int i = tid; i < n; i += blockDim.x) {
-      gkey[i] = keys[(size_t)m * kLrCap + i];
-      gidx[i] = ids[(size_t)m * kLrCap + i];
+  if (tid == 0) { s_nsel = 0; s_over = 0; }
+  __syncthreads();
+  const int cj = tid < nseg ? count[(size_t)tid * M + m] : 0;
+  if (cj > kLrSlots) s_over = 1;
+  const int off = block_excl_scan(min(cj, kLrSlots), wsum, &s_total);
+  const int n = s_total;
+  if (!s_over && n >= Kc && n <= kLrCap) {
+    if (tid < nseg) {
+      const size_t e0 = ((size_t)tid * M + m) * kLrSlots;
+      for (int i = 0; i < cj; ++i) {
+        gkey[off + i] = keys[e0 + i];
+        gidx[off + i] = ids[e0 + i];
+      }
     }
     __syncthreads();
     select_gathered(gkey, gidx, n, Kc, out_ids + (size_t)m * Kc, skey, sidx, hist, &s_prefix, &s_need, &s_nsel);
@@ -2476,12 +2482,20 @@ void launch_topk_select(const float* s, int M, int V, int Kc, int32_t* out_ids, 
 }
 
 void launch_lr_threshold(const float* part, const SKPlan& p, int M, int r, void* z, const void* up, int V, int Kc,
-                         uint32_t* tau, int* count, cudaStream_t st) {
-  launch_pdl(lr_threshold_kernel, dim3(M), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
-             (const __nv_bfloat16*)up, lr_sample(V, Kc), tau, count);
+                         uint32_t* tau, cudaStream_t st) {
+  const LrSample smp = lr_sample(V, Kc);
+  if (r <= 64)
+    launch_pdl(lr_threshold_kernel<8>, dim3(M), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
+               (const __nv_bfloat16*)up, smp, tau);
+  else if (r <= 128)
+    launch_pdl(lr_threshold_kernel<16>, dim3(M), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
+               (const __nv_bfloat16*)up, smp, tau);
+  else
+    launch_pdl(lr_threshold_kernel<32>, dim3(M), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
+               (const __nv_bfloat16*)up, smp, tau);
 }
 
-void launch_lr_select(const uint32_t* keys, const int* ids, const int* count, int M, int V, int Kc, int r,
+void launch_lr_select(const uint32_t* keys, const int* ids, const int* count, int nseg, int M, int V, int Kc, int r,
                       const void* z, const void* up, float* scratch, int32_t* out_ids, cudaStream_t st) {
   static int attr_dev = -1;
   int dev = 0;
@@ -2490,11 +2504,11 @@ void launch_lr_select(const uint32_t* keys, const int* ids, const int* count, in
     cudaFuncSetAttribute(lr_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lr_select_smem());
     attr_dev = dev;
   }
-  launch_pdl(lr_select_kernel, dim3(M), dim3(1024), lr_select_smem(), st, keys, ids, count, V, Kc, r,
+  launch_pdl(lr_select_kernel, dim3(M), dim3(1024), lr_select_smem(), st, keys, ids, count, nseg, M, V, Kc, r,
              (const __nv_bfloat16*)z, (const __nv_bfloat16*)up, scratch, out_ids);
 }
 
-int lr_list_cap() { return kLrCap; }
+int lr_list_slots() { return kLrSlots; }
 
 void launch_rescore(int dtype, const void* hn, const void* lm_head, int H, int V, const int32_t* cand, int M, int Kc,
                     float* exact, void* ws, cudaStream_t st) {

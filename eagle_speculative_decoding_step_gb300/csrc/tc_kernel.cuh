@@ -150,28 +150,35 @@ SPEC_DEV uint32_t sort_key(float f) {
 }
 
 // Candidate retrieval without writing the outputs: an output (row m, feature n)
-// whose key reaches the row's threshold tau[m] is appended to row m's list
-// (keys and feature ids, cap entries per row; the count keeps growing past cap so
-// the reader sees the overflow).  Row-range schedule: every tile is complete in
-// one CTA, and [lo, hi) keeps the shifted last tile's overlap from being taken twice.
+// whose key reaches the row's threshold tau[m] goes to a list private to (CTA,
+// epilogue warp, row) -- `slots` entries of keys and feature ids -- so no global
+// atomics sit in the drain; each warp keeps its per-row counts in registers
+// (row m's in lane m % 32) and writes them when the CTA is done (a count above
+// `slots` tells the reader that entries were dropped).  Row-range schedule:
+// every tile is complete in one CTA, and [lo, hi) keeps the shifted last tile's
+// overlap from being taken twice.  At most 64 rows.
 template <int MPAD>
 struct EpiFilter {
   struct Params {
     int M;
-    int cap;
+    int slots;
     const uint32_t* tau;
-    uint32_t* keys;
-    int* ids;
-    int* count;
+    uint32_t* keys;      // [G * 4][M][slots]
+    int* ids;            // [G * 4][M][slots]
+    int* count;          // [G * 4][M]
   };
+  static_assert(MPAD <= 64, "rows in two registers per lane");
   const Params& P;
+  int c;
+  int cnt[2];
   static constexpr int kScratch = 0;
   static SPEC_DEV void init(uint8_t*) {}
-  SPEC_DEV EpiFilter(const Params& pp, int, uint8_t*, volatile int*) : P(pp) {}
+  SPEC_DEV EpiFilter(const Params& pp, int cc, uint8_t*, volatile int*) : P(pp), c(cc) { cnt[0] = cnt[1] = 0; }
   SPEC_DEV bool after(const Seg&, int, int) { return true; }
   SPEC_DEV bool segment(const Seg& s, uint32_t tb, int warp, int lane) {
     const int n = s.row0 + warp * 32 + lane;
     const bool valid = n >= s.lo && n < s.hi;
+    const size_t region = (size_t)(c * 4 + warp) * P.M;
 #pragma unroll
     for (int c16 = 0; c16 < MPAD / 16; ++c16) {
       if (c16 * 16 >= P.M) break;
@@ -182,19 +189,17 @@ struct EpiFilter {
       for (int q = 0; q < 16; ++q) {
         const int m = c16 * 16 + q;
         if (m >= P.M) break;
-        const uint32_t key = sort_key(__uint_as_float(r[q]));
-        const bool take = valid && key >= __ldg(P.tau + m);
+        const bool take = valid && sort_key(__uint_as_float(r[q])) >= __ldg(P.tau + m);
         const unsigned bal = __ballot_sync(0xffffffffu, take);
         if (bal != 0u) {
-          const int lead = __ffs(bal) - 1;
-          int base = 0;
-          if (lane == lead) base = atomicAdd(P.count + m, __popc(bal));
-          base = __shfl_sync(0xffffffffu, base, lead);
+          const int base = __shfl_sync(0xffffffffu, cnt[m >> 5], m & 31);
+          if (lane == (m & 31)) cnt[m >> 5] += __popc(bal);
           if (take) {
             const int at = base + __popc(bal & ((1u << lane) - 1u));
-            if (at < P.cap) {
-              P.keys[(size_t)m * P.cap + at] = key;
-              P.ids[(size_t)m * P.cap + at] = n;
+            if (at < P.slots) {
+              const size_t e = (region + m) * P.slots + at;
+              P.keys[e] = sort_key(__uint_as_float(r[q]));
+              P.ids[e] = n;
             }
           }
         }
@@ -202,7 +207,11 @@ struct EpiFilter {
     }
     return true;
   }
-  SPEC_DEV void finish(int, int) {}
+  SPEC_DEV void finish(int warp, int lane) {
+    const size_t region = (size_t)(c * 4 + warp) * P.M;
+    if (lane < P.M) P.count[region + lane] = cnt[0];
+    if (lane + 32 < P.M) P.count[region + lane + 32] = cnt[1];
+  }
 };
 
 // ---------------------------------------------------------------- kernel
