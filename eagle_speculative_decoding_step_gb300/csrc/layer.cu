@@ -1998,14 +1998,16 @@ inline LrSample lr_sample(int V, int Kc) {
   return s;
 }
 
-// Row m: z = bf16(sum of the stream-K partials) (the rank-r projection), the
-// sample's scores z . up[v] for v = 0, stride, 2 stride, ..., and the key of
-// their J-th largest as the row's threshold.
+// Row m, on a cluster of kLrCL CTAs: z = bf16(sum of the stream-K partials)
+// (the rank-r projection; every CTA sums it, rank 0 stores it), each CTA scores
+// its part of the sample z . up[v] for v = 0, stride, 2 stride, ..., and rank 0
+// takes the key of their J-th largest as the row's threshold.
+constexpr int kLrCL = 4;
+
 template <int R8>
-__global__ void __launch_bounds__(512) lr_threshold_kernel(const float* __restrict__ part, SKPlan p, int r,
-                                                          __nv_bfloat16* __restrict__ z,
-                                                          const __nv_bfloat16* __restrict__ up, LrSample smp,
-                                                          uint32_t* __restrict__ tau) {
+__global__ void __cluster_dims__(kLrCL, 1, 1) __launch_bounds__(512)
+    lr_threshold_kernel(const float* __restrict__ part, SKPlan p, int r, __nv_bfloat16* __restrict__ z,
+                        const __nv_bfloat16* __restrict__ up, LrSample smp, uint32_t* __restrict__ tau) {
   pdl_wait();
   pdl_trigger();
   __shared__ __align__(16) float zs[8 * R8];
@@ -2013,14 +2015,17 @@ __global__ void __launch_bounds__(512) lr_threshold_kernel(const float* __restri
   __shared__ int hist[256];
   __shared__ uint32_t s_prefix;
   __shared__ int s_need;
-  const int m = blockIdx.x, tid = threadIdx.x;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
+  const int m = blockIdx.x / kLrCL, tid = threadIdx.x;
   for (int n = tid; n < r; n += blockDim.x) {
     const __nv_bfloat16 b = __float2bfloat16_rn(sk_sum(part, p, m, n));
-    z[(size_t)m * r + n] = b;
+    if (rank == 0) z[(size_t)m * r + n] = b;
     zs[n] = __bfloat162float(b);
   }
   __syncthreads();
-  for (int i = tid; i < smp.nsub; i += blockDim.x) {
+  const int i0 = (int)((long long)rank * smp.nsub / kLrCL), i1 = (int)((long long)(rank + 1) * smp.nsub / kLrCL);
+  for (int i = i0 + tid; i < i1; i += blockDim.x) {
     // one sampled row of up: all its 16-byte pieces in flight at once
     const uint4* u4 = reinterpret_cast<const uint4*>(up + (size_t)i * smp.stride * r);
     uint4 q[R8];
@@ -2036,10 +2041,19 @@ __global__ void __launch_bounds__(512) lr_threshold_kernel(const float* __restri
     }
     skeys[i] = order_key(acc);
   }
-  __syncthreads();
-  int tie_need;
-  const uint32_t t = radix_select<true>(nullptr, skeys, smp.nsub, smp.J, hist, &s_prefix, &s_need, &tie_need);
-  if (tid == 0) tau[m] = t;
+  cl.sync();                  // every CTA's sample keys are final
+  if (rank == 0) {
+    for (int q = 1; q < kLrCL; ++q) {
+      const uint32_t* rk = cl.map_shared_rank(skeys, q);
+      const int a = (int)((long long)q * smp.nsub / kLrCL), b = (int)((long long)(q + 1) * smp.nsub / kLrCL);
+      for (int i = a + tid; i < b; i += blockDim.x) skeys[i] = rk[i];
+    }
+    __syncthreads();
+    int tie_need;
+    const uint32_t t = radix_select<true>(nullptr, skeys, smp.nsub, smp.J, hist, &s_prefix, &s_need, &tie_need);
+    if (tid == 0) tau[m] = t;
+  }
+  cl.sync();                  // no CTA leaves while rank 0 may still read its keys
 }
 
 size_t lr_select_smem() { return (size_t)kLrCap * 8 + 1024 * 8 + 256 * 4; }
@@ -2075,6 +2089,7 @@ __global__ void __launch_bounds__(1024) lr_select_kernel(const uint32_t* __restr
   if (!s_over && n >= Kc && n <= kLrCap) {
     if (tid < nseg) {
       const size_t e0 = ((size_t)tid * M + m) * kLrSlots;
+#pragma unroll 4
       for (int i = 0; i < cj; ++i) {
         gkey[off + i] = keys[e0 + i];
         gidx[off + i] = ids[e0 + i];
@@ -2485,13 +2500,13 @@ void launch_lr_threshold(const float* part, const SKPlan& p, int M, int r, void*
                          uint32_t* tau, cudaStream_t st) {
   const LrSample smp = lr_sample(V, Kc);
   if (r <= 64)
-    launch_pdl(lr_threshold_kernel<8>, dim3(M), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
+    launch_pdl(lr_threshold_kernel<8>, dim3(M * kLrCL), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
                (const __nv_bfloat16*)up, smp, tau);
   else if (r <= 128)
-    launch_pdl(lr_threshold_kernel<16>, dim3(M), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
+    launch_pdl(lr_threshold_kernel<16>, dim3(M * kLrCL), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
                (const __nv_bfloat16*)up, smp, tau);
   else
-    launch_pdl(lr_threshold_kernel<32>, dim3(M), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
+    launch_pdl(lr_threshold_kernel<32>, dim3(M * kLrCL), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
                (const __nv_bfloat16*)up, smp, tau);
 }
 

@@ -170,37 +170,51 @@ struct EpiFilter {
   static_assert(MPAD <= 64, "rows in two registers per lane");
   const Params& P;
   int c;
-  int cnt[2];
+  int cnt0, cnt1;        // this warp's list lengths of rows (lane) and (lane + 32), in lane order
+  uint32_t tau0, tau1;   // thresholds of rows (lane) and (lane + 32)
   static constexpr int kScratch = 0;
   static SPEC_DEV void init(uint8_t*) {}
-  SPEC_DEV EpiFilter(const Params& pp, int cc, uint8_t*, volatile int*) : P(pp), c(cc) { cnt[0] = cnt[1] = 0; }
+  SPEC_DEV EpiFilter(const Params& pp, int cc, uint8_t*, volatile int*) : P(pp), c(cc), cnt0(0), cnt1(0) {
+    const int lane = threadIdx.x & 31;
+    tau0 = lane < P.M ? P.tau[lane] : 0xffffffffu;
+    tau1 = lane + 32 < P.M ? P.tau[lane + 32] : 0xffffffffu;
+  }
   SPEC_DEV bool after(const Seg&, int, int) { return true; }
   SPEC_DEV bool segment(const Seg& s, uint32_t tb, int warp, int lane) {
     const int n = s.row0 + warp * 32 + lane;
     const bool valid = n >= s.lo && n < s.hi;
     const size_t region = (size_t)(c * 4 + warp) * P.M;
+    // all of the tile's columns in flight at once, then one wait
+    uint32_t r[MPAD];
+#pragma unroll
+    for (int c16 = 0; c16 < MPAD / 16; ++c16) tmem_ld16(tb + (uint32_t)(c16 * 16), r + 16 * c16);
+    tmem_ld_wait();
 #pragma unroll
     for (int c16 = 0; c16 < MPAD / 16; ++c16) {
       if (c16 * 16 >= P.M) break;
-      uint32_t r[16];
-      tmem_ld16(tb + (uint32_t)(c16 * 16), r);
-      tmem_ld_wait();
+      // sixteen rows' take flags and ballots, independent of each other
+      unsigned bal[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
         const int m = c16 * 16 + q;
-        if (m >= P.M) break;
-        const bool take = valid && sort_key(__uint_as_float(r[q])) >= __ldg(P.tau + m);
-        const unsigned bal = __ballot_sync(0xffffffffu, take);
-        if (bal != 0u) {
-          const int base = __shfl_sync(0xffffffffu, cnt[m >> 5], m & 31);
-          if (lane == (m & 31)) cnt[m >> 5] += __popc(bal);
-          if (take) {
-            const int at = base + __popc(bal & ((1u << lane) - 1u));
-            if (at < P.slots) {
-              const size_t e = (region + m) * P.slots + at;
-              P.keys[e] = sort_key(__uint_as_float(r[q]));
-              P.ids[e] = n;
-            }
+        const uint32_t t = __shfl_sync(0xffffffffu, m < 32 ? tau0 : tau1, m & 31);
+        bal[q] = __ballot_sync(0xffffffffu, valid && m < P.M && sort_key(__uint_as_float(r[m])) >= t);
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        if (bal[q] == 0u) continue;
+        const int m = c16 * 16 + q;
+        const int base = __shfl_sync(0xffffffffu, m < 32 ? cnt0 : cnt1, m & 31);
+        if (lane == (m & 31)) {
+          if (m < 32) cnt0 += __popc(bal[q]);
+          else cnt1 += __popc(bal[q]);
+        }
+        if ((bal[q] >> lane) & 1u) {
+          const int at = base + __popc(bal[q] & ((1u << lane) - 1u));
+          if (at < P.slots) {
+            const size_t e = (region + m) * P.slots + at;
+            P.keys[e] = sort_key(__uint_as_float(r[m]));
+            P.ids[e] = n;
           }
         }
       }
@@ -209,8 +223,8 @@ struct EpiFilter {
   }
   SPEC_DEV void finish(int warp, int lane) {
     const size_t region = (size_t)(c * 4 + warp) * P.M;
-    if (lane < P.M) P.count[region + lane] = cnt[0];
-    if (lane + 32 < P.M) P.count[region + lane + 32] = cnt[1];
+    if (lane < P.M) P.count[region + lane] = cnt0;
+    if (lane + 32 < P.M) P.count[region + lane + 32] = cnt1;
   }
 };
 
