@@ -37,14 +37,6 @@ void launch_row_stats(const float*, int, int, int, int32_t*, int, float*, float*
 void launch_topk_select(const float*, int, int, int, int32_t*, cudaStream_t);
 void launch_rescore(int, const void*, const void*, int, int, const int32_t*, int, int, float*, void*, cudaStream_t);
 void launch_cand_best(const float*, const int32_t*, int, int, int, int32_t*, int, float*, cudaStream_t);
-void launch_lr_threshold(const float*, const SKPlan&, int, int, void*, const void*, int, int, uint32_t*,
-                         cudaStream_t);
-void launch_lr_select(const uint32_t*, const int*, const int*, int, int, int, int, int, const void*, const void*,
-                      float*, int32_t*, cudaStream_t);
-int lr_list_slots();
-int tc_filter_ctas(int N);
-spec_status launch_tc_gemm_filter(const void* W, int N, int K, const void* X, int M, const uint32_t* tau,
-                                  uint32_t* keys, int* ids, int* count, int slots, void* ws, cudaStream_t st);
 spec_status launch_lm_head_fused(const spec_model_desc&, const void*, const void*, int, int, int32_t*, int, float*,
                                  float*, const int32_t*, void*, size_t, cudaStream_t);
 size_t lm_fused_ws_bytes(int M, int sms);
@@ -148,14 +140,6 @@ WsLayout ws_layout(const spec_model_desc& d, int M, int /*max_ctx*/, int sms) {
   L.z = take((size_t)M * (r > 0 ? r : 1) * es);
   const int Kc = d.num_candidates > 0 ? d.num_candidates : 1;
   L.cand = take((size_t)M * Kc * 8);
-  // threshold-filtered candidate lists of the bf16 candidate head: one per (CTA of
-  // the score GEMM, epilogue warp, row)
-  const bool lr = r > 0 && d.dtype == SPEC_DTYPE_BF16 && M <= 64;
-  const size_t nlist = lr ? (size_t)4 * tc_filter_ctas(V) * M : 0;
-  L.lr_tau = take((size_t)M * 4);
-  L.lr_cnt = take(nlist * 4);
-  L.lr_keys = take(nlist * lr_list_slots() * 4);
-  L.lr_ids = take(nlist * lr_list_slots() * 4);
   L.total = o;
   return L;
 }
@@ -399,24 +383,6 @@ extern "C" spec_status spec_lowrank_candidates(const spec_model_desc* desc, cons
   float* exact = cand_logits ? cand_logits : reinterpret_cast<float*>(at<int32_t>(ws, L.cand) + (size_t)M * Kc);
   SKPlan p;
   if ((s = gemm(d, {w->lr_down}, {d.rank}, d.hidden, hn, M, part, ws, stream, &p)) != SPEC_OK) return s;
-  if (d.dtype == SPEC_DTYPE_BF16 && d.rank <= 256 && M <= 64) {
-    // candidates straight from the score GEMM's accumulators, no score matrix: z and
-    // a per-row threshold from a vocabulary sample, the GEMM keeps the scores at or
-    // above it, an exact selection of the Kc best among those
-    uint32_t* tau = at<uint32_t>(ws, L.lr_tau);
-    int* cnt = at<int>(ws, L.lr_cnt);
-    uint32_t* keys = at<uint32_t>(ws, L.lr_keys);
-    int* ids = at<int>(ws, L.lr_ids);
-    launch_lr_threshold(part, p, M, d.rank, z, w->lr_up, d.vocab, Kc, tau, stream);
-    if ((s = launch_tc_gemm_filter(w->lr_up, d.vocab, d.rank, z, M, tau, keys, ids, cnt, lr_list_slots(), ws,
-                                   stream)) != SPEC_OK)
-      return s;
-    launch_lr_select(keys, ids, cnt, 4 * tc_filter_ctas(d.vocab), M, d.vocab, Kc, d.rank, z, w->lr_up, sc, cand,
-                     stream);
-    launch_rescore(d.dtype, hn, w->lm_head, d.hidden, d.vocab, cand, M, Kc, exact, ws, stream);
-    launch_cand_best(exact, cand, M, Kc, k_out, out_ids, out_ld, out_logprob, stream);
-    return last_launch();
-  }
   launch_epi_store(d.dtype, part, p, M, d.rank, z, d.rank, stream);
   if (d.dtype == SPEC_DTYPE_BF16) {
     if ((s = launch_tc_gemm_store(w->lr_up, d.vocab, d.rank, z, M, sc, d.vocab, ws, stream)) != SPEC_OK) return s;

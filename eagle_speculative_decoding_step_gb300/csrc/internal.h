@@ -39,8 +39,7 @@ size_t plan_partial_bytes(const SKPlan& p);
 
 // Bytes of the workspace regions of the draft-layer / head entry points.
 struct WsLayout {
-  size_t err, x, q, attn_part, attn_work, attn, r1, n, act, part, lm_part, logits, z, cand, lr_tau, lr_cnt, lr_keys,
-      lr_ids, total;
+  size_t err, x, q, attn_part, attn_work, attn, r1, n, act, part, lm_part, logits, z, cand, total;
   int attn_splits;
 };
 WsLayout ws_layout(const spec_model_desc& d, int max_rows, int max_ctx, int sms);

@@ -1710,69 +1710,6 @@ SPEC_DEV void select_row_exact(const float* x, int V, int Kc, uint32_t* skey, in
   }
 }
 
-// The Kc best of n gathered (key, id) pairs in shared memory gkey / gidx (n <=
-// blockDim.x: each pair's rank among them is its output position; otherwise an
-// exact radix selection, ties by id, then a bitonic sort).  gkey / gidx have room
-// for n rounded up to 8; skey / sidx for blockDim.x entries.  Block-wide.
-SPEC_DEV void select_gathered(uint32_t* gkey, int* gidx, int n, int Kc, int32_t* out, uint32_t* skey, int* sidx,
-                              int* hist, uint32_t* s_prefix, int* s_need, int* s_nsel) {
-  const int tid = threadIdx.x;
-  if (n <= (int)blockDim.x) {
-    uint32_t k = tid < n ? gkey[tid] : 0u;
-    int id = tid < n ? gidx[tid] : 0x7fffffff;
-    const int tpad = (n + 7) & ~7;
-    __syncthreads();
-    // pad to a multiple of 8 with entries that never rank above a pair (key 0, id max)
-    if (tid >= n && tid < tpad) {
-      gkey[tid] = 0u;
-      gidx[tid] = 0x7fffffff;
-    }
-    __syncthreads();
-    if (tid < n) {
-      const uint4* k4 = reinterpret_cast<const uint4*>(gkey);
-      const int4* i4 = reinterpret_cast<const int4*>(gidx);
-      int r0 = 0, r1 = 0;
-      int j = 0;
-      for (; j + 1 < tpad / 4; j += 2) {
-        const uint4 ka = k4[j], kb = k4[j + 1];
-        const int4 ia = i4[j], ib = i4[j + 1];
-        r0 += (ka.x > k || (ka.x == k && ia.x < id)) + (ka.y > k || (ka.y == k && ia.y < id)) +
-              (ka.z > k || (ka.z == k && ia.z < id)) + (ka.w > k || (ka.w == k && ia.w < id));
-        r1 += (kb.x > k || (kb.x == k && ib.x < id)) + (kb.y > k || (kb.y == k && ib.y < id)) +
-              (kb.z > k || (kb.z == k && ib.z < id)) + (kb.w > k || (kb.w == k && ib.w < id));
-      }
-      if (j < tpad / 4) {
-        const uint4 ka = k4[j];
-        const int4 ia = i4[j];
-        r0 += (ka.x > k || (ka.x == k && ia.x < id)) + (ka.y > k || (ka.y == k && ia.y < id)) +
-              (ka.z > k || (ka.z == k && ia.z < id)) + (ka.w > k || (ka.w == k && ia.w < id));
-      }
-      const int rnk = r0 + r1;
-      if (rnk < Kc) out[rnk] = id;
-    }
-    return;
-  }
-  int tie_need;
-  const uint32_t kth = radix_select<true>(nullptr, gkey, n, Kc, hist, s_prefix, s_need, &tie_need);
-  for (int i = tid; i < n; i += blockDim.x) {
-    const uint32_t k = gkey[i];
-    bool take = k > kth;
-    if (k == kth) {
-      const int id = gidx[i];
-      int rnk = 0;
-      for (int j = 0; j < n; ++j) rnk += (gkey[j] == kth && gidx[j] < id);
-      take = rnk < tie_need;
-    }
-    if (take) {
-      const int p = atomicAdd(s_nsel, 1);
-      skey[p] = k;
-      sidx[p] = gidx[i];
-    }
-  }
-  __syncthreads();
-  sort_selected(skey, sidx, Kc, out);
-}
-
 __global__ void __cluster_dims__(kTkCL, 1, 1) __launch_bounds__(1024)
     topk_select_kernel(const float* __restrict__ s, int V, int Kc, int32_t* __restrict__ out_ids) {
   pdl_wait();
@@ -1965,154 +1902,6 @@ __global__ void __cluster_dims__(kTkCL, 1, 1) __launch_bounds__(1024)
     }
   }
   cl.sync();                  // no CTA leaves while rank 0 may still read its copies
-}
-
-// ---------------------------------------------------------------- candidate retrieval by threshold
-// The bf16 candidate head retrieves the Kc best low-rank scores of a row
-// without writing the [M, V] score matrix: a threshold per row that about
-// kLrWant scores reach is taken from a systematic sample of the vocabulary,
-// the score GEMM keeps every (key, id) at or above it in lists private to each
-// (CTA, epilogue warp, row) as it drains its accumulators, and the lists' Kc
-// best are the exact top-Kc as long as they hold at least Kc entries together
-// (every score above the Kc-th is then above the threshold too).  Lists that
-// hold fewer than Kc, or dropped entries, send the row to an exact fallback
-// over recomputed scores.
-constexpr int kLrCap = 8192;        // entries the selection takes per row
-constexpr int kLrSlots = 32;        // entries per (CTA, epilogue warp, row) list
-constexpr int kLrSample = 2048;     // about this many ids sampled per row
-constexpr int kLrWant = 2048;       // list length the threshold aims at (16 Kc for Kc = 128)
-
-struct LrSample {
-  int stride, nsub, J;
-};
-inline LrSample lr_sample(int V, int Kc) {
-  LrSample s;
-  s.stride = (V + kLrSample - 1) / kLrSample;
-  s.nsub = (V + s.stride - 1) / s.stride;
-  int want = std::max(kLrWant, 16 * Kc);
-  want = std::min(want, kLrCap / 2);
-  want = std::min(want, V);
-  // the J-th largest of nsub samples: about V * J / nsub scores reach it
-  s.J = (int)std::min<long long>(s.nsub, ((long long)want * s.nsub + V - 1) / V);
-  if (s.J < 1) s.J = 1;
-  return s;
-}
-
-// Row m, on a cluster of kLrCL CTAs: z = bf16(sum of the stream-K partials)
-// (the rank-r projection; every CTA sums it, rank 0 stores it), each CTA scores
-// its part of the sample z . up[v] for v = 0, stride, 2 stride, ..., and rank 0
-// takes the key of their J-th largest as the row's threshold.
-constexpr int kLrCL = 4;
-
-template <int R8>
-__global__ void __cluster_dims__(kLrCL, 1, 1) __launch_bounds__(512)
-    lr_threshold_kernel(const float* __restrict__ part, SKPlan p, int r, __nv_bfloat16* __restrict__ z,
-                        const __nv_bfloat16* __restrict__ up, LrSample smp, uint32_t* __restrict__ tau) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ __align__(16) float zs[8 * R8];
-  __shared__ uint32_t skeys[kLrSample];
-  __shared__ int hist[256];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
-  cg::cluster_group cl = cg::this_cluster();
-  const int rank = (int)cl.block_rank();
-  const int m = blockIdx.x / kLrCL, tid = threadIdx.x;
-  for (int n = tid; n < r; n += blockDim.x) {
-    const __nv_bfloat16 b = __float2bfloat16_rn(sk_sum(part, p, m, n));
-    if (rank == 0) z[(size_t)m * r + n] = b;
-    zs[n] = __bfloat162float(b);
-  }
-  __syncthreads();
-  const int i0 = (int)((long long)rank * smp.nsub / kLrCL), i1 = (int)((long long)(rank + 1) * smp.nsub / kLrCL);
-  for (int i = i0 + tid; i < i1; i += blockDim.x) {
-    // one sampled row of up: all its 16-byte pieces in flight at once
-    const uint4* u4 = reinterpret_cast<const uint4*>(up + (size_t)i * smp.stride * r);
-    uint4 q[R8];
-#pragma unroll
-    for (int e = 0; e < R8; ++e) q[e] = __ldg(u4 + e);
-    float acc = 0.f;
-#pragma unroll
-    for (int e = 0; e < R8; ++e) {
-      float f[8];
-      unpack16<__nv_bfloat16>(q[e], f);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) acc = fmaf(zs[8 * e + t], f[t], acc);
-    }
-    skeys[i] = order_key(acc);
-  }
-  cl.sync();                  // every CTA's sample keys are final
-  if (rank == 0) {
-    for (int q = 1; q < kLrCL; ++q) {
-      const uint32_t* rk = cl.map_shared_rank(skeys, q);
-      const int a = (int)((long long)q * smp.nsub / kLrCL), b = (int)((long long)(q + 1) * smp.nsub / kLrCL);
-      for (int i = a + tid; i < b; i += blockDim.x) skeys[i] = rk[i];
-    }
-    __syncthreads();
-    int tie_need;
-    const uint32_t t = radix_select<true>(nullptr, skeys, smp.nsub, smp.J, hist, &s_prefix, &s_need, &tie_need);
-    if (tid == 0) tau[m] = t;
-  }
-  cl.sync();                  // no CTA leaves while rank 0 may still read its keys
-}
-
-size_t lr_select_smem() { return (size_t)kLrCap * 8 + 1024 * 8 + 256 * 4; }
-
-// Row m's Kc best list entries, in descending order (ties to the smaller id).
-// nseg = 4 x the filter GEMM's CTAs lists per row, gathered in list order.  Too
-// few entries, or a list that dropped some: the row's scores are recomputed
-// (z . up[v] in fp32) into the scratch row and selected exactly.
-__global__ void __launch_bounds__(1024) lr_select_kernel(const uint32_t* __restrict__ keys,
-                                                        const int* __restrict__ ids, const int* __restrict__ count,
-                                                        int nseg, int M, int V, int Kc, int r,
-                                                        const __nv_bfloat16* __restrict__ z,
-                                                        const __nv_bfloat16* __restrict__ up,
-                                                        float* __restrict__ scratch, int32_t* __restrict__ out_ids) {
-  pdl_wait();
-  pdl_trigger();
-  extern __shared__ __align__(16) uint8_t lr_smem[];
-  uint32_t* gkey = reinterpret_cast<uint32_t*>(lr_smem);          // [kLrCap]
-  int* gidx = reinterpret_cast<int*>(gkey + kLrCap);                // [kLrCap]
-  uint32_t* skey = reinterpret_cast<uint32_t*>(gidx + kLrCap);      // [1024]
-  int* sidx = reinterpret_cast<int*>(skey + 1024);                  // [1024]
-  int* hist = sidx + 1024;                                          // [256]
-  __shared__ int wsum[32];
-  __shared__ int s_total, s_nsel, s_need, s_tie, s_over;
-  __shared__ uint32_t s_prefix;
-  const int m = blockIdx.x, tid = threadIdx.x;
-  if (tid == 0) { s_nsel = 0; s_over = 0; }
-  __syncthreads();
-  const int cj = tid < nseg ? count[(size_t)tid * M + m] : 0;
-  if (cj > kLrSlots) s_over = 1;
-  const int off = block_excl_scan(min(cj, kLrSlots), wsum, &s_total);
-  const int n = s_total;
-  if (!s_over && n >= Kc && n <= kLrCap) {
-    if (tid < nseg) {
-      const size_t e0 = ((size_t)tid * M + m) * kLrSlots;
-#pragma unroll 4
-      for (int i = 0; i < cj; ++i) {
-        gkey[off + i] = keys[e0 + i];
-        gidx[off + i] = ids[e0 + i];
-      }
-    }
-    __syncthreads();
-    select_gathered(gkey, gidx, n, Kc, out_ids + (size_t)m * Kc, skey, sidx, hist, &s_prefix, &s_need, &s_nsel);
-    return;
-  }
-  // fallback: the whole row's scores, then the exact selection over them
-  float* x = scratch + (size_t)m * V;
-  const __nv_bfloat16* zr = z + (size_t)m * r;
-  for (int v = tid; v < V; v += blockDim.x) {
-    const __nv_bfloat16* u = up + (size_t)v * r;
-    float acc = 0.f;
-    for (int k = 0; k < r; ++k) acc = fmaf(__bfloat162float(zr[k]), __bfloat162float(u[k]), acc);
-    x[v] = acc;
-  }
-  __threadfence_block();
-  __syncthreads();
-  select_row_exact(x, V, Kc, skey, sidx, hist, wsum, &s_prefix, &s_need, &s_tie, &s_total, &s_nsel);
-  __syncthreads();
-  sort_selected(skey, sidx, Kc, out_ids + (size_t)m * Kc);
 }
 
 // exact logits of the candidates: lm_head[cand] . hn[m]; one warp per candidate
@@ -2495,35 +2284,6 @@ void launch_topk_select(const float* s, int M, int V, int Kc, int32_t* out_ids, 
   }
   launch_pdl(topk_select_kernel, dim3(M * kTkCL), dim3(1024), topk_select_smem(), st, s, V, Kc, out_ids);
 }
-
-void launch_lr_threshold(const float* part, const SKPlan& p, int M, int r, void* z, const void* up, int V, int Kc,
-                         uint32_t* tau, cudaStream_t st) {
-  const LrSample smp = lr_sample(V, Kc);
-  if (r <= 64)
-    launch_pdl(lr_threshold_kernel<8>, dim3(M * kLrCL), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
-               (const __nv_bfloat16*)up, smp, tau);
-  else if (r <= 128)
-    launch_pdl(lr_threshold_kernel<16>, dim3(M * kLrCL), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
-               (const __nv_bfloat16*)up, smp, tau);
-  else
-    launch_pdl(lr_threshold_kernel<32>, dim3(M * kLrCL), dim3(512), 0, st, part, p, r, (__nv_bfloat16*)z,
-               (const __nv_bfloat16*)up, smp, tau);
-}
-
-void launch_lr_select(const uint32_t* keys, const int* ids, const int* count, int nseg, int M, int V, int Kc, int r,
-                      const void* z, const void* up, float* scratch, int32_t* out_ids, cudaStream_t st) {
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev) {
-    cudaFuncSetAttribute(lr_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lr_select_smem());
-    attr_dev = dev;
-  }
-  launch_pdl(lr_select_kernel, dim3(M), dim3(1024), lr_select_smem(), st, keys, ids, count, nseg, M, V, Kc, r,
-             (const __nv_bfloat16*)z, (const __nv_bfloat16*)up, scratch, out_ids);
-}
-
-int lr_list_slots() { return kLrSlots; }
 
 void launch_rescore(int dtype, const void* hn, const void* lm_head, int H, int V, const int32_t* cand, int M, int Kc,
                     float* exact, void* ws, cudaStream_t st) {

@@ -156,45 +156,3 @@ spec_status launch_tc_gemm_store(const void* W, int N, int K, const void* X, int
 }
 
 }  // namespace spec
-
-namespace spec {
-
-// CTAs of the filtered score GEMM over N weight rows (one row range each)
-int tc_filter_ctas(int N) {
-  int G = sm_count();
-  if (G > (N + 127) / 128) G = (N + 127) / 128;
-  return G;
-}
-
-// Rows of X[M, K] @ W[N, K]^T filtered on the fly: (m, n) with key(out) >= tau[m]
-// go to the lists of row m (see EpiFilter, `slots` entries per CTA, warp and
-// row); nothing else is written.
-spec_status launch_tc_gemm_filter(const void* W, int N, int K, const void* X, int M, const uint32_t* tau,
-                                  uint32_t* keys, int* ids, int* count, int slots, void* ws, cudaStream_t st) {
-  using namespace tc;
-  if (M < 1 || M > 64 || K % 8 != 0) return SPEC_ERR_SHAPE;
-  if (!aligned(W, 16) || !aligned(X, 16)) return SPEC_ERR_ALIGN;
-  const int mpad = tc_mpad(M);
-  const int G = tc_filter_ctas(N);
-  CUtensorMap a[3];
-  if (!make_map(&a[0], W, N, K, 128)) return SPEC_ERR_CUDA;
-  a[1] = a[0];
-  a[2] = a[0];
-  CUtensorMap b;
-  if (!make_map(&b, X, M, K, bbox_rows(mpad))) return SPEC_ERR_CUDA;
-  RowsParams rp{N, G, (K + kBK - 1) / kBK};
-  switch (mpad) {
-#define FILTER_CASE(MP)                                                                         \
-  case MP: {                                                                                    \
-    typename EpiFilter<MP>::Params ep{M, slots, tau, keys, ids, count};                         \
-    return launch_tc<MP, SchedRows, EpiFilter<MP>>(a, b, rp, ep, G, 0, ws, st);                 \
-  }
-    FILTER_CASE(16)
-    FILTER_CASE(32)
-    FILTER_CASE(64)
-#undef FILTER_CASE
-    default: return SPEC_ERR_SHAPE;
-  }
-}
-
-}  // namespace spec

@@ -90,15 +90,19 @@ struct EpiPartial {
   SPEC_DEV bool after(const Seg&, int, int) { return true; }
   SPEC_DEV bool segment(const Seg& s, uint32_t tb, int warp, int lane) {
     float* dst = P.part + sk_slot(P.p, c, s.idx) + warp * 32 + lane;
+    // up to 64 accumulator columns in flight before one wait
+    constexpr int CB = MPAD < 64 ? MPAD : 64;
 #pragma unroll
-    for (int c16 = 0; c16 < MPAD / 16; ++c16) {
-      if (c16 * 16 >= P.M) break;
-      uint32_t r[16];
-      tmem_ld16(tb + (uint32_t)(c16 * 16), r);
+    for (int cb = 0; cb < MPAD; cb += CB) {
+      if (cb >= P.M) break;
+      uint32_t r[CB];
+#pragma unroll
+      for (int c16 = 0; c16 < CB / 16; ++c16)
+        if (cb + c16 * 16 < P.M) tmem_ld16(tb + (uint32_t)(cb + c16 * 16), r + 16 * c16);
       tmem_ld_wait();
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int m = c16 * 16 + q;
+      for (int q = 0; q < CB; ++q) {
+        const int m = cb + q;
         if (m < P.M) dst[(size_t)m * 128] = __uint_as_float(r[q]);
       }
     }
@@ -124,16 +128,20 @@ struct EpiStore {
   SPEC_DEV bool segment(const Seg& s, uint32_t tb, int warp, int lane) {
     const int n = s.row0 + warp * 32 + lane;
     const bool valid = n >= s.lo && n < s.hi;
+    // up to 64 accumulator columns in flight before one wait
+    constexpr int CB = MPAD < 64 ? MPAD : 64;
 #pragma unroll
-    for (int c16 = 0; c16 < MPAD / 16; ++c16) {
-      if (c16 * 16 >= P.M) break;
-      uint32_t r[16];
-      tmem_ld16(tb + (uint32_t)(c16 * 16), r);
+    for (int cb = 0; cb < MPAD; cb += CB) {
+      if (cb >= P.M) break;
+      uint32_t r[CB];
+#pragma unroll
+      for (int c16 = 0; c16 < CB / 16; ++c16)
+        if (cb + c16 * 16 < P.M) tmem_ld16(tb + (uint32_t)(cb + c16 * 16), r + 16 * c16);
       tmem_ld_wait();
       if (valid) {
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int m = c16 * 16 + q;
+        for (int q = 0; q < CB; ++q) {
+          const int m = cb + q;
           if (m < P.M) P.out[(size_t)m * P.ld + n] = __uint_as_float(r[q]);
         }
       }
@@ -141,91 +149,6 @@ struct EpiStore {
     return true;
   }
   SPEC_DEV void finish(int, int) {}
-};
-
-// order-preserving 32-bit key of a float (larger float, larger key)
-SPEC_DEV uint32_t sort_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Candidate retrieval without writing the outputs: an output (row m, feature n)
-// whose key reaches the row's threshold tau[m] goes to a list private to (CTA,
-// epilogue warp, row) -- `slots` entries of keys and feature ids -- so no global
-// atomics sit in the drain; each warp keeps its per-row counts in registers
-// (row m's in lane m % 32) and writes them when the CTA is done (a count above
-// `slots` tells the reader that entries were dropped).  Row-range schedule:
-// every tile is complete in one CTA, and [lo, hi) keeps the shifted last tile's
-// overlap from being taken twice.  At most 64 rows.
-template <int MPAD>
-struct EpiFilter {
-  struct Params {
-    int M;
-    int slots;
-    const uint32_t* tau;
-    uint32_t* keys;      // [G * 4][M][slots]
-    int* ids;            // [G * 4][M][slots]
-    int* count;          // [G * 4][M]
-  };
-  static_assert(MPAD <= 64, "rows in two registers per lane");
-  const Params& P;
-  int c;
-  int cnt0, cnt1;        // this warp's list lengths of rows (lane) and (lane + 32), in lane order
-  uint32_t tau0, tau1;   // thresholds of rows (lane) and (lane + 32)
-  static constexpr int kScratch = 0;
-  static SPEC_DEV void init(uint8_t*) {}
-  SPEC_DEV EpiFilter(const Params& pp, int cc, uint8_t*, volatile int*) : P(pp), c(cc), cnt0(0), cnt1(0) {
-    const int lane = threadIdx.x & 31;
-    tau0 = lane < P.M ? P.tau[lane] : 0xffffffffu;
-    tau1 = lane + 32 < P.M ? P.tau[lane + 32] : 0xffffffffu;
-  }
-  SPEC_DEV bool after(const Seg&, int, int) { return true; }
-  SPEC_DEV bool segment(const Seg& s, uint32_t tb, int warp, int lane) {
-    const int n = s.row0 + warp * 32 + lane;
-    const bool valid = n >= s.lo && n < s.hi;
-    const size_t region = (size_t)(c * 4 + warp) * P.M;
-    // all of the tile's columns in flight at once, then one wait
-    uint32_t r[MPAD];
-#pragma unroll
-    for (int c16 = 0; c16 < MPAD / 16; ++c16) tmem_ld16(tb + (uint32_t)(c16 * 16), r + 16 * c16);
-    tmem_ld_wait();
-#pragma unroll
-    for (int c16 = 0; c16 < MPAD / 16; ++c16) {
-      if (c16 * 16 >= P.M) break;
-      // sixteen rows' take flags and ballots, independent of each other
-      unsigned bal[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int m = c16 * 16 + q;
-        const uint32_t t = __shfl_sync(0xffffffffu, m < 32 ? tau0 : tau1, m & 31);
-        bal[q] = __ballot_sync(0xffffffffu, valid && m < P.M && sort_key(__uint_as_float(r[m])) >= t);
-      }
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        if (bal[q] == 0u) continue;
-        const int m = c16 * 16 + q;
-        const int base = __shfl_sync(0xffffffffu, m < 32 ? cnt0 : cnt1, m & 31);
-        if (lane == (m & 31)) {
-          if (m < 32) cnt0 += __popc(bal[q]);
-          else cnt1 += __popc(bal[q]);
-        }
-        if ((bal[q] >> lane) & 1u) {
-          const int at = base + __popc(bal[q] & ((1u << lane) - 1u));
-          if (at < P.slots) {
-            const size_t e = (region + m) * P.slots + at;
-            P.keys[e] = sort_key(__uint_as_float(r[m]));
-            P.ids[e] = n;
-          }
-        }
-      }
-    }
-    return true;
-  }
-  SPEC_DEV void finish(int warp, int lane) {
-    const size_t region = (size_t)(c * 4 + warp) * P.M;
-    if (lane < P.M) P.count[region + lane] = cnt0;
-    if (lane + 32 < P.M) P.count[region + lane + 32] = cnt1;
-  }
 };
 
 // ---------------------------------------------------------------- kernel

@@ -214,29 +214,6 @@ def test_lowrank_candidates(M, w):
     no_device_error(dm)
 
 
-def test_lowrank_candidates_threshold_fallbacks():
-    """The two ways a row leaves the thresholded candidate list: (1) the sampled ids
-    (every 20th at V = 40000) score far above the rest, so fewer than Kc scores reach
-    the sample's threshold; (2) all V = 9000 scores equal, so the list overflows.
-    Both rows fall back to the exact selection and still give the oracle's top-Kc."""
-    w = replace(LOWRANK, name="small_lowrank_sampled", V=40000, seed=29)
-    up = synth.round_to_bf16(synth.normal((w.V, w.rank), w.seed, "aux", 0.02, 0.0, 95))
-    up[::20] = synth.round_to_bf16(up[::20] * 8.0)
-    W, dm = _lowrank_model(w, up.astype(np.float32))
-    M = 3
-    hn = synth.make_hidden(w, M, sub=12)
-    cand, out = _run_lowrank(w, W, dm, hn, M)
-    stats = tf.new_stats()
-    tf.check_candidate_head(w, W, np.asarray(hn, np.float64), cand, out, None, "sampled", stats)
-    assert all((c % 20 == 0).all() for c in cand)
-    w2 = replace(LOWRANK, name="small_lowrank_flat_overflow", V=9000, seed=30)
-    row = synth.round_to_bf16(synth.normal((1, w2.rank), w2.seed, "aux", 0.1, 0.0, 96))
-    W2, dm2 = _lowrank_model(w2, np.repeat(row, w2.V, axis=0).astype(np.float32))
-    cand2, _ = _run_lowrank(w2, W2, dm2, synth.make_hidden(w2, 2, sub=13), 2)
-    for m in range(2):
-        np.testing.assert_array_equal(cand2[m], np.arange(w2.num_candidates))
-
-
 DRAFTVOCAB = replace(SMALL_BF16, name="small_d2t", V=6000, draft_vocab=2500, seed=41)
 
 
