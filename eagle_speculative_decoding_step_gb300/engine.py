@@ -258,7 +258,12 @@ class PrefillChainStep:
         self.kv_src = torch.zeros(B, K + 1, **i32)
         self.vws = torch.zeros(lib.spec_verify_workspace_bytes(B, K + 1, w.V), dtype=torch.uint8, device=dev)
 
-    def draft(self):
+    def draft(self, trace=None):
+        """Issue the drafting calls.  ``trace(key, tensors)``, if given, is called on
+        the host after the batched pass and its head ("prefill": the pass's rows,
+        FC feature, pre-norm and normalised states, the gathered last rows and the
+        first draft ids) and after recurrent pass i (i: hn, pre-norm state, ids);
+        it must synchronise before reading them."""
         dm, w, B, R, K = self.dm, self.dm.w, self.B, self.R, self.K
         M = B * R
         es = 2 if w.dtype == "bf16" else 4
@@ -271,6 +276,10 @@ class PrefillChainStep:
         lib.spec_gather_rows(self.hn_all, M, w.H * es, self.last_row, B, self.hn, ws=dm.ws)
         lib.spec_gather_rows(self.pre_all, M, w.H * es, self.last_row, B, self.pre[1], ws=dm.ws)
         lib.spec_lm_head(dm.desc, dm.weights, self.hn, B, 1, self.drafts, self.lp, ws=dm.ws, ids_ld=K)
+        if trace is not None:
+            trace("prefill", {"tok": self.tok, "pos": self.pos, "kv_idx": self.kv_idx, "mask": self.mask,
+                              "last_row": self.last_row, "ctx_next": self.ctx_next, "h0": self.h0,
+                              "pre": self.pre_all, "hn": self.hn_all, "ids": self.drafts[:, 0]})
         # EAGLE-3.1 norm_output: the recurrent passes take the normalised state
         hid = self.hn if w.norm_output else self.pre[1]
         for i in range(1, K):
@@ -281,6 +290,8 @@ class PrefillChainStep:
             lib.spec_draft_layer(dm.desc, dm.weights, rows, hid, out, hn, dm.kv, dm.ws)
             lib.spec_lm_head(dm.desc, dm.weights, hn, B, 1, self.drafts.data_ptr() + 4 * i,
                              self.lp.data_ptr() + 4 * i, ws=dm.ws, ids_ld=K)
+            if trace is not None:
+                trace(i, {"hn": hn, "pre": out, "ids": self.drafts[:, i]})
             hid = hn if w.norm_output else out
 
     def verify(self):

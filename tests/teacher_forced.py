@@ -269,3 +269,45 @@ def gpu_tree_of(st):
     return {"tok": st.t_tok.cpu().numpy(), "par": st.t_par.cpu().numpy(), "dep": st.t_dep.cpu().numpy(),
             "pos": st.t_pos.cpu().numpy(), "score": st.t_score.cpu().numpy(),
             "mask": st.t_mask.cpu().numpy().view(np.uint64)}
+
+
+def prefill_chain(w, W, aux_rows, input_ids, next_token, last_idx, ctx, kv, recs, drafts, stats=None):
+    """The batched initial pass ([NEURON] "EagleProposer", prefill phase) and the
+    recurrent passes after it, on the GPU's own rows, FC feature, states and
+    tokens: the index rows bit for bit, every pass's hidden states within the
+    tolerance, every draft id against the oracle's head on the GPU's state.
+    Returns the oracle's logits of the K passes [B, K, V] (for target logits)."""
+    from oracle import step as ostep
+    stats = stats if stats is not None else new_stats()
+    B, K = drafts.shape
+    g = recs["prefill"]
+    rows, last_row = ostep.prefill_inputs(input_ids, next_token, last_idx, ctx)
+    for key in ("tok", "pos", "kv_idx"):
+        np.testing.assert_array_equal(g[key], rows[key], err_msg="prefill rows " + key)
+    assert [int(x) for x in g["mask"]] == [int(x) for x in rows["mask"]], "prefill masks"
+    np.testing.assert_array_equal(g["last_row"], last_row)
+    ctx2 = np.asarray(ctx, np.int64) + np.asarray(last_idx, np.int64) + 1
+    np.testing.assert_array_equal(g["ctx_next"], ctx2)
+    check_hidden(w, g["h0"], od.fc_fuse(w, W, aux_rows), "prefill h0 (FC fuse)", stats)
+    pre, hn = od.draft_layer(w, W, rows, g["h0"], kv)
+    check_hidden(w, g["pre"], pre, "prefill hidden_prenorm", stats)
+    check_hidden(w, g["hn"], hn, "prefill hidden_normed", stats)
+    Wl = np.asarray(W["lm_head"], np.float64)
+    hn_last = g["hn"][last_row]
+    check_full_head(w, W, hn_last, g["ids"].reshape(B, 1), None, "prefill head", stats)
+    logits = [hn[last_row] @ Wl.T]
+    state = g["hn"] if getattr(w, "norm_output", False) else g["pre"]
+    hid = state[last_row]
+    tok = drafts[:, 0].astype(np.int64)
+    for i in range(1, K):
+        r = {"M": B, "B": B, "R": 1, "step": i - 1, "ctx_len": ctx2, "tok": tok}
+        pre_i, hn_i = od.draft_layer(w, W, r, hid, kv)
+        gi = recs[i]
+        check_hidden(w, gi["pre"], pre_i, "pass %d hidden_prenorm" % i, stats)
+        check_hidden(w, gi["hn"], hn_i, "pass %d hidden_normed" % i, stats)
+        check_full_head(w, W, gi["hn"], gi["ids"].reshape(B, 1), None, "pass %d" % i, stats)
+        logits.append(hn_i @ Wl.T)
+        hid = gi["hn"] if getattr(w, "norm_output", False) else gi["pre"]
+        tok = drafts[:, i].astype(np.int64)
+    return np.stack(logits, axis=1), stats
+
