@@ -34,8 +34,12 @@ def main():
     ap.add_argument("--config", default="llama8b_chain")
     ap.add_argument("--rows", type=int, default=0, help="rows per call (default: the workload's draft rows)")
     ap.add_argument("--iters", type=int, default=5)
+    ap.add_argument("--ctx", type=int, default=0, help="context length override (draft_layer)")
     args = ap.parse_args()
     w = configs.WORKLOADS[args.config]
+    if args.ctx > 0:
+        from dataclasses import replace
+        w = replace(w, ctx=args.ctx, ctx_range=None)
     lib.load()
     torch.manual_seed(0)
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
