@@ -52,11 +52,18 @@ RowInfo to_rowinfo(const spec_rows& r) {
 }
 
 // ---------------------------------------------------------------- cluster helpers
-// Row-wide reductions (RMSNorm over H) run on a thread-block cluster of kCL
-// CTAs per row: each CTA owns H / kCL features, the per-CTA sums meet in
-// distributed shared memory, summed in rank order (deterministic).
-constexpr int kCL = 8;
+// Row-wide reductions (RMSNorm over H) run on a thread-block cluster of CL
+// CTAs per row, 2048 threads a row: each CTA owns H / CL features, the per-CTA
+// sums meet in distributed shared memory, summed in rank order
+// (deterministic).  Few rows spread over many SMs (CL = 8 CTAs of 256);
+// from 32 rows on, a row takes two CTAs of 1024 (fewer cluster barriers;
+// measured: 32 rows 384 -> 389 steps/s, 4 rows 686 -> 676 with CL = 2).
+template <int CL> struct NormCL {
+  static constexpr int kThreads = 2048 / CL < 1024 ? 2048 / CL : 1024;
+};
+inline int norm_cl(int M) { return M >= 32 ? 2 : 8; }
 
+template <int kCL>
 SPEC_DEV float2 cluster_sum2(float2 v, float* red, float2* slot) {
   v.x = block_sum(v.x, red);
   v.y = block_sum(v.y, red);
@@ -83,8 +90,8 @@ struct RopeFreq {
 // row's rotary cos/sin table.  The angle pos * theta^(-2i/hd) is formed in fp64,
 // reduced modulo 2*pi in fp64 (Cody-Waite, two-part 2*pi), then sin/cos are
 // taken in fp32 on the reduced argument.
-template <typename T>
-__global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(256)
+template <typename T, int kCL>
+__global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThreads)
     prologue_kernel(RowInfo ri, int H, int V, int hd, float eps, const __grid_constant__ RopeFreq rf,
                     const T* __restrict__ embed, const T* __restrict__ g_in, const T* __restrict__ g_hid,
                     const T* __restrict__ hid_in, T* __restrict__ x, float2* __restrict__ cs, void* ws) {
@@ -107,7 +114,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(256)
     ss.x += a * a;
     ss.y += c * c;
   }
-  const float2 tot = cluster_sum2(ss, red, &slot);
+  const float2 tot = cluster_sum2<kCL>(ss, red, &slot);
   const float re = 1.f / sqrtf(tot.x / H + eps), rh = 1.f / sqrtf(tot.y / H + eps);
   T* xo = x + (size_t)m * 2 * H;
   for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) {
@@ -191,8 +198,8 @@ __global__ void epi_qkv_kernel(const float* __restrict__ part, SKPlan p, RowInfo
 // MODE 1 (after down):    r = r + down; out_a = r (hidden_prenorm); out_b = final_norm(r)
 // MODE 2 (after the FC, EAGLE-3.1 fc_norm): r = fc output; out_b = fc_norm(r)
 // One cluster of kCL CTAs per row.
-template <typename T, int MODE>
-__global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(256)
+template <typename T, int MODE, int kCL>
+__global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThreads)
     resnorm_kernel(const float* __restrict__ part, SKPlan p, RowInfo ri, int H, float eps,
                    const T* __restrict__ hid_in, const T* __restrict__ gain, float* __restrict__ r,
                    T* __restrict__ out_a, T* __restrict__ out_b) {
@@ -212,7 +219,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(256)
     if (MODE == 1) st(out_a + (size_t)m * H + n, v);
     ss += v * v;
   }
-  const float2 tot = cluster_sum2(make_float2(ss, 0.f), red, &slot);
+  const float2 tot = cluster_sum2<kCL>(make_float2(ss, 0.f), red, &slot);
   const float rs = 1.f / sqrtf(tot.x / H + eps);
   for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) st(out_b + (size_t)m * H + n, rr[n] * rs * ld(gain + n));
 }
@@ -2017,10 +2024,29 @@ void launch_prologue(const spec_model_desc& d, const spec_rows& rows, const spec
   RopeFreq rf;
   for (int i = 0; i < d.head_dim / 2 && i < 128; ++i)
     rf.inv[i] = pow((double)d.rope_theta, -2.0 * (double)i / (double)d.head_dim);
-  DISPATCH_T(d.dtype, launch_pdl(prologue_kernel<T>, dim3(rows.M * kCL), dim3(256), 0, st, 
-                          ri, d.hidden, d.vocab, d.head_dim, d.rms_eps, rf,
-                          (const T*)w.embed, (const T*)w.in_norm, (const T*)w.hidden_norm, (const T*)hid_in,
-                          (T*)x, cs, ws));
+#define PROLOGUE_CL(CL)                                                                                   \
+  DISPATCH_T(d.dtype, launch_pdl(prologue_kernel<T, CL>, dim3(rows.M * CL), dim3(NormCL<CL>::kThreads), 0, st, \
+                                 ri, d.hidden, d.vocab, d.head_dim, d.rms_eps, rf, (const T*)w.embed,          \
+                                 (const T*)w.in_norm, (const T*)w.hidden_norm, (const T*)hid_in, (T*)x, cs, ws))
+  if (norm_cl(rows.M) == 2)
+    PROLOGUE_CL(2);
+  else
+    PROLOGUE_CL(8);
+#undef PROLOGUE_CL
+}
+
+// residual + RMSNorm epilogue of MODE over M rows, cluster size by the row count
+template <int MODE>
+static void launch_resnorm(int dtype, int M, const float* part, const SKPlan& p, const RowInfo& ri, int H, float eps,
+                           const void* hid_in, const void* gain, float* r, void* out_a, void* out_b, cudaStream_t st) {
+#define RESNORM_CL(CL)                                                                                     \
+  DISPATCH_T(dtype, (launch_pdl(resnorm_kernel<T, MODE, CL>, dim3(M * CL), dim3(NormCL<CL>::kThreads), 0, st, \
+                                part, p, ri, H, eps, (const T*)hid_in, (const T*)gain, r, (T*)out_a, (T*)out_b)))
+  if (norm_cl(M) == 2)
+    RESNORM_CL(2);
+  else
+    RESNORM_CL(8);
+#undef RESNORM_CL
 }
 
 void launch_epi_store(int dtype_out, const float* part, const SKPlan& p, int M, int N, void* out, int ld_out,
@@ -2043,16 +2069,13 @@ void launch_epi_qkv(const spec_model_desc& d, const float* part, const SKPlan& p
 void launch_epi_oproj(const spec_model_desc& d, const float* part, const SKPlan& p, const spec_rows& rows,
                       const void* hid_in, const spec_weights& w, float* r1, void* nout, cudaStream_t st) {
   RowInfo ri = to_rowinfo(rows);
-  DISPATCH_T(d.dtype, (launch_pdl(resnorm_kernel<T, 0>, dim3(rows.M * kCL), dim3(256), 0, st, 
-                          part, p, ri, d.hidden, d.rms_eps, (const T*)hid_in, (const T*)w.post_norm, r1, nullptr,
-                          (T*)nout)));
+  launch_resnorm<0>(d.dtype, rows.M, part, p, ri, d.hidden, d.rms_eps, hid_in, w.post_norm, r1, nullptr, nout, st);
 }
 
 void launch_epi_fcnorm(const spec_model_desc& d, const float* part, const SKPlan& p, int M, float* r,
                        const void* gain, void* h0, cudaStream_t st) {
   RowInfo ri{};
-  DISPATCH_T(d.dtype, (launch_pdl(resnorm_kernel<T, 2>, dim3(M * kCL), dim3(256), 0, st, part, p, ri, d.hidden,
-                                  d.rms_eps, nullptr, (const T*)gain, r, nullptr, (T*)h0)));
+  launch_resnorm<2>(d.dtype, M, part, p, ri, d.hidden, d.rms_eps, nullptr, gain, r, nullptr, h0, st);
 }
 
 void launch_epi_swiglu(const spec_model_desc& d, const float* part, const SKPlan& p, int M, void* act,
@@ -2065,9 +2088,7 @@ void launch_epi_swiglu(const spec_model_desc& d, const float* part, const SKPlan
 void launch_epi_down(const spec_model_desc& d, const float* part, const SKPlan& p, int M, float* r1,
                      const spec_weights& w, void* prenorm, void* normed, cudaStream_t st) {
   RowInfo ri{};
-  DISPATCH_T(d.dtype, (launch_pdl(resnorm_kernel<T, 1>, dim3(M * kCL), dim3(256), 0, st, part, p, ri, d.hidden, d.rms_eps, nullptr,
-                                                                     (const T*)w.final_norm, r1, (T*)prenorm,
-                                                                     (T*)normed)));
+  launch_resnorm<1>(d.dtype, M, part, p, ri, d.hidden, d.rms_eps, nullptr, w.final_norm, r1, prenorm, normed, st);
 }
 
 void launch_simt_gemm(int dtype, const void* A0, const void* A1, const void* A2, int K, const void* X, int M,
