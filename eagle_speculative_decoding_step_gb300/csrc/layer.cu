@@ -1066,8 +1066,6 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : 2) attn_ws_kernel(const __g
                                                          int nqg, int n_items, int bh, float scale_log2,
                                                          float* __restrict__ opart, float2* __restrict__ mlpart,
                                                          int* __restrict__ work, void* ws) {
-  pdl_wait();
-  pdl_trigger();
   using S = WsShape<HD, MT>;
   constexpr int TK = S::TK, QM = S::QM, NS = S::NS, NH = S::NH, KP = S::KP, NT = HD / 8, KS = HD / 16;
   constexpr int WPM = 4 / MT, KPW = TK / WPM;   // warps per m-tile, keys per warp
@@ -1099,6 +1097,10 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : 2) attn_ws_kernel(const __g
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     uint32_t fill = 0;
@@ -1106,37 +1108,69 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : 2) attn_ws_kernel(const __g
     int it = blockIdx.x;
     bool ok = true;
     const int ng = TK / bh;                    // block-table runs per tile
-    while (ok && it < n_items) {
-      int nxt = it;
-      if (lane == 0) nxt = work != nullptr ? (int)gridDim.x + atomicAdd(work, 1) : it + (int)gridDim.x;
-      const int s = it % nsplit;
-      const int g = (it / nsplit) % nkv;
-      const int bq = it / (nsplit * nkv);
-      const int b = bq / nqg, q0 = (bq % nqg) * QM;
-      const int nQ = min(QM, nQall - q0);
-      const int ctx = ri.ctx_len[b];
-      int lo = 0x7fffffff;
-      unsigned long long mk = 0;
-      if (lane < nQ) {
-        const int m = b * ri.R + (q0 + lane) / G;
-        const int pos = row_pos(ri, m);
-        lo = window > 0 ? max(0, pos - window + 1) : 0;
-        if (lo > ctx) lo = ctx;
-        mk = row_mask(ri, m);
+    // An item's keys and the block-table entries of its tiles.  Context lengths,
+    // row positions and masks and the block table are inputs of the call that no
+    // kernel of it writes, and this kernel starts only once every block of the
+    // launch before it has passed its own dependency wait, i.e. once all earlier
+    // launches (this call's prologue and QKV GEMM among them) have finished: so
+    // the first item is described before the wait, reading through L2.
+    struct Item {
+      int s, g, b, q0, nQ, ctx, lo, klo, kend, cb, t0, ntiles;
+      unsigned long long mk;
+    };
+    auto describe = [&](int i) {
+      Item d;
+      d.s = i % nsplit;
+      d.g = (i / nsplit) % nkv;
+      const int bq = i / (nsplit * nkv);
+      d.b = bq / nqg;
+      d.q0 = (bq % nqg) * QM;
+      d.nQ = min(QM, nQall - d.q0);
+      d.ctx = __ldcg(ri.ctx_len + d.b);
+      d.lo = 0x7fffffff;
+      d.mk = 0;
+      if (lane < d.nQ) {
+        const int m = d.b * ri.R + (d.q0 + lane) / G;
+        const int pos = ri.pos ? __ldcg(ri.pos + m) : d.ctx + ri.step;
+        d.lo = window > 0 ? max(0, pos - window + 1) : 0;
+        if (d.lo > d.ctx) d.lo = d.ctx;
+        d.mk = ri.mask ? __ldcg(reinterpret_cast<const unsigned long long*>(ri.mask) + m) : row_mask(ri, m);
       }
-      int klo = lo;
-      unsigned long long om = mk;
+      int klo = d.lo;
+      unsigned long long om = d.mk;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         klo = min(klo, __shfl_xor_sync(0xffffffffu, klo, o));
         om |= __shfl_xor_sync(0xffffffffu, om, o);
       }
-      const int kend = ctx + (om ? 64 - __clzll((long long)om) : 0);   // keys: cache indices [klo, kend)
-      const int cb = klo & ~(TK - 1);
-      const int T = kend > klo ? (kend - cb + TK - 1) / TK : 0;
+      d.klo = klo;
+      d.kend = d.ctx + (om ? 64 - __clzll((long long)om) : 0);   // keys: cache indices [klo, kend)
+      d.cb = klo & ~(TK - 1);
+      const int T = d.kend > klo ? (d.kend - d.cb + TK - 1) / TK : 0;
       const int ct = (T + nsplit - 1) / nsplit;
-      const int t0 = s * ct;
-      const int ntiles = max(0, min(T, t0 + ct) - t0);
+      d.t0 = d.s * ct;
+      d.ntiles = max(0, min(T, d.t0 + ct) - d.t0);
+      return d;
+    };
+    auto table_entry = [&](const Item& d, int j) {   // lane r < ng: block-table entry of run r of tile j
+      int ent = -1;
+      if (lane < ng) {
+        const int ci = d.cb + (d.t0 + j) * TK + lane * bh;
+        const int blk = ci / kv.block_size;
+        if (ci < d.kend && blk < kv.max_blocks) ent = __ldcg(kv.block_table + (size_t)d.b * kv.max_blocks + blk);
+      }
+      return ent;
+    };
+    Item cur = describe(it);
+    int ent0 = table_entry(cur, 0);
+    pdl_wait();
+    pdl_trigger();
+    while (ok && it < n_items) {
+      int nxt = it;
+      if (lane == 0) nxt = work != nullptr ? (int)gridDim.x + atomicAdd(work, 1) : it + (int)gridDim.x;
+      const int s = cur.s, g = cur.g, b = cur.b, q0 = cur.q0, nQ = cur.nQ, ctx = cur.ctx, lo = cur.lo;
+      const unsigned long long mk = cur.mk;
+      const int klo = cur.klo, kend = cur.kend, cb = cur.cb, t0 = cur.t0, ntiles = cur.ntiles;
       if (ntiles == 0) {
         // an empty split: its partials say "no keys"
         for (int e = lane; e < nQ * HD; e += 32) {
@@ -1153,12 +1187,7 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : 2) attn_ws_kernel(const __g
         for (int j = 0; j < ntiles; ++j) {
           const int slot = (int)(fill % NS);
           const int ci0 = cb + (t0 + j) * TK;
-          int ent = -1;                        // lane r < ng: block-table entry of run r
-          if (lane < ng) {
-            const int ci = ci0 + lane * bh;
-            const int blk = ci / kv.block_size;
-            if (ci < kend && blk < kv.max_blocks) ent = kv.block_table[(size_t)b * kv.max_blocks + blk];
-          }
+          const int ent = j == 0 ? ent0 : table_entry(cur, j);
           if (fill >= (uint32_t)NS) {
             const bool w = tc::mbar_wait(empty0 + 8u * slot, ((fill / NS) - 1u) & 1u, abort);
             if (__any_sync(0xffffffffu, !w)) { ok = false; break; }
@@ -1216,6 +1245,10 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : 2) attn_ws_kernel(const __g
         qbuf_sel ^= 1;
       }
       it = __shfl_sync(0xffffffffu, nxt, 0);
+      if (it < n_items) {
+        cur = describe(it);
+        ent0 = table_entry(cur, 0);
+      }
     }
     // end of the sequence: one more slot, without copies
     if (ok) {
@@ -1230,6 +1263,8 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : 2) attn_ws_kernel(const __g
     if (lane == 0) misc[5] = (int)fill;
   } else {
     // ------------------------------------------------------------ consumers
+    pdl_wait();
+    pdl_trigger();
     const int grp = lane >> 2, tig = lane & 3;
     const int mtile = MT == 1 ? 0 : warp / WPM, kbase = (warp % WPM) * KPW;   // this warp's m-tile and keys
     uint32_t fill = 0, mph = 0;
@@ -1404,27 +1439,44 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : 2) attn_ws_kernel(const __g
         okm = tc::mbar_wait(mbar, mph, abort);
         mph ^= 1u;
         if (!okm) break;
-        for (int e = tid; e < nQ * HD; e += 128) {
-          const int qi = e / HD, d = e % HD;
+        // thread -> one query row (TPR threads a row) and every TPR-th 4-float chunk of
+        // it: the row's weights once, then independent 16-byte loads and stores
+        constexpr int TPR = 128 / QM, NCH = HD / 4 / TPR;
+        const int qi = tid / TPR, cq = tid % TPR;
+        if (qi < nQ) {
           const int r = qi & 15, w0 = (qi >> 4) * WPM;
-          const int col = (((d >> 3) ^ (r & 7)) << 3) + (d & 7);
-          float M = -INFINITY;
+          float mw[WPM], f[WPM];
+          float M = -INFINITY, L = 0.f;
 #pragma unroll
-          for (int w = 0; w < WPM; ++w) M = fmaxf(M, sMw[(w0 + w) * 16 + r]);
-          float o = 0.f, L = 0.f;
-          if (M > -INFINITY) {
+          for (int w = 0; w < WPM; ++w) {
+            mw[w] = sMw[(w0 + w) * 16 + r];
+            M = fmaxf(M, mw[w]);
+          }
 #pragma unroll
-            for (int w = 0; w < WPM; ++w) {
-              const float f = exp2f(sMw[(w0 + w) * 16 + r] - M);
-              o += red[((size_t)(w0 + w) * 16 + r) * HD + col] * f;
-              L += sLw[(w0 + w) * 16 + r] * f;
-            }
+          for (int w = 0; w < WPM; ++w) {
+            f[w] = M == -INFINITY ? 0.f : exp2f(mw[w] - M);
+            L += sLw[(w0 + w) * 16 + r] * f[w];
           }
           const int q = mt.q0 + qi;
           const size_t base = ((size_t)(mt.b * ri.R + q / G) * nq + mt.g * G + q % G) * nsplit + mt.s;
-          opart[base * HD + d] = o;
+          float4* dst = reinterpret_cast<float4*>(opart + base * HD);
+#pragma unroll
+          for (int k = 0; k < NCH; ++k) {
+            const int c = k * TPR + cq;                                   // dims 4c .. 4c + 3
+            const int col = (((c >> 1) ^ (r & 7)) << 3) + ((c & 1) << 2);
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < WPM; ++w) {
+              const float4 v = *reinterpret_cast<const float4*>(red + ((size_t)(w0 + w) * 16 + r) * HD + col);
+              o.x += v.x * f[w];
+              o.y += v.y * f[w];
+              o.z += v.z * f[w];
+              o.w += v.w * f[w];
+            }
+            dst[c] = o;
+          }
           // the combine kernel takes natural-log maxima of the scaled scores
-          if (d == 0) mlpart[base] = make_float2(M == -INFINITY ? -INFINITY : M * 0.69314718055994531f, L);
+          if (cq == 0) mlpart[base] = make_float2(M == -INFINITY ? -INFINITY : M * 0.69314718055994531f, L);
         }
         wrote = true;
       }
