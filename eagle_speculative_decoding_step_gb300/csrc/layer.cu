@@ -166,7 +166,11 @@ __global__ void epi_qkv_kernel(const float* __restrict__ part, SKPlan p, RowInfo
   const int rem = (int)(idx % (nh * half));
   const int hh = rem / half, i = rem % half;
   const int n1 = hh * hd + i, n2 = n1 + half;
-  float x1 = sk_sum(part, p, m, n1), x2 = sk_sum(part, p, m, n2);
+  const int nn[2] = {n1, n2};
+  const bool on[2] = {true, true};
+  float xv[2];
+  sk_sum_n<2>(part, p, m, nn, on, xv);
+  float x1 = xv[0], x2 = xv[1];
   if (hh < nq + nkv) {
     const float2 c = cs[(size_t)m * half + i];
     const float y1 = x1 * c.x - x2 * c.y;
@@ -212,12 +216,24 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
   const T* h = (MODE == 0) ? hid_in + (size_t)row_src(ri, m) * H : nullptr;
   float* rr = r + (size_t)m * H;
   float ss = 0.f;
-  for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) {
-    const float base = (MODE == 0) ? ld(h + n) : (MODE == 1 ? rr[n] : 0.f);
-    const float v = base + sk_sum(part, p, m, n);
-    rr[n] = v;
-    if (MODE == 1) st(out_a + (size_t)m * H + n, v);
-    ss += v * v;
+  // two features a thread per round, their partials' loads in flight together
+  for (int n = n0 + threadIdx.x; n < n1; n += 2 * blockDim.x) {
+    const int nn[2] = {n, n + (int)blockDim.x};
+    const bool on[2] = {true, nn[1] < n1};
+    float base[2], sv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      base[u] = !on[u] ? 0.f : (MODE == 0) ? ld(h + nn[u]) : (MODE == 1 ? rr[nn[u]] : 0.f);
+    sk_sum_n<2>(part, p, m, nn, on, sv);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (!on[u]) continue;
+      const int k = nn[u];
+      const float v = base[u] + sv[u];
+      rr[k] = v;
+      if (MODE == 1) st(out_a + (size_t)m * H + k, v);
+      ss += v * v;
+    }
   }
   const float2 tot = cluster_sum2<kCL>(make_float2(ss, 0.f), red, &slot);
   const float rs = 1.f / sqrtf(tot.x / H + eps);
@@ -232,8 +248,11 @@ __global__ void epi_swiglu_kernel(const float* __restrict__ part, SKPlan p, int 
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)M * I) return;
   const int m = (int)(idx / I), i = (int)(idx % I);
-  const float g = sk_sum(part, p, m, i);
-  const float u = sk_sum(part, p, m, I + i);
+  const int nn[2] = {i, I + i};
+  const bool on[2] = {true, true};
+  float gu[2];
+  sk_sum_n<2>(part, p, m, nn, on, gu);
+  const float g = gu[0], u = gu[1];
   st(act + (size_t)m * I + i, g / (1.f + expf(-g)) * u);
 }
 

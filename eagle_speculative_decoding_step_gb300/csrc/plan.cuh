@@ -43,18 +43,51 @@ SPEC_DEV void sk_feature(const SKPlan& p, int n, int& tile, int& lane) {
   tile = p.tbase[i] + (local >> 7);
   lane = local & 127;
 }
-SPEC_DEV float sk_sum_segs(const float* __restrict__ part, const SKPlan& p, const SKTileSegs& s, int m, int lane) {
-  float acc = part[sk_slot(p, s.c0, s.j0) + (size_t)m * 128 + lane];
-  for (int c = s.c0 + 1; c <= s.c1; ++c) acc += part[sk_slot(p, c, 0) + (size_t)m * 128 + lane];
-  return acc;
+// Sum over the segments of the fp32 partials of outputs (row m, features n[f]),
+// n in the stacked feature space; CTAs in ascending order (deterministic).  The
+// loads of up to 1 + kSegBatch segments of every feature are issued before the
+// first add, so a feature costs one round trip to L2 rather than one per
+// segment; a tile spread over more CTAs takes the rest one by one.  Features
+// with on[f] false read nothing and give 0.
+constexpr int kSegBatch = 8;
+template <int NF>
+SPEC_DEV void sk_sum_n(const float* __restrict__ part, const SKPlan& p, int m, const int (&n)[NF],
+                       const bool (&on)[NF], float (&out)[NF]) {
+  SKTileSegs s[NF];
+  const float* q[NF];
+  float first[NF], v[NF][kSegBatch];
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    int tile, lane;
+    sk_feature(p, n[f], tile, lane);
+    s[f] = sk_tile_segs(p, tile);
+    q[f] = part + (size_t)m * 128 + lane;
+  }
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    first[f] = on[f] ? q[f][sk_slot(p, s[f].c0, s[f].j0)] : 0.f;
+#pragma unroll
+    for (int k = 0; k < kSegBatch; ++k)
+      v[f][k] = on[f] && s[f].c0 + 1 + k <= s[f].c1 ? q[f][sk_slot(p, s[f].c0 + 1 + k, 0)] : 0.f;
+  }
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    float acc = first[f];
+#pragma unroll
+    for (int k = 0; k < kSegBatch; ++k)
+      if (s[f].c0 + 1 + k <= s[f].c1) acc += v[f][k];
+    if (on[f])
+      for (int c = s[f].c0 + 1 + kSegBatch; c <= s[f].c1; ++c) acc += q[f][sk_slot(p, c, 0)];
+    out[f] = on[f] ? acc : 0.f;
+  }
 }
 
-// Sum over the segments of the fp32 partials of output (row m, feature n),
-// n in the stacked feature space; CTAs in ascending order (deterministic).
 SPEC_DEV float sk_sum(const float* __restrict__ part, const SKPlan& p, int m, int n) {
-  int tile, lane;
-  sk_feature(p, n, tile, lane);
-  return sk_sum_segs(part, p, sk_tile_segs(p, tile), m, lane);
+  const int nn[1] = {n};
+  const bool on[1] = {true};
+  float out[1];
+  sk_sum_n<1>(part, p, m, nn, on, out);
+  return out[0];
 }
 
 }  // namespace spec
