@@ -62,22 +62,36 @@ template <int CL> struct NormCL {
   static constexpr int kThreads = 2048 / CL < 1024 ? 2048 / CL : 1024;
 };
 inline int norm_cl(int M) { return M >= 32 ? 2 : 8; }
+// Features a thread of the row-norm kernels keeps in registers (rows up to
+// 2 x 2048 = 4096 features); wider rows take the looping form.
+constexpr int kNormKeep = 2;
 
+// Sum of v over the kCL CTAs of the cluster (each CTA: a block sum of both
+// components in one pass, then its total pushed into slot[rank] of every CTA of
+// the cluster; one cluster barrier; each CTA adds the slots in rank order).
+// red: 64 floats of shared memory, slot: kCL float2 of shared memory.
 template <int kCL>
 SPEC_DEV float2 cluster_sum2(float2 v, float* red, float2* slot) {
-  v.x = block_sum(v.x, red);
-  v.y = block_sum(v.y, red);
-  if (threadIdx.x == 0) *slot = v;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v.x = warp_sum(v.x);
+  v.y = warp_sum(v.y);
+  __syncthreads();
+  if (lane == 0) reinterpret_cast<float2*>(red)[wid] = v;
+  __syncthreads();
+  float2 w = lane < nw ? reinterpret_cast<float2*>(red)[lane] : make_float2(0.f, 0.f);
+  w.x = warp_sum(w.x);
+  w.y = warp_sum(w.y);
   cg::cluster_group cl = cg::this_cluster();
-  cl.sync();
+  const int me = (int)cl.block_rank();
+  if (threadIdx.x < kCL) cl.map_shared_rank(slot, (int)threadIdx.x)[me] = w;
+  cl.sync();     // the pushes land before any CTA reads its slots; none is touched after
   float2 t = make_float2(0.f, 0.f);
 #pragma unroll
   for (int r = 0; r < kCL; ++r) {
-    const float2 o = *cl.map_shared_rank(slot, r);
+    const float2 o = slot[r];
     t.x += o.x;
     t.y += o.y;
   }
-  cl.sync();     // no CTA leaves while another still reads its slot
   return t;
 }
 
@@ -97,8 +111,8 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
                     const T* __restrict__ hid_in, T* __restrict__ x, float2* __restrict__ cs, void* ws) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float red[32];
-  __shared__ float2 slot;
+  __shared__ float red[64];
+  __shared__ float2 slot[kCL];
   const int m = blockIdx.x / kCL, rk = blockIdx.x % kCL;
   int tok = ri.tok[(size_t)m * ri.tok_stride];
   if (tok < 0 || tok >= V) {
@@ -108,18 +122,48 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
   const T* e = embed + (size_t)tok * H;
   const T* h = hid_in + (size_t)row_src(ri, m) * H;
   const int n0 = rk * H / kCL, n1 = (rk + 1) * H / kCL;
-  float2 ss = make_float2(0.f, 0.f);
-  for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) {
-    const float a = ld(e + n), c = ld(h + n);
-    ss.x += a * a;
-    ss.y += c * c;
-  }
-  const float2 tot = cluster_sum2<kCL>(ss, red, &slot);
-  const float re = 1.f / sqrtf(tot.x / H + eps), rh = 1.f / sqrtf(tot.y / H + eps);
   T* xo = x + (size_t)m * 2 * H;
-  for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) {
-    st(xo + n, ld(e + n) * re * ld(g_in + n));
-    st(xo + H + n, ld(h + n) * rh * ld(g_hid + n));
+  float2 ss = make_float2(0.f, 0.f);
+  if (n1 - n0 <= kNormKeep * (int)blockDim.x) {
+    // at most kNormKeep features a thread: rows, gains and all loads at once, kept
+    // in registers across the cluster reduction
+    float a[kNormKeep], c[kNormKeep], ga[kNormKeep], gh[kNormKeep];
+#pragma unroll
+    for (int u = 0; u < kNormKeep; ++u) {
+      const int n = n0 + threadIdx.x + u * blockDim.x;
+      const bool on = n < n1;
+      a[u] = on ? ld(e + n) : 0.f;
+      c[u] = on ? ld(h + n) : 0.f;
+      ga[u] = on ? ld(g_in + n) : 0.f;
+      gh[u] = on ? ld(g_hid + n) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kNormKeep; ++u) {
+      ss.x += a[u] * a[u];
+      ss.y += c[u] * c[u];
+    }
+    const float2 tot = cluster_sum2<kCL>(ss, red, slot);
+    const float re = 1.f / sqrtf(tot.x / H + eps), rh = 1.f / sqrtf(tot.y / H + eps);
+#pragma unroll
+    for (int u = 0; u < kNormKeep; ++u) {
+      const int n = n0 + threadIdx.x + u * blockDim.x;
+      if (n < n1) {
+        st(xo + n, a[u] * re * ga[u]);
+        st(xo + H + n, c[u] * rh * gh[u]);
+      }
+    }
+  } else {
+    for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) {
+      const float a = ld(e + n), c = ld(h + n);
+      ss.x += a * a;
+      ss.y += c * c;
+    }
+    const float2 tot = cluster_sum2<kCL>(ss, red, slot);
+    const float re = 1.f / sqrtf(tot.x / H + eps), rh = 1.f / sqrtf(tot.y / H + eps);
+    for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) {
+      st(xo + n, ld(e + n) * re * ld(g_in + n));
+      st(xo + H + n, ld(h + n) * rh * ld(g_hid + n));
+    }
   }
   if (rk == 0) {
     const int pos = row_pos(ri, m);
@@ -209,13 +253,42 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
                    T* __restrict__ out_a, T* __restrict__ out_b) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float red[32];
-  __shared__ float2 slot;
+  __shared__ float red[64];
+  __shared__ float2 slot[kCL];
   const int m = blockIdx.x / kCL, rk = blockIdx.x % kCL;
   const int n0 = rk * H / kCL, n1 = (rk + 1) * H / kCL;
   const T* h = (MODE == 0) ? hid_in + (size_t)row_src(ri, m) * H : nullptr;
   float* rr = r + (size_t)m * H;
   float ss = 0.f;
+  if (n1 - n0 <= kNormKeep * (int)blockDim.x) {
+    // at most kNormKeep features a thread: bases, partials and gains loaded at once,
+    // the row kept in registers across the cluster reduction
+    int nn[kNormKeep];
+    bool on[kNormKeep];
+    float base[kNormKeep], sv[kNormKeep], gv[kNormKeep];
+#pragma unroll
+    for (int u = 0; u < kNormKeep; ++u) {
+      nn[u] = n0 + threadIdx.x + u * blockDim.x;
+      on[u] = nn[u] < n1;
+      base[u] = !on[u] ? 0.f : (MODE == 0) ? ld(h + nn[u]) : (MODE == 1 ? rr[nn[u]] : 0.f);
+      gv[u] = on[u] ? ld(gain + nn[u]) : 0.f;
+    }
+    sk_sum_n<kNormKeep>(part, p, m, nn, on, sv);
+#pragma unroll
+    for (int u = 0; u < kNormKeep; ++u) {
+      sv[u] += base[u];
+      if (!on[u]) continue;
+      rr[nn[u]] = sv[u];
+      if (MODE == 1) st(out_a + (size_t)m * H + nn[u], sv[u]);
+      ss += sv[u] * sv[u];
+    }
+    const float2 tot = cluster_sum2<kCL>(make_float2(ss, 0.f), red, slot);
+    const float rs = 1.f / sqrtf(tot.x / H + eps);
+#pragma unroll
+    for (int u = 0; u < kNormKeep; ++u)
+      if (on[u]) st(out_b + (size_t)m * H + nn[u], sv[u] * rs * gv[u]);
+    return;
+  }
   // two features a thread per round, their partials' loads in flight together
   for (int n = n0 + threadIdx.x; n < n1; n += 2 * blockDim.x) {
     const int nn[2] = {n, n + (int)blockDim.x};
@@ -235,7 +308,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
       ss += v * v;
     }
   }
-  const float2 tot = cluster_sum2<kCL>(make_float2(ss, 0.f), red, &slot);
+  const float2 tot = cluster_sum2<kCL>(make_float2(ss, 0.f), red, slot);
   const float rs = 1.f / sqrtf(tot.x / H + eps);
   for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) st(out_b + (size_t)m * H + n, rr[n] * rs * ld(gain + n));
 }
@@ -1527,9 +1600,13 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restric
   pdl_trigger();
   const int mh = blockIdx.x;          // m * nq + h
   const int d = threadIdx.x;
-  // the splits' (max, sum) pairs once into shared memory (nsplit <= 64 <= HD), the
-  // weights there too; then each thread sums its dimension over the splits with
-  // independent loads
+  // every split's value of this dimension (nsplit <= 64) is loaded together with the
+  // splits' (max, sum) pairs, which go to shared memory (nsplit <= 64 <= HD) with
+  // the splits' weights; the weighted sum then takes the splits in order
+  const float* op = opart + (size_t)mh * nsplit * HD + d;
+  float v[64];
+#pragma unroll
+  for (int u = 0; u < 64; ++u) v[u] = u < nsplit ? op[(size_t)u * HD] : 0.f;
   __shared__ float sm_[64], sl_[64], sw[64];
   if (d < nsplit) {
     const float2 ml = mlpart[(size_t)mh * nsplit + d];
@@ -1543,18 +1620,10 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restric
   __syncthreads();
   float L = 0.f;
   for (int s = 0; s < nsplit; ++s) L += sl_[s] * sw[s];
-  // sixteen splits' loads in flight per round, four partial sums
-  const float* op = opart + (size_t)mh * nsplit * HD + d;
   float o4[4] = {0.f, 0.f, 0.f, 0.f};
-  int s = 0;
-  for (; s + 16 <= nsplit; s += 16) {
-    float v[16];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) v[u] = op[(size_t)(s + u) * HD];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) o4[u & 3] += v[u] * sw[s + u];
-  }
-  for (; s < nsplit; ++s) o4[s & 3] += op[(size_t)s * HD] * sw[s];
+  for (int u = 0; u < 64; ++u)
+    if (u < nsplit) o4[u & 3] += v[u] * sw[u];
   const float o = (o4[0] + o4[1]) + (o4[2] + o4[3]);
   st(out + (size_t)mh * HD + d, L > 0.f ? o / L : 0.f);
 }

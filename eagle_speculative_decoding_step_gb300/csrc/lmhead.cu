@@ -187,10 +187,11 @@ struct EpiStats {
 
 }  // namespace tc
 
-// Merge the per-CTA records of row m: lse (whole block) and the k best (the
-// records' lists are staged in shared memory; every thread keeps a sorted top-KT
-// of the entries it scans, every warp takes its k best by k rounds of a warp
-// argmax over the lanes' heads, and warp 0 does the same over the warps' lists).
+// Merge the per-CTA records of row m: lse (whole block) and the k best (every
+// thread loads its CTA's (max, sum) head and its share of the list entries at
+// once, keeps a sorted top-KT of those entries; every warp takes its k best by k
+// rounds of a warp argmax over the lanes' heads, and warp 0 does the same over
+// the warps' lists).  256 threads.
 constexpr int kLmMaxCtas = 256;
 
 template <int KT>
@@ -201,24 +202,30 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__
   pdl_wait();
   pdl_trigger();
   constexpr int REC = 2 + 2 * KT;
+  constexpr int PER = (kLmMaxCtas * KT + 255) / 256;     // list entries a thread scans
   __shared__ float red[32];
-  __shared__ float cv[kLmMaxCtas * KT];
-  __shared__ int ci[kLmMaxCtas * KT];
   const int m = blockIdx.x;
-  float mx = -INFINITY;
-  for (int c = threadIdx.x; c < G; c += blockDim.x) mx = fmaxf(mx, part[((size_t)c * mpad + m) * REC]);
-  for (int e = threadIdx.x; e < G * KT; e += blockDim.x) {
-    const float* r = part + ((size_t)(e / KT) * mpad + m) * REC;
-    cv[e] = r[2 + e % KT];
-    ci[e] = __float_as_int(r[2 + KT + e % KT]);
+  float hm = -INFINITY, hs = 0.f;
+  if ((int)threadIdx.x < G) {
+    const float* r = part + ((size_t)threadIdx.x * mpad + m) * REC;
+    hm = r[0];
+    hs = r[1];
   }
-  mx = block_max(mx, red);
-  float s = 0.f;
-  for (int c = threadIdx.x; c < G; c += blockDim.x) {
-    const float* r = part + ((size_t)c * mpad + m) * REC;
-    if (r[0] > -INFINITY) s += r[1] * expf(r[0] - mx);
+  float ev[PER];
+  int ei[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = threadIdx.x + 256 * j;
+    ev[j] = -INFINITY;
+    ei[j] = 0x7fffffff;
+    if (e < G * KT) {
+      const float* r = part + ((size_t)(e / KT) * mpad + m) * REC;
+      ev[j] = r[2 + e % KT];
+      ei[j] = __float_as_int(r[2 + KT + e % KT]);
+    }
   }
-  s = block_sum(s, red);      // its barriers also publish cv / ci
+  const float mx = block_max(hm, red);
+  const float s = block_sum(hm > -INFINITY ? hs * expf(hm - mx) : 0.f, red);
   const float lse = mx + logf(s);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // every thread: a sorted top-KT of the entries it scans; every warp: its best k
@@ -245,7 +252,9 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__
     }
   };
   auto pop_rounds = [&](float* ov, int* oi) {     // k rounds; lane 0 receives the winners
-    for (int rr = 0; rr < k; ++rr) {
+#pragma unroll
+    for (int rr = 0; rr < KT; ++rr) {
+      if (rr >= k) break;
       float bv = tv[0];
       int bi = ti[0];
       warp_argmax_redux(bv, bi);
@@ -258,7 +267,9 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__
       if (lane == 0) { ov[rr] = bv; oi[rr] = bi; }
     }
   };
-  for (int e = threadIdx.x; e < G * KT; e += blockDim.x) insert(cv[e], ci[e]);
+#pragma unroll
+  for (int j = 0; j < PER; ++j)
+    if (threadIdx.x + 256 * j < G * KT) insert(ev[j], ei[j]);
   pop_rounds(wv[warp], wi[warp]);
   __syncthreads();
   if (warp != 0) return;
@@ -270,7 +281,9 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__
   int fi[KT];
   pop_rounds(fv, fi);
   if (lane == 0) {
-    for (int rr = 0; rr < k; ++rr) {
+#pragma unroll
+    for (int rr = 0; rr < KT; ++rr) {
+      if (rr >= k) break;
       ids[(size_t)m * ld_ids + rr] = d2t ? d2t[fi[rr]] : fi[rr];
       lp[(size_t)m * ld_ids + rr] = fv[rr] - lse;
     }

@@ -36,11 +36,17 @@ SPEC_DEV SKTileSegs sk_tile_segs(const SKPlan& p, int tile) {
   return s;
 }
 // Stacked-feature n -> (tile, lane)
+// (constant indices only: the plan stays in parameter space)
 SPEC_DEV void sk_feature(const SKPlan& p, int n, int& tile, int& lane) {
-  int i = 0;
-  while (i + 1 < p.nmat && n >= p.obase[i + 1]) ++i;
-  const int local = n - p.obase[i];
-  tile = p.tbase[i] + (local >> 7);
+  int ob = p.obase[0], tb = p.tbase[0];
+#pragma unroll
+  for (int k = 1; k < 4; ++k)
+    if (k < p.nmat && n >= p.obase[k]) {
+      ob = p.obase[k];
+      tb = p.tbase[k];
+    }
+  const int local = n - ob;
+  tile = tb + (local >> 7);
   lane = local & 127;
 }
 // Sum over the segments of the fp32 partials of outputs (row m, features n[f]),
