@@ -1592,7 +1592,7 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : 2) attn_ws_kernel(const __g
   }
 }
 
-template <typename T, int HD>
+template <typename T, int HD, int NSM>
 __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restrict__ opart,
                                                           const float2* __restrict__ mlpart, int nq, int nsplit,
                                                           T* __restrict__ out) {
@@ -1600,13 +1600,13 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restric
   pdl_trigger();
   const int mh = blockIdx.x;          // m * nq + h
   const int d = threadIdx.x;
-  // every split's value of this dimension (nsplit <= 64) is loaded together with the
-  // splits' (max, sum) pairs, which go to shared memory (nsplit <= 64 <= HD) with
-  // the splits' weights; the weighted sum then takes the splits in order
+  // every split's value of this dimension (nsplit <= NSM <= 64) is loaded together
+  // with the splits' (max, sum) pairs, which go to shared memory (nsplit <= 64 <= HD)
+  // with the splits' weights; the weighted sum then takes the splits in order
   const float* op = opart + (size_t)mh * nsplit * HD + d;
-  float v[64];
+  float v[NSM];
 #pragma unroll
-  for (int u = 0; u < 64; ++u) v[u] = u < nsplit ? op[(size_t)u * HD] : 0.f;
+  for (int u = 0; u < NSM; ++u) v[u] = u < nsplit ? op[(size_t)u * HD] : 0.f;
   __shared__ float sm_[64], sl_[64], sw[64];
   if (d < nsplit) {
     const float2 ml = mlpart[(size_t)mh * nsplit + d];
@@ -1622,10 +1622,23 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restric
   for (int s = 0; s < nsplit; ++s) L += sl_[s] * sw[s];
   float o4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int u = 0; u < 64; ++u)
+  for (int u = 0; u < NSM; ++u)
     if (u < nsplit) o4[u & 3] += v[u] * sw[u];
   const float o = (o4[0] + o4[1]) + (o4[2] + o4[3]);
   st(out + (size_t)mh * HD + d, L > 0.f ? o / L : 0.f);
+}
+
+// The combine with a register batch sized to the split count (16, 32 or 64).
+template <typename T, int HD>
+static void launch_combine(const float* opart, const float2* mlpart, int M, int nq, int nsplit, void* out,
+                           cudaStream_t st) {
+  const dim3 grid(M * nq), block(HD);
+  if (nsplit <= 16)
+    launch_pdl(attn_combine_kernel<T, HD, 16>, grid, block, 0, st, opart, mlpart, nq, nsplit, (T*)out);
+  else if (nsplit <= 32)
+    launch_pdl(attn_combine_kernel<T, HD, 32>, grid, block, 0, st, opart, mlpart, nq, nsplit, (T*)out);
+  else
+    launch_pdl(attn_combine_kernel<T, HD, 64>, grid, block, 0, st, opart, mlpart, nq, nsplit, (T*)out);
 }
 
 // ---------------------------------------------------------------- row statistics
@@ -2293,8 +2306,7 @@ static spec_status attn_launch(const spec_model_desc& d, const RowInfo& ri, cons
   const float scale = 1.f / sqrtf((float)d.head_dim);
   launch_pdl(kern, dim3(grid), dim3(128), smem, st, (const TT*)qbuf, kv, ri, d.n_q_heads, d.n_kv_heads, d.window,
              nsplit, nqg, n_items, scale, opart, mlpart, ws);
-  launch_pdl(attn_combine_kernel<TT, HDV>, dim3(rows.M * d.n_q_heads), dim3(HDV), 0, st, opart, mlpart, d.n_q_heads, nsplit,
-                                                                     (TT*)attn_out);
+  launch_combine<TT, HDV>(opart, mlpart, rows.M, d.n_q_heads, nsplit, attn_out, st);
   return SPEC_OK;
 }
 
@@ -2318,8 +2330,7 @@ static spec_status attn_mma_launch(const spec_model_desc& d, const RowInfo& ri, 
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)d.head_dim);
   launch_pdl(kern, dim3(grid), dim3(128), smem, st, (const __nv_bfloat16*)qbuf, kv, ri, d.n_q_heads, d.n_kv_heads,
              d.window, nsplit, nqg, n_items, scale_log2, opart, mlpart, n_items > grid ? work : nullptr, ws);
-  launch_pdl(attn_combine_kernel<__nv_bfloat16, HDV>, dim3(rows.M * d.n_q_heads), dim3(HDV), 0, st, opart, mlpart,
-             d.n_q_heads, nsplit, (__nv_bfloat16*)attn_out);
+  launch_combine<__nv_bfloat16, HDV>(opart, mlpart, rows.M, d.n_q_heads, nsplit, attn_out, st);
   return SPEC_OK;
 }
 
@@ -2373,8 +2384,7 @@ static spec_status attn_ws_launch(const spec_model_desc& d, const RowInfo& ri, c
   launch_pdl(kern, dim3(grid), dim3(160), smem, st, tk, tv, (const __nv_bfloat16*)qbuf, kv, ri, d.n_q_heads,
              d.n_kv_heads, d.window, nsplit, nqg, n_items, bh, scale_log2, opart, mlpart,
              n_items > grid ? work : nullptr, ws);
-  launch_pdl(attn_combine_kernel<__nv_bfloat16, HDV>, dim3(rows.M * d.n_q_heads), dim3(HDV), 0, st, opart, mlpart,
-             d.n_q_heads, nsplit, (__nv_bfloat16*)attn_out);
+  launch_combine<__nv_bfloat16, HDV>(opart, mlpart, rows.M, d.n_q_heads, nsplit, attn_out, st);
   return SPEC_OK;
 }
 
