@@ -210,13 +210,23 @@ __global__ void epi_qkv_kernel(const float* __restrict__ part, SKPlan p, RowInfo
   const int rem = (int)(idx % (nh * half));
   const int hh = rem / half, i = rem % half;
   const int n1 = hh * hd + i, n2 = n1 + half;
+  // the rotary pair and the row's cache entry are read while the partials load
+  float2 c = make_float2(1.f, 0.f);
+  if (hh < nq + nkv) c = cs[(size_t)m * half + i];
+  int b = 0, ci = 0;
+  if (hh >= nq) {
+    b = row_req(ri, m);
+    ci = ri.ctx_len[b] + row_kvidx(ri, m);
+  }
   const int nn[2] = {n1, n2};
   const bool on[2] = {true, true};
+  SKGather<2, kSegBatch> gat;
+  sk_gather<2, kSegBatch>(part, p, m, nn, on, gat);
+  const long long slot = hh >= nq ? slot_of(kv, b, ci) : 0;
   float xv[2];
-  sk_sum_n<2>(part, p, m, nn, on, xv);
+  sk_reduce<2, kSegBatch>(p, gat, xv);
   float x1 = xv[0], x2 = xv[1];
   if (hh < nq + nkv) {
-    const float2 c = cs[(size_t)m * half + i];
     const float y1 = x1 * c.x - x2 * c.y;
     const float y2 = x2 * c.x + x1 * c.y;
     x1 = y1;
@@ -228,9 +238,6 @@ __global__ void epi_qkv_kernel(const float* __restrict__ part, SKPlan p, RowInfo
     st(q + i + half, x2);
     return;
   }
-  const int b = row_req(ri, m);
-  const int ci = ri.ctx_len[b] + row_kvidx(ri, m);
-  const long long slot = slot_of(kv, b, ci);
   if (slot < 0) {
     report(ws, SPEC_ERR_DEVICE, m, ci);
     return;
@@ -313,20 +320,35 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
   for (int n = n0 + threadIdx.x; n < n1; n += blockDim.x) st(out_b + (size_t)m * H + n, rr[n] * rs * ld(gain + n));
 }
 
-// act = silu(gate) * up  (gate rows [0, I), up rows [I, 2I) of the stacked output)
-template <typename T>
-__global__ void epi_swiglu_kernel(const float* __restrict__ part, SKPlan p, int M, int I, T* __restrict__ act) {
+// act = silu(gate) * up  (gate rows [0, I), up rows [I, 2I) of the stacked output).
+// Block (x, m): features x * 256 U + u * 256 + threadIdx.x of row m, u < U (U = 4
+// when the batch gives enough blocks, else 1); every partial of a thread's
+// features is loaded before the first add (a gate / up tile spans few CTAs:
+// three segments are loaded at once, more one by one).
+template <typename T, int U>
+__global__ void __launch_bounds__(256) epi_swiglu_kernel(const float* __restrict__ part, SKPlan p, int M, int I,
+                                                         T* __restrict__ act) {
   pdl_wait();
   pdl_trigger();
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long long)M * I) return;
-  const int m = (int)(idx / I), i = (int)(idx % I);
-  const int nn[2] = {i, I + i};
-  const bool on[2] = {true, true};
-  float gu[2];
-  sk_sum_n<2>(part, p, m, nn, on, gu);
-  const float g = gu[0], u = gu[1];
-  st(act + (size_t)m * I + i, g / (1.f + expf(-g)) * u);
+  const int m = blockIdx.y;
+  const int i0 = blockIdx.x * U * 256 + threadIdx.x;
+  int nn[2 * U];
+  bool on[2 * U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int i = i0 + u * 256;
+    on[2 * u] = on[2 * u + 1] = i < I;
+    nn[2 * u] = i < I ? i : 0;
+    nn[2 * u + 1] = I + nn[2 * u];
+  }
+  float gu[2 * U];
+  sk_sum_n<2 * U, 2>(part, p, m, nn, on, gu);
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if (!on[2 * u]) continue;
+    const float g = gu[2 * u], v = gu[2 * u + 1];
+    st(act + (size_t)m * I + nn[2 * u], g / (1.f + expf(-g)) * v);
+  }
 }
 
 // ---------------------------------------------------------------- SIMT GEMM
@@ -2233,9 +2255,15 @@ void launch_epi_fcnorm(const spec_model_desc& d, const float* part, const SKPlan
 
 void launch_epi_swiglu(const spec_model_desc& d, const float* part, const SKPlan& p, int M, void* act,
                        cudaStream_t st) {
-  const long long n = (long long)M * d.intermediate;
-  DISPATCH_T(d.dtype,
-             launch_pdl(epi_swiglu_kernel<T>, dim3(blocks_for(n, 256)), dim3(256), 0, st, part, p, M, d.intermediate, (T*)act));
+  // four features a thread once that still gives two blocks per SM
+  const int I = d.intermediate;
+  if ((long long)((I + 1023) / 1024) * M >= 2LL * sm_count()) {
+    const dim3 grid((I + 1023) / 1024, M);
+    DISPATCH_T(d.dtype, launch_pdl(epi_swiglu_kernel<T, 4>, grid, dim3(256), 0, st, part, p, M, I, (T*)act));
+  } else {
+    const dim3 grid((I + 255) / 256, M);
+    DISPATCH_T(d.dtype, launch_pdl(epi_swiglu_kernel<T, 1>, grid, dim3(256), 0, st, part, p, M, I, (T*)act));
+  }
 }
 
 void launch_epi_down(const spec_model_desc& d, const float* part, const SKPlan& p, int M, float* r1,

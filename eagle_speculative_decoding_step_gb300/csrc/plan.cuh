@@ -51,41 +51,57 @@ SPEC_DEV void sk_feature(const SKPlan& p, int n, int& tile, int& lane) {
 }
 // Sum over the segments of the fp32 partials of outputs (row m, features n[f]),
 // n in the stacked feature space; CTAs in ascending order (deterministic).  The
-// loads of up to 1 + kSegBatch segments of every feature are issued before the
+// loads of up to 1 + SB segments of every feature are issued before the
 // first add, so a feature costs one round trip to L2 rather than one per
 // segment; a tile spread over more CTAs takes the rest one by one.  Features
 // with on[f] false read nothing and give 0.
 constexpr int kSegBatch = 8;
-template <int NF>
-SPEC_DEV void sk_sum_n(const float* __restrict__ part, const SKPlan& p, int m, const int (&n)[NF],
-                       const bool (&on)[NF], float (&out)[NF]) {
+template <int NF, int SB = kSegBatch>
+struct SKGather {
   SKTileSegs s[NF];
   const float* q[NF];
-  float first[NF], v[NF][kSegBatch];
+  float first[NF], v[NF][SB];
+  bool on[NF];
+};
+// Issue the loads (sk_gather), do other work, then add them up (sk_reduce).
+template <int NF, int SB>
+SPEC_DEV void sk_gather(const float* __restrict__ part, const SKPlan& p, int m, const int (&n)[NF],
+                        const bool (&on)[NF], SKGather<NF, SB>& g) {
 #pragma unroll
   for (int f = 0; f < NF; ++f) {
     int tile, lane;
     sk_feature(p, n[f], tile, lane);
-    s[f] = sk_tile_segs(p, tile);
-    q[f] = part + (size_t)m * 128 + lane;
+    g.s[f] = sk_tile_segs(p, tile);
+    g.q[f] = part + (size_t)m * 128 + lane;
+    g.on[f] = on[f];
   }
 #pragma unroll
   for (int f = 0; f < NF; ++f) {
-    first[f] = on[f] ? q[f][sk_slot(p, s[f].c0, s[f].j0)] : 0.f;
+    g.first[f] = on[f] ? g.q[f][sk_slot(p, g.s[f].c0, g.s[f].j0)] : 0.f;
 #pragma unroll
-    for (int k = 0; k < kSegBatch; ++k)
-      v[f][k] = on[f] && s[f].c0 + 1 + k <= s[f].c1 ? q[f][sk_slot(p, s[f].c0 + 1 + k, 0)] : 0.f;
+    for (int k = 0; k < SB; ++k)
+      g.v[f][k] = on[f] && g.s[f].c0 + 1 + k <= g.s[f].c1 ? g.q[f][sk_slot(p, g.s[f].c0 + 1 + k, 0)] : 0.f;
   }
+}
+template <int NF, int SB>
+SPEC_DEV void sk_reduce(const SKPlan& p, const SKGather<NF, SB>& g, float (&out)[NF]) {
 #pragma unroll
   for (int f = 0; f < NF; ++f) {
-    float acc = first[f];
+    float acc = g.first[f];
 #pragma unroll
-    for (int k = 0; k < kSegBatch; ++k)
-      if (s[f].c0 + 1 + k <= s[f].c1) acc += v[f][k];
-    if (on[f])
-      for (int c = s[f].c0 + 1 + kSegBatch; c <= s[f].c1; ++c) acc += q[f][sk_slot(p, c, 0)];
-    out[f] = on[f] ? acc : 0.f;
+    for (int k = 0; k < SB; ++k)
+      if (g.s[f].c0 + 1 + k <= g.s[f].c1) acc += g.v[f][k];
+    if (g.on[f])
+      for (int c = g.s[f].c0 + 1 + SB; c <= g.s[f].c1; ++c) acc += g.q[f][sk_slot(p, c, 0)];
+    out[f] = g.on[f] ? acc : 0.f;
   }
+}
+template <int NF, int SB = kSegBatch>
+SPEC_DEV void sk_sum_n(const float* __restrict__ part, const SKPlan& p, int m, const int (&n)[NF],
+                       const bool (&on)[NF], float (&out)[NF]) {
+  SKGather<NF, SB> g;
+  sk_gather<NF, SB>(part, p, m, n, on, g);
+  sk_reduce<NF, SB>(p, g, out);
 }
 
 SPEC_DEV float sk_sum(const float* __restrict__ part, const SKPlan& p, int m, int n) {

@@ -164,30 +164,39 @@ __global__ void __launch_bounds__(256) tree_expand_kernel(TreeDims td, int d, co
     s_order[r] = p;    // final index r + 1
   }
   __syncthreads();
+  // final index of every selected node; then one thread per node writes its
+  // outputs, and its mask is the OR of its ancestors' bits (final parents come
+  // first in the numbering, so the chain ends at the root)
+  for (int n = threadIdx.x; n < N; n += blockDim.x) s_map[s_order[n]] = n + 1;
+  __syncthreads();
+  __shared__ int s_pf[64];
+  const size_t o = (size_t)b * (N + 1);
+  const int ctx = ctx_len[b];
+  for (int n = 1 + threadIdx.x; n <= N; n += blockDim.x) {
+    const int p = s_order[n - 1];
+    const int par = tv.parent[p];
+    int pf = (par < 0) ? 0 : s_map[par];
+    if (pf < 0 || pf >= n) pf = 0;   // cannot happen: the selection is ancestor-closed
+    s_pf[n] = pf;
+    io.tree_tok[o + n] = tv.tok[p];
+    io.tree_parent[o + n] = pf;
+    io.tree_depth[o + n] = s_depth[p];
+    io.tree_pos[o + n] = ctx + s_depth[p];
+    io.tree_score[o + n] = s_score[p];
+  }
   if (threadIdx.x == 0) {
-    const size_t o = (size_t)b * (N + 1);
-    for (int n = 1; n <= N; ++n) s_map[s_order[n - 1]] = n;
     io.tree_tok[o] = tv.count[1];
     io.tree_parent[o] = -1;
     io.tree_depth[o] = 0;
-    io.tree_pos[o] = ctx_len[b];
+    io.tree_pos[o] = ctx;
     io.tree_score[o] = 0.f;
     io.tree_mask[o] = 1ull;
-    unsigned long long masks[64];
-    masks[0] = 1ull;
-    for (int n = 1; n <= N; ++n) {
-      const int p = s_order[n - 1];
-      const int par = tv.parent[p];
-      int pf = (par < 0) ? 0 : s_map[par];
-      if (pf < 0 || pf >= n) pf = 0;   // cannot happen: the selection is ancestor-closed
-      masks[n] = masks[pf] | (1ull << n);
-      io.tree_tok[o + n] = tv.tok[p];
-      io.tree_parent[o + n] = pf;
-      io.tree_depth[o + n] = tv.depth[p];
-      io.tree_pos[o + n] = ctx_len[b] + tv.depth[p];
-      io.tree_score[o + n] = tv.score[p];
-      io.tree_mask[o + n] = masks[n];
-    }
+  }
+  __syncthreads();
+  for (int n = 1 + threadIdx.x; n <= N; n += blockDim.x) {
+    unsigned long long msk = 1ull;
+    for (int a = n; a > 0; a = s_pf[a]) msk |= 1ull << a;
+    io.tree_mask[o + n] = msk;
   }
 }
 
