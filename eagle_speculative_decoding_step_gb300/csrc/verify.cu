@@ -21,6 +21,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_core.cuh"
 
 namespace spec {
 
@@ -76,6 +77,71 @@ __device__ bool last_arrival(int* counter, int total, int* s_flag) {
   return *s_flag != 0;
 }
 
+// ---------------------------------------------------------------- chunk streaming
+// A chunk [lo, hi) of a 16-byte aligned fp32 row (lo and hi - lo multiples of 4)
+// passes through a ring of kVStages shared-memory stages of kVStage floats that
+// thread 0 fills with bulk copies (cp.async.bulk) kVStages ahead, so the
+// copies in flight do not depend on registers.  Thread t calls f(j, v) for the
+// 4-float group at offset 4t + 1024u (u < 4) of every stage: the same
+// thread-to-element order as a loop of four 16-byte loads per thread over the
+// chunk.  256 threads.  Every wait is bounded (2 s); the block leaves the loop
+// together (a vote per stage), waits for the copies it issued and returns false.
+constexpr int kVStages = 4, kVStage = 4096;
+constexpr int kVStreamMin = 4 * kVStage;     // shorter chunks keep the register loop
+constexpr size_t kVRingBytes = (size_t)kVStages * kVStage * 4 + 8 * kVStages;
+
+template <class F>
+__device__ bool stream_chunk(const float* __restrict__ x, int lo, int hi, uint8_t* ring, F&& f) {
+  float* buf = reinterpret_cast<float*>(ring);
+  const uint32_t bar0 = tc::su32(ring + (size_t)kVStages * kVStage * 4);
+  __shared__ int s_abort;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < kVStages; ++i) tc::mbar_init(bar0 + 8u * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int nst = (hi - lo + kVStage - 1) / kVStage;
+  auto issue = [&](int k) {
+    const int base = lo + k * kVStage;
+    const uint32_t bytes = (uint32_t)min(kVStage, hi - base) * 4u;
+    const uint32_t bar = bar0 + 8u * (uint32_t)(k % kVStages);
+    tc::mbar_expect_tx(bar, bytes);
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(tc::su32(buf + (size_t)(k % kVStages) * kVStage)), "l"(x + base), "r"(bytes), "r"(bar)
+                 : "memory");
+  };
+  if (threadIdx.x == 0)
+    for (int k = 0; k < min(kVStages, nst); ++k) issue(k);
+  int k = 0;
+  for (; k < nst; ++k) {
+    const int slot = k % kVStages;
+    const bool w = tc::mbar_wait(bar0 + 8u * slot, (uint32_t)(k / kVStages) & 1u, &s_abort);
+    if (w) {
+      const int base = lo + k * kVStage, n = min(kVStage, hi - base);
+      const float* sb = buf + (size_t)slot * kVStage;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int o = 4 * threadIdx.x + 1024 * u;
+        if (o >= n) break;
+        const float4 q = *reinterpret_cast<const float4*>(sb + o);
+        const float v[4] = {q.x, q.y, q.z, q.w};
+        f(base + o, v);
+      }
+    }
+    if (!__syncthreads_and(w)) break;          // every thread is done with the slot
+    if (threadIdx.x == 0 && k + kVStages < nst) issue(k + kVStages);
+  }
+  if (k == nst) return true;
+  // the copies issued for stages k .. min(k + kVStages, nst) - 1 land before the
+  // shared memory is given up
+  if (threadIdx.x == 0)
+    for (int q = k; q < min(k + kVStages, nst); ++q)
+      tc::mbar_wait(bar0 + 8u * (uint32_t)(q % kVStages), (uint32_t)(q / kVStages) & 1u, &s_abort, false);
+  __syncthreads();
+  return false;
+}
+
 // ---------------------------------------------------------------- greedy
 // One launch: CTA (c, row) reduces chunk c of a logits row to its argmax; the
 // last CTA of a request to finish (completion counter, no waiting) merges the
@@ -115,6 +181,10 @@ __device__ void compact_path(const spec_kv& kv, int b, int ctx, const int* src, 
   }
 }
 
+// Chunk records of one request the deciding CTA stages in shared memory at once
+// (more are read row by row).
+constexpr int kStageRecs = 1024;
+
 struct GreedyArgs {
   const float* logits;
   int V, R, nch, L;
@@ -148,8 +218,16 @@ __global__ void __launch_bounds__(256) verify_greedy_kernel(GreedyArgs g) {
   const int lo = c * g.L, hi = min(V, lo + g.L);
   float bv = -INFINITY;
   int bi = 0x7fffffff;
-  if (VEC) {
-    // four 16-byte loads in flight per thread
+  if (VEC && g.L >= kVStreamMin) {
+    extern __shared__ __align__(128) uint8_t vring[];   // chunk ring (kVRingBytes)
+    const bool ok = stream_chunk(x, lo, hi, vring, [&](int j, const float* v) {
+#pragma unroll
+      for (int l = 0; l < 4; ++l)
+        if (better(v[l], j + l, bv, bi)) { bv = v[l]; bi = j + l; }
+    });
+    if (!ok && threadIdx.x == 0) report(g.ws, SPEC_ERR_TIMEOUT, row, c);
+  } else if (VEC) {
+    // short chunks: four 16-byte loads in flight per thread
     for (int j0 = lo + 4 * threadIdx.x; j0 < hi; j0 += 16 * blockDim.x) {
       float4 q[4];
 #pragma unroll
@@ -162,9 +240,9 @@ __global__ void __launch_bounds__(256) verify_greedy_kernel(GreedyArgs g) {
         const int j = j0 + 4 * u * blockDim.x;
         if (j >= hi) break;
         if (better(q[u].x, j, bv, bi)) { bv = q[u].x; bi = j; }
-        if (j + 1 < hi && better(q[u].y, j + 1, bv, bi)) { bv = q[u].y; bi = j + 1; }
-        if (j + 2 < hi && better(q[u].z, j + 2, bv, bi)) { bv = q[u].z; bi = j + 2; }
-        if (j + 3 < hi && better(q[u].w, j + 3, bv, bi)) { bv = q[u].w; bi = j + 3; }
+        if (better(q[u].y, j + 1, bv, bi)) { bv = q[u].y; bi = j + 1; }
+        if (better(q[u].z, j + 2, bv, bi)) { bv = q[u].z; bi = j + 2; }
+        if (better(q[u].w, j + 3, bv, bi)) { bv = q[u].w; bi = j + 3; }
       }
     }
   } else {
@@ -183,7 +261,35 @@ __global__ void __launch_bounds__(256) verify_greedy_kernel(GreedyArgs g) {
   if (!last_arrival(&g.cnt[b], R * g.nch, &s_last)) return;
 
   // ---- the request's last CTA: decisions, outputs, K/V compaction
-  for (int n = threadIdx.x; n < R; n += blockDim.x) t[n] = merged_argmax(g.part, b * R + n, g.nch);
+  if (R * g.nch <= kStageRecs) {
+    // every chunk record of the request loaded at once, then each row merged from
+    // shared memory in chunk order
+    __shared__ ArgPart s_rec[kStageRecs];
+    const ArgPart* src = g.part + (size_t)b * R * g.nch;
+    ArgPart rec[kStageRecs / 256];
+#pragma unroll
+    for (int u = 0; u < kStageRecs / 256; ++u) {
+      const int e = threadIdx.x + 256 * u;
+      if (e < R * g.nch) rec[u] = ArgPart{__ldcg(&src[e].v), __ldcg(&src[e].i)};
+    }
+#pragma unroll
+    for (int u = 0; u < kStageRecs / 256; ++u) {
+      const int e = threadIdx.x + 256 * u;
+      if (e < R * g.nch) s_rec[e] = rec[u];
+    }
+    __syncthreads();
+    for (int n = threadIdx.x; n < R; n += blockDim.x) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int c = 0; c < g.nch; ++c) {
+        const ArgPart q = s_rec[n * g.nch + c];
+        if (better(q.v, q.i, bv, bi)) { bv = q.v; bi = q.i; }
+      }
+      t[n] = bi;
+    }
+  } else {
+    for (int n = threadIdx.x; n < R; n += blockDim.x) t[n] = merged_argmax(g.part, b * R + n, g.nch);
+  }
   __syncthreads();
   const int W = (g.parent == nullptr) ? R : g.max_depth + 1;
   if (threadIdx.x == 0) {
@@ -466,7 +572,7 @@ struct RejArgs {
 };
 
 template <bool VEC>
-__device__ void rej_stats(const RejArgs& g, int row, int c, float* red, int* redi) {
+__device__ void rej_stats(const RejArgs& g, int row, int c, float* red, int* redi, uint8_t* ring) {
   const int K = g.K, V = g.V;
   const Thr tr = g.thr ? g.thr[row] : Thr{0u, 0x7fffffff};
   const int b = row / (K + 1);
@@ -478,47 +584,54 @@ __device__ void rej_stats(const RejArgs& g, int row, int c, float* red, int* red
   const int lo = c * g.L, hi = min(V, lo + g.L);
   float m = -INFINITY, s = 0.f, bk = -INFINITY;
   int bi = 0x7fffffff;
-  constexpr int UNR = 4;                      // 16-byte loads in flight per thread
-  for (int j0 = lo + 4 * threadIdx.x; j0 < hi; j0 += 4 * UNR * blockDim.x) {
-    float vv[UNR][4];
+  // one group of four ids j .. j + 3 (ids past hi are ignored)
+  auto group = [&](int j, const float* v) {
+    if (greedy) {
 #pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const int j = j0 + 4 * u * blockDim.x;
-      if (VEC) {
-        if (j < hi) {
-          const float4 q = *reinterpret_cast<const float4*>(x + j);
-          vv[u][0] = q.x; vv[u][1] = q.y; vv[u][2] = q.z; vv[u][3] = q.w;
-        }
-      } else {
-#pragma unroll
-        for (int l = 0; l < 4; ++l) vv[u][l] = (j + l < hi) ? x[j + l] : -INFINITY;
-      }
+      for (int l = 0; l < 4; ++l)
+        if (j + l < hi && better(v[l], j + l, bk, bi)) { bk = v[l]; bi = j + l; }
+      return;
     }
+    // the group's kept values, -inf for the rest (ids past hi, filtered by top-k / top-p)
+    float y[4];
 #pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const int j = j0 + 4 * u * blockDim.x;
-      if (j >= hi) break;
-      const float* v = vv[u];
-      if (greedy) {
+    for (int l = 0; l < 4; ++l) {
+      y[l] = (j + l < hi) ? (unit ? v[l] : v[l] / T) : -INFINITY;
+      if (filt && y[l] > -INFINITY && !kept_by(tr, okey(y[l]), j + l)) y[l] = -INFINITY;
+    }
+    // online sum of exp: one max update per group of four
+    const float gm = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
+    if (gm > m) {
+      s *= __expf(m - gm);
+      m = gm;
+    }
+    if (m > -INFINITY) s += (__expf(y[0] - m) + __expf(y[1] - m)) + (__expf(y[2] - m) + __expf(y[3] - m));
+  };
+  if (VEC && g.L >= kVStreamMin) {
+    if (!stream_chunk(x, lo, hi, ring, group) && threadIdx.x == 0) report(g.ws, SPEC_ERR_TIMEOUT, row, c);
+  } else {
+    constexpr int UNR = 4;                    // 16-byte loads in flight per thread
+    for (int j0 = lo + 4 * threadIdx.x; j0 < hi; j0 += 4 * UNR * blockDim.x) {
+      float vv[UNR][4];
 #pragma unroll
-        for (int l = 0; l < 4; ++l)
-          if (j + l < hi && better(v[l], j + l, bk, bi)) { bk = v[l]; bi = j + l; }
-        continue;
-      }
-      // the group's kept values, -inf for the rest (ids past hi, filtered by top-k / top-p)
-      float y[4];
+      for (int u = 0; u < UNR; ++u) {
+        const int j = j0 + 4 * u * blockDim.x;
+        if (VEC) {
+          if (j < hi) {
+            const float4 q = *reinterpret_cast<const float4*>(x + j);
+            vv[u][0] = q.x; vv[u][1] = q.y; vv[u][2] = q.z; vv[u][3] = q.w;
+          }
+        } else {
 #pragma unroll
-      for (int l = 0; l < 4; ++l) {
-        y[l] = (j + l < hi) ? (unit ? v[l] : v[l] / T) : -INFINITY;
-        if (filt && y[l] > -INFINITY && !kept_by(tr, okey(y[l]), j + l)) y[l] = -INFINITY;
+          for (int l = 0; l < 4; ++l) vv[u][l] = (j + l < hi) ? x[j + l] : -INFINITY;
+        }
       }
-      // online sum of exp: one max update per group of four
-      const float gm = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
-      if (gm > m) {
-        s *= __expf(m - gm);
-        m = gm;
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int j = j0 + 4 * u * blockDim.x;
+        if (j >= hi) break;
+        group(j, vv[u]);
       }
-      if (m > -INFINITY) s += (__expf(y[0] - m) + __expf(y[1] - m)) + (__expf(y[2] - m) + __expf(y[3] - m));
     }
   }
   const float bm = block_max(m, red);
@@ -596,25 +709,38 @@ __device__ void rej_sample(const RejArgs& g, int b, int c, int i, float* red, in
   const int lo = c * g.Ls, hi = min(V, lo + g.Ls);
   float bk = -INFINITY;
   int bi = 0x7fffffff;
-  // every thread handles aligned groups of 4 vocabulary ids = one Philox block
-  for (int j = lo + 4 * threadIdx.x; j < hi; j += 4 * blockDim.x) {
-    float v[4];
-    if (VEC) {
-      float4 q = *reinterpret_cast<const float4*>(x + j);
-      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-    } else {
+  // every thread handles aligned groups of 4 vocabulary ids = one Philox block;
+  // the logits of two groups are loaded before the first one's noise is drawn
+  constexpr int SB = 2;
+  for (int j0 = lo + 4 * threadIdx.x; j0 < hi; j0 += 4 * SB * blockDim.x) {
+    float v[SB][4];
 #pragma unroll
-      for (int l = 0; l < 4; ++l) v[l] = (j + l < hi) ? x[j + l] : -INFINITY;
+    for (int u = 0; u < SB; ++u) {
+      const int j = j0 + 4 * u * blockDim.x;
+      if (VEC) {
+        if (j < hi) {
+          const float4 q = *reinterpret_cast<const float4*>(x + j);
+          v[u][0] = q.x; v[u][1] = q.y; v[u][2] = q.z; v[u][3] = q.w;
+        }
+      } else {
+#pragma unroll
+        for (int l = 0; l < 4; ++l) v[u][l] = (j + l < hi) ? x[j + l] : -INFINITY;
+      }
     }
-    const uint4 r = philox4x32_10(make_uint4((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b, g.w0 + 1u), g.key);
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int l = 0; l < 4; ++l) {
-      if (j + l >= hi) break;
-      const float y = unit ? v[l] : v[l] / T;
-      if (j + l == excl || !kept_by(tr, okey(y), j + l)) continue;
-      const float gk = y - logf(-logf(word_to_uniform(w[l])));
-      if (better(gk, j + l, bk, bi)) { bk = gk; bi = j + l; }
+    for (int u = 0; u < SB; ++u) {
+      const int j = j0 + 4 * u * blockDim.x;
+      if (j >= hi) break;
+      const uint4 r = philox4x32_10(make_uint4((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b, g.w0 + 1u), g.key);
+      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int l = 0; l < 4; ++l) {
+        if (j + l >= hi) break;
+        const float y = unit ? v[u][l] : v[u][l] / T;
+        if (j + l == excl || !kept_by(tr, okey(y), j + l)) continue;
+        const float gk = y - logf(-logf(word_to_uniform(w[l])));
+        if (better(gk, j + l, bk, bi)) { bk = gk; bi = j + l; }
+      }
     }
   }
   block_argmax(bk, bi, red, redi);
@@ -622,9 +748,10 @@ __device__ void rej_sample(const RejArgs& g, int b, int c, int i, float* red, in
 }
 
 template <bool VEC>
-__global__ void __launch_bounds__(256) verify_rejection_kernel(RejArgs g) {
+__global__ void __launch_bounds__(256, 3) verify_rejection_kernel(RejArgs g) {
   pdl_wait();
   pdl_trigger();
+  extern __shared__ __align__(128) uint8_t vring[];   // chunk ring (VEC: kVRingBytes)
   __shared__ float red[32];
   __shared__ int redi[32];
   __shared__ int s_t, s_flag, s_ok, s_i;
@@ -635,7 +762,7 @@ __global__ void __launch_bounds__(256) verify_rejection_kernel(RejArgs g) {
   const int K = g.K;
   if (t < nstat) {
     const int row = t / g.nch, c = t % g.nch, b = row / (K + 1);
-    rej_stats<VEC>(g, row, c, red, redi);
+    rej_stats<VEC>(g, row, c, red, redi, vring);
     if (last_arrival(&g.cnt[b], (K + 1) * g.nch, &s_flag)) {
       if (threadIdx.x < 32) rej_decide(g, b);
       if (threadIdx.x == 0) {
@@ -762,6 +889,19 @@ static spec_status greedy_args(int32_t B, int32_t R, int32_t V, const float* tar
   return SPEC_OK;
 }
 
+// The chunk ring's dynamic shared memory, allowed once per device and kernel.
+template <class K>
+static bool ring_attr(K* kern) {
+  static int done_dev = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (done_dev == dev) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kVRingBytes) != cudaSuccess)
+    return false;
+  done_dev = dev;
+  return true;
+}
+
 static spec_status launch_greedy(GreedyArgs g, int B, void* ws, const VLayout& L, cudaStream_t stream) {
   g.nch = L.nch;
   g.L = chunk_len(g.V, L.nch);
@@ -771,8 +911,11 @@ static spec_status launch_greedy(GreedyArgs g, int B, void* ws, const VLayout& L
   g.ws = ws;
   const dim3 grid(L.nch, B * g.R);
   const bool vec = (g.V % 4 == 0) && aligned(g.logits, 16);
-  if (vec)
-    launch_pdl(verify_greedy_kernel<true>, grid, dim3(256), 0, stream, g);
+  if (vec) {
+    const bool ring = g.L >= kVStreamMin;
+    if (ring && !ring_attr(verify_greedy_kernel<true>)) return SPEC_ERR_CUDA;
+    launch_pdl(verify_greedy_kernel<true>, grid, dim3(256), ring ? kVRingBytes : 0, stream, g);
+  }
   else
     launch_pdl(verify_greedy_kernel<false>, grid, dim3(256), 0, stream, g);
   return last_launch();
@@ -844,8 +987,11 @@ extern "C" spec_status spec_verify_rejection(int32_t B, int32_t K, int32_t V, co
     g.thr = thr;
   }
   const bool vec = (V % 4 == 0) && aligned(target_logits, 16);
-  if (vec)
-    launch_pdl(verify_rejection_kernel<true>, dim3(g.ncta), dim3(256), 0, stream, g);
+  if (vec) {
+    const bool ring = g.L >= kVStreamMin;
+    if (ring && !ring_attr(verify_rejection_kernel<true>)) return SPEC_ERR_CUDA;
+    launch_pdl(verify_rejection_kernel<true>, dim3(g.ncta), dim3(256), ring ? kVRingBytes : 0, stream, g);
+  }
   else
     launch_pdl(verify_rejection_kernel<false>, dim3(g.ncta), dim3(256), 0, stream, g);
   return last_launch();
