@@ -378,46 +378,57 @@ def run_workload(args, w, dist, device, world):
     dom["peak_kind"] = kind + " (burst copy)"
 
     # end to end through the public API with host buffers: every step copies its inputs
-    # H2D from pinned memory and reads its result back.  The target logits are read only
-    # by verification, so their copy runs while the step drafts; all of the step's input
-    # copies go on one copy stream, the drafting inputs first (copies on one stream run in
-    # order, so the large logits copy cannot hold up the small ones drafting waits for), and
-    # they wait for the previous step's verification (same buffers); drafting and
-    # verification replay as two graphs with the copies' events between.
+    # H2D from pinned memory and reads its result back.  Two sets of device input
+    # buffers (aux features, root tokens, target logits) alternate between steps, each
+    # with its own pair of graphs (drafting, verification): step s's copies go on a copy
+    # stream as soon as step s-2 (the last user of that set) is verified, so they run
+    # while step s-1 computes; on the copy stream the drafting inputs come first, then
+    # the target logits, which only verification reads.
     aux_h = aux_d.cpu().pin_memory()
     root_h = root_d.cpu().pin_memory()
     tgt_h = target.cpu().pin_memory()
     out_h = torch.empty(tuple(st.out.shape), dtype=torch.int32).pin_memory()
     acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
-    g_draft, g_verify = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    sets = [(aux_d, root_d, target), (torch.empty_like(aux_d), torch.empty_like(root_d), torch.empty_like(target))]
+    graphs = []
     with torch.cuda.stream(stream):
-        with torch.cuda.graph(g_draft, stream=stream):
-            st.draft()
-        with torch.cuda.graph(g_verify, stream=stream):
-            st.verify()
+        for a_d, r_d, t_d in sets:
+            st.aux, st.root, st.target = a_d, r_d, t_d
+            g_draft, g_verify = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_draft, stream=stream):
+                st.draft()
+            with torch.cuda.graph(g_verify, stream=stream):
+                st.verify()
+            graphs.append((g_draft, g_verify))
+    st.aux, st.root, st.target = sets[0]
     torch.cuda.synchronize()
     copy_stream = torch.cuda.Stream(device=device)
-    in_ready, t_ready, v_done = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
-    n_e2e = max(3, args.steps // 2)
+    in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+    t_ready = [torch.cuda.Event(), torch.cuda.Event()]
+    v_done = [torch.cuda.Event(), torch.cuda.Event()]
+    n_e2e = max(4, args.steps // 2)
     with torch.cuda.stream(stream):
         b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         b0.record(stream)
-        v_done.record(stream)
-        for _ in range(n_e2e):
-            copy_stream.wait_event(v_done)
+        v_done[0].record(stream)
+        v_done[1].record(stream)
+        for s_i in range(n_e2e):
+            k = s_i % 2
+            a_d, r_d, t_d = sets[k]
+            copy_stream.wait_event(v_done[k])
             with torch.cuda.stream(copy_stream):
-                aux_d.copy_(aux_h, non_blocking=True)
-                root_d.copy_(root_h, non_blocking=True)
-                in_ready.record(copy_stream)
-                target.copy_(tgt_h, non_blocking=True)
-                t_ready.record(copy_stream)
-            stream.wait_event(in_ready)
-            g_draft.replay()
-            stream.wait_event(t_ready)
-            g_verify.replay()
+                a_d.copy_(aux_h, non_blocking=True)
+                r_d.copy_(root_h, non_blocking=True)
+                in_ready[k].record(copy_stream)
+                t_d.copy_(tgt_h, non_blocking=True)
+                t_ready[k].record(copy_stream)
+            stream.wait_event(in_ready[k])
+            graphs[k][0].replay()
+            stream.wait_event(t_ready[k])
+            graphs[k][1].replay()
             out_h.copy_(st.out, non_blocking=True)
             acc_h.copy_(st.acc, non_blocking=True)
-            v_done.record(stream)
+            v_done[k].record(stream)
         b1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(b0.elapsed_time(b1) / n_e2e, dist, device)
@@ -435,7 +446,8 @@ def run_workload(args, w, dist, device, world):
         "roofline": dom,
         "e2e": {"value": world * 1000.0 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "overlap": "inputs then target logits copied on a side stream; drafting starts after the inputs"},
+                "overlap": "two input buffer sets: a step's inputs and target logits are copied on a side "
+                           "stream while the previous step computes"},
         "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clocks, "setup_s": gen_s, "config": config_of(w),
     }
@@ -643,6 +655,56 @@ def summary(r):
     return {k: r[k] for k in keep}
 
 
+def run_timeline(args, w):
+    """The workload's step, captured as in the bench, replayed three times with the
+    instrumented library's per-block log attached; writes the last step's per-kernel
+    table and launch sequence (markdown) to args.timeline."""
+    os.environ["EAGLESPEC_TIMELINE"] = "1"
+    from eagle_speculative_decoding_step_gb300 import build
+    build.build(timeline=True)
+    import torch
+    from eagle_speculative_decoding_step_gb300 import binding as lib, engine, timeline
+    device = "cuda:0"
+    L = lib.load()
+    W = synth.make_weights(w)
+    if w.rank > 0:
+        W["lr_down"], W["lr_up"] = synth.lowrank_factors(W["lm_head"], w.rank, w.dtype)
+    ctx = synth.context_lengths(w)
+    kv = synth.make_kv(w, ctx)
+    aux = synth.make_aux(w)
+    root = synth.root_tokens(w)
+    dm = engine.DeviceModel(w, W, kv, ctx, device=device)
+    del W, kv
+    aux_d = engine.to_device(aux, w.dtype, device)
+    root_d = torch.from_numpy(root).to(device)
+    st = build_tree_step(w, dm, aux_d, root_d, device) if w.mode == "tree" else \
+        build_chain_step(w, dm, aux_d, root_d, device)
+    for _ in range(max(1, args.warmup)):
+        st.run()
+    stream = torch.cuda.Stream(device=device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            st.run()
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    log = torch.zeros(timeline.LOG_WORDS, dtype=torch.int64, device=device)
+    timeline.attach(L, log.data_ptr())
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+    torch.cuda.synchronize()
+    timeline.attach(L, 0)
+    assert dm.device_error() == 0, "device error"
+    step = timeline.last_step(timeline.launches(log.cpu().numpy()))
+    with open(args.timeline, "w") as f:
+        f.write("# Timeline: %s, one graph-replayed step (instrumented build)\n\n" % w.name)
+        f.write(timeline.markdown(step) + "\n\nLaunch sequence (us from the step's first launch: start, end, "
+                "duration, kernel, blocks):\n\n```\n" + timeline.sequence(step) + "\n```\n")
+    print(timeline.markdown(step))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -653,6 +715,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub", action="store_true", help="headline workload only")
     ap.add_argument("--oracle-probe", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--timeline", default=None, metavar="FILE",
+                    help="instead of the bench line: per-kernel timeline of the workload's graph-replayed step "
+                         "from the instrumented library (markdown to FILE)")
     args = ap.parse_args()
     if args.oracle_probe:
         print(json.dumps(oracle_probe(args.oracle_probe, max(1, args.steps))))
@@ -666,6 +731,9 @@ def main():
         print(json.dumps(run_reference(args, w)))
         return
 
+    if args.timeline:
+        run_timeline(args, w)
+        return
     import torch
     from eagle_speculative_decoding_step_gb300 import binding as lib
     world = int(os.environ.get("WORLD_SIZE", "1"))

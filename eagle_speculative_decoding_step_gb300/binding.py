@@ -11,7 +11,10 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libeaglespec.so")
+# EAGLESPEC_TIMELINE=1 loads the instrumented build (build(timeline=True)): the same
+# library with per-block start / end stamps, for timeline.py only
+LIB_PATH = os.path.join(_HERE, "libeaglespec_timeline.so" if os.environ.get("EAGLESPEC_TIMELINE") == "1"
+                        else "libeaglespec.so")
 
 c_i32 = ctypes.c_int32
 c_u64 = ctypes.c_uint64

@@ -19,6 +19,55 @@ struct WsHeader {
 };
 constexpr size_t kWsHeader = 256;
 
+// ---------------------------------------------------------------- timeline (instrumented build)
+// Compiled only with SPEC_TIMELINE (libeaglespec_timeline.so): thread 0 of every
+// block of every kernel takes a slot of the log set by spec_timeline_set_<unit>
+// (one per translation unit) and writes the global timer at its start and at
+// its exit, with kernel id | grid size << 8 | block index << 32.  Log layout
+// (u64): [0] slot counter, then 4 words a slot from index 8.  The product
+// build has none of this (SPEC_TL expands to nothing).
+enum TLKernel : unsigned {
+  kTLTc = 1, kTLAttnWs, kTLAttnMma, kTLAttnSplit, kTLCombine, kTLPrologue, kTLEpiStore, kTLEpiQkv,
+  kTLResnorm, kTLSwiglu, kTLSimt, kTLRowStats, kTLTopk, kTLRescore, kTLCandBest, kTLLmMerge, kTLTree,
+  kTLGreedy, kTLRejection, kTLThreshold, kTLPrefill, kTLMetadata, kTLGather
+};
+#ifdef SPEC_TIMELINE
+static __device__ unsigned long long* g_spec_tl;
+constexpr unsigned kTLSlots = 1u << 20;
+SPEC_DEV unsigned long long tl_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+struct TLRec {
+  unsigned idx = 0xffffffffu;
+  SPEC_DEV bool first() const { return threadIdx.x == 0 && threadIdx.y == 0 && threadIdx.z == 0; }
+  SPEC_DEV explicit TLRec(unsigned id) {
+    if (first() && g_spec_tl != nullptr) {
+      const unsigned i = atomicAdd(reinterpret_cast<unsigned*>(g_spec_tl), 1u);
+      if (i < kTLSlots) {
+        idx = i;
+        unsigned long long* e = g_spec_tl + 8 + 4ull * i;
+        e[0] = tl_now();
+        e[3] = (unsigned long long)id | ((unsigned long long)(gridDim.x * gridDim.y) << 8) |
+               ((unsigned long long)(blockIdx.x + gridDim.x * blockIdx.y) << 32);
+      }
+    }
+  }
+  SPEC_DEV ~TLRec() {
+    if (idx != 0xffffffffu) g_spec_tl[8 + 4ull * idx + 2] = tl_now();
+  }
+};
+#define SPEC_TL(id) ::spec::TLRec spec_tl_rec_(id)
+#define SPEC_TL_SETTER(unit)                                                   \
+  extern "C" int spec_timeline_set_##unit(void* p) {                          \
+    return (int)cudaMemcpyToSymbol(::spec::g_spec_tl, &p, sizeof(p));          \
+  }
+#else
+#define SPEC_TL(id) ((void)0)
+#define SPEC_TL_SETTER(unit)
+#endif
+
 SPEC_DEV void report(void* ws, int code, int a = 0, int b = 0) {
   if (ws == nullptr) return;
   WsHeader* h = reinterpret_cast<WsHeader*>(ws);

@@ -109,6 +109,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
     prologue_kernel(RowInfo ri, int H, int V, int hd, float eps, const __grid_constant__ RopeFreq rf,
                     const T* __restrict__ embed, const T* __restrict__ g_in, const T* __restrict__ g_hid,
                     const T* __restrict__ hid_in, T* __restrict__ x, float2* __restrict__ cs, void* ws) {
+  SPEC_TL(spec::kTLPrologue);
   pdl_wait();
   pdl_trigger();
   __shared__ float red[64];
@@ -185,6 +186,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
 template <typename TO>
 __global__ void epi_store_kernel(const float* __restrict__ part, SKPlan p, int M, int N, TO* __restrict__ out,
                                  int ld_out) {
+  SPEC_TL(spec::kTLEpiStore);
   pdl_wait();
   pdl_trigger();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -199,6 +201,7 @@ template <typename T>
 __global__ void epi_qkv_kernel(const float* __restrict__ part, SKPlan p, RowInfo ri, int nq, int nkv, int hd,
                                const float2* __restrict__ cs, T* __restrict__ qbuf, spec_kv kv, int* __restrict__ work,
                                void* ws) {
+  SPEC_TL(spec::kTLEpiQkv);
   pdl_wait();
   pdl_trigger();
   if (work != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *work = 0;   // the attention's item counter
@@ -258,6 +261,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
     resnorm_kernel(const float* __restrict__ part, SKPlan p, RowInfo ri, int H, float eps,
                    const T* __restrict__ hid_in, const T* __restrict__ gain, float* __restrict__ r,
                    T* __restrict__ out_a, T* __restrict__ out_b) {
+  SPEC_TL(spec::kTLResnorm);
   pdl_wait();
   pdl_trigger();
   __shared__ float red[64];
@@ -328,6 +332,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
 template <typename T, int U>
 __global__ void __launch_bounds__(256) epi_swiglu_kernel(const float* __restrict__ part, SKPlan p, int M, int I,
                                                          T* __restrict__ act) {
+  SPEC_TL(spec::kTLSwiglu);
   pdl_wait();
   pdl_trigger();
   const int m = blockIdx.y;
@@ -359,6 +364,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const T* __restrict__ A0, const T* __restrict__ A1,
                                                         const T* __restrict__ A2, int K, const T* __restrict__ X,
                                                         int M, SKPlan p, float* __restrict__ part) {
+  SPEC_TL(spec::kTLSimt);
   pdl_wait();
   pdl_trigger();
   __shared__ float sW[128][65];
@@ -472,6 +478,7 @@ __global__ void __launch_bounds__(128) attn_split_kernel(const T* __restrict__ q
                                                          int nq, int nkv, int window, int nsplit, int nqg,
                                                          int n_items, float scale, float* __restrict__ opart,
                                                          float2* __restrict__ mlpart, void* ws) {
+  SPEC_TL(spec::kTLAttnSplit);
   pdl_wait();
   pdl_trigger();
   using A = AttnShape<T, HD>;
@@ -773,6 +780,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __nv_bfloat16* __re
                                                        int n_items, float scale_log2, float* __restrict__ opart,
                                                        float2* __restrict__ mlpart, int* __restrict__ work,
                                                        void* ws) {
+  SPEC_TL(spec::kTLAttnMma);
   pdl_wait();
   pdl_trigger();
   using Sh = MmaShape<HD>;
@@ -1180,6 +1188,7 @@ __global__ void __launch_bounds__(160, MT == 1 ? 3 : 2) attn_ws_kernel(const __g
                                                          int nqg, int n_items, int bh, float scale_log2,
                                                          float* __restrict__ opart, float2* __restrict__ mlpart,
                                                          int* __restrict__ work, void* ws) {
+  SPEC_TL(spec::kTLAttnWs);
   using S = WsShape<HD, MT>;
   constexpr int TK = S::TK, QM = S::QM, NS = S::NS, NH = S::NH, KP = S::KP, NT = HD / 8, KS = HD / 16;
   constexpr int WPM = 4 / MT, KPW = TK / WPM;   // warps per m-tile, keys per warp
@@ -1618,6 +1627,7 @@ template <typename T, int HD, int NSM>
 __global__ void __launch_bounds__(HD) attn_combine_kernel(const float* __restrict__ opart,
                                                           const float2* __restrict__ mlpart, int nq, int nsplit,
                                                           T* __restrict__ out) {
+  SPEC_TL(spec::kTLCombine);
   pdl_wait();
   pdl_trigger();
   const int mh = blockIdx.x;          // m * nq + h
@@ -1668,6 +1678,7 @@ static void launch_combine(const float* opart, const float2* mlpart, int M, int 
 __global__ void __launch_bounds__(256) row_stats_kernel(const float* __restrict__ logits, int V, int k,
                                                         int32_t* __restrict__ ids, int ld_ids, float* __restrict__ lp,
                                                         float* __restrict__ lse_out, const int32_t* __restrict__ d2t) {
+  SPEC_TL(spec::kTLRowStats);
   pdl_wait();
   pdl_trigger();
   __shared__ float red[32];
@@ -1894,6 +1905,7 @@ SPEC_DEV void select_row_exact(const float* x, int V, int Kc, uint32_t* skey, in
 
 __global__ void __cluster_dims__(kTkCL, 1, 1) __launch_bounds__(1024)
     topk_select_kernel(const float* __restrict__ s, int V, int Kc, int32_t* __restrict__ out_ids) {
+  SPEC_TL(spec::kTLTopk);
   pdl_wait();
   pdl_trigger();
   extern __shared__ __align__(16) uint8_t tk_smem[];
@@ -2091,6 +2103,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) rescore_kernel(const T* __restrict__ hn, const T* __restrict__ lm_head,
                                                       int H, int V, const int32_t* __restrict__ cand, int Kc,
                                                       float* __restrict__ exact, void* ws) {
+  SPEC_TL(spec::kTLRescore);
   pdl_wait();
   pdl_trigger();
   const int m = blockIdx.y;
@@ -2143,6 +2156,7 @@ __global__ void __launch_bounds__(128) cand_best_kernel(const float* __restrict_
                                                         const int32_t* __restrict__ cand, int Kc, int k_out,
                                                         int32_t* __restrict__ out, int ld_out,
                                                         float* __restrict__ out_lp) {
+  SPEC_TL(spec::kTLCandBest);
   pdl_wait();
   pdl_trigger();
   __shared__ float red[32];
@@ -2497,3 +2511,6 @@ void launch_cand_best(const float* exact, const int32_t* cand, int M, int Kc, in
 }
 
 }  // namespace spec
+
+// per-unit log setter of the instrumented build (no-op otherwise)
+SPEC_TL_SETTER(layer)

@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(256) lm_merge_kernel(const float* __restrict__
                                                        int32_t* __restrict__ ids, int ld_ids,
                                                        float* __restrict__ lp, float* __restrict__ lse_out,
                                                        const int32_t* __restrict__ d2t) {
+  SPEC_TL(spec::kTLLmMerge);
   pdl_wait();
   pdl_trigger();
   constexpr int REC = 2 + 2 * KT;
@@ -346,3 +347,6 @@ spec_status launch_lm_head_fused(const spec_model_desc& d, const void* hn, const
 }
 
 }  // namespace spec
+
+// per-unit log setter of the instrumented build (no-op otherwise)
+SPEC_TL_SETTER(lmhead)

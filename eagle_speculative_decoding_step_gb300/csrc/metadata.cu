@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(1024) spec_metadata_kernel(int R, const int32_
                                                              int32_t* __restrict__ cu_nd, int32_t* __restrict__ logits,
                                                              int32_t* __restrict__ target, int32_t* __restrict__ bonus,
                                                              int32_t* __restrict__ draft_ids, void* ws) {
+  SPEC_TL(spec::kTLMetadata);
   pdl_wait();
   pdl_trigger();
   __shared__ int wsum[32];
@@ -96,3 +97,6 @@ extern "C" spec_status spec_decode_metadata(int32_t R, const int32_t* cu_num_sch
              cu_num_draft, logits_indices, target_logits_indices, bonus_logits_indices, draft_token_ids, ws);
   return last_launch();
 }
+
+// per-unit log setter of the instrumented build (no-op otherwise)
+SPEC_TL_SETTER(metadata)

@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(256) prefill_inputs_kernel(int B, int R, const
                                                              int32_t* __restrict__ kv_idx,
                                                              uint64_t* __restrict__ mask, int32_t* __restrict__ last_row,
                                                              int32_t* __restrict__ ctx_next, void* ws) {
+  SPEC_TL(spec::kTLPrefill);
   pdl_wait();
   pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(256) prefill_inputs_kernel(int B, int R, const
 
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ rows,
                                                           int n_src, int chunks, uint4* __restrict__ dst, void* ws) {
+  SPEC_TL(spec::kTLGather);
   pdl_wait();
   pdl_trigger();
   const int r = blockIdx.y;
@@ -86,3 +88,6 @@ extern "C" spec_status spec_gather_rows(const void* src, int32_t n_src, int32_t 
              chunks, reinterpret_cast<uint4*>(dst), ws);
   return last_launch();
 }
+
+// per-unit log setter of the instrumented build (no-op otherwise)
+SPEC_TL_SETTER(prefill)

@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const __grid_constant__ CUtensorMap tA2, const __grid_constant__ CUtensorMap tB,
               const __grid_constant__ typename Sched::Params sp, const __grid_constant__ typename Epi::Params ep,
               void* ws) {
+  SPEC_TL(spec::kTLTc);
   using C = Cfg<MPAD, Epi::kScratch>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];

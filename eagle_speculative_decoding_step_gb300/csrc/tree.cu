@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(256) tree_expand_kernel(TreeDims td, int d, co
                                                           const int32_t* __restrict__ ids,
                                                           const float* __restrict__ lp, void* state,
                                                           spec_tree_io io) {
+  SPEC_TL(spec::kTLTree);
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
@@ -237,3 +238,6 @@ extern "C" spec_status spec_tree_expand(int32_t B, int32_t top_k, int32_t depth_
                                             *io);
   return last_launch();
 }
+
+// per-unit log setter of the instrumented build (no-op otherwise)
+SPEC_TL_SETTER(tree)

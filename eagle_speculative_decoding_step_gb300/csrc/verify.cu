@@ -205,6 +205,7 @@ struct GreedyArgs {
 
 template <bool VEC>
 __global__ void __launch_bounds__(256) verify_greedy_kernel(GreedyArgs g) {
+  SPEC_TL(spec::kTLGreedy);
   pdl_wait();
   pdl_trigger();
   __shared__ float rv[32];
@@ -411,6 +412,7 @@ __global__ void __launch_bounds__(1024) reject_threshold_kernel(const float* __r
                                                                 const float* __restrict__ temperature,
                                                                 const int32_t* __restrict__ top_k,
                                                                 const float* __restrict__ top_p, Thr* __restrict__ thr) {
+  SPEC_TL(spec::kTLThreshold);
   pdl_wait();
   pdl_trigger();
   __shared__ unsigned long long hist[256];
@@ -749,6 +751,7 @@ __device__ void rej_sample(const RejArgs& g, int b, int c, int i, float* red, in
 
 template <bool VEC>
 __global__ void __launch_bounds__(256, 3) verify_rejection_kernel(RejArgs g) {
+  SPEC_TL(spec::kTLRejection);
   pdl_wait();
   pdl_trigger();
   extern __shared__ __align__(128) uint8_t vring[];   // chunk ring (VEC: kVRingBytes)
@@ -1066,3 +1069,6 @@ extern "C" spec_status spec_verify_greedy_static_error(int32_t* code_out, spec_s
   *code_out = v;
   return SPEC_OK;
 }
+
+// per-unit log setter of the instrumented build (no-op otherwise)
+SPEC_TL_SETTER(verify)
