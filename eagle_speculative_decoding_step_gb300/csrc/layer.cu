@@ -221,10 +221,17 @@ __global__ void epi_qkv_kernel(const float* __restrict__ part, SKPlan p, RowInfo
     b = row_req(ri, m);
     ci = ri.ctx_len[b] + row_kvidx(ri, m);
   }
-  const int nn[2] = {n1, n2};
+  // both features of the pair lie in one tile (heads do not straddle tiles): its
+  // segments are worked out once
+  SKTileSegs seg[2];
+  int lane[2], t1, t2;
+  sk_feature(p, n1, t1, lane[0]);
+  sk_feature(p, n2, t2, lane[1]);
+  seg[0] = sk_tile_segs(p, t1);
+  seg[1] = t2 == t1 ? seg[0] : sk_tile_segs(p, t2);
   const bool on[2] = {true, true};
   SKGather<2, kSegBatch> gat;
-  sk_gather<2, kSegBatch>(part, p, m, nn, on, gat);
+  sk_gather_segs<2, kSegBatch>(part, p, m, seg, lane, on, gat);
   const long long slot = hh >= nq ? slot_of(kv, b, ci) : 0;
   float xv[2];
   sk_reduce<2, kSegBatch>(p, gat, xv);
@@ -333,26 +340,40 @@ template <typename T, int U>
 __global__ void __launch_bounds__(256) epi_swiglu_kernel(const float* __restrict__ part, SKPlan p, int M, int I,
                                                          T* __restrict__ act) {
   SPEC_TL(spec::kTLSwiglu);
+  // the block's 2U gate tiles and 2U up tiles: their segments once, into shared
+  // memory, from the plan alone (before the dependency wait)
+  __shared__ SKTileSegs s_seg[4 * U];
+  const int ib = blockIdx.x * U * 256;
+  if (threadIdx.x < 4 * U) {
+    const int k = threadIdx.x, half = k / (2 * U);
+    int tile, lane;
+    sk_feature(p, half * I + min(ib + 128 * (k % (2 * U)), I - 1), tile, lane);
+    s_seg[k] = sk_tile_segs(p, tile);
+  }
   pdl_wait();
   pdl_trigger();
+  __syncthreads();
   const int m = blockIdx.y;
-  const int i0 = blockIdx.x * U * 256 + threadIdx.x;
-  int nn[2 * U];
+  SKTileSegs seg[2 * U];
+  int lane[2 * U];
   bool on[2 * U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    const int i = i0 + u * 256;
+    const int i = ib + threadIdx.x + u * 256;
     on[2 * u] = on[2 * u + 1] = i < I;
-    nn[2 * u] = i < I ? i : 0;
-    nn[2 * u + 1] = I + nn[2 * u];
+    lane[2 * u] = lane[2 * u + 1] = i & 127;
+    seg[2 * u] = s_seg[(threadIdx.x >> 7) + 2 * u];
+    seg[2 * u + 1] = s_seg[2 * U + (threadIdx.x >> 7) + 2 * u];
   }
+  SKGather<2 * U, 2> gat;
+  sk_gather_segs<2 * U, 2>(part, p, m, seg, lane, on, gat);
   float gu[2 * U];
-  sk_sum_n<2 * U, 2>(part, p, m, nn, on, gu);
+  sk_reduce<2 * U, 2>(p, gat, gu);
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     if (!on[2 * u]) continue;
     const float g = gu[2 * u], v = gu[2 * u + 1];
-    st(act + (size_t)m * I + nn[2 * u], g / (1.f + expf(-g)) * v);
+    st(act + (size_t)m * I + ib + threadIdx.x + u * 256, g / (1.f + expf(-g)) * v);
   }
 }
 

@@ -64,15 +64,15 @@ struct SKGather {
   bool on[NF];
 };
 // Issue the loads (sk_gather), do other work, then add them up (sk_reduce).
+// sk_gather_segs takes each feature's tile segments and lane from the caller
+// (e.g. a block-wide table in shared memory), sk_gather works them out.
 template <int NF, int SB>
-SPEC_DEV void sk_gather(const float* __restrict__ part, const SKPlan& p, int m, const int (&n)[NF],
-                        const bool (&on)[NF], SKGather<NF, SB>& g) {
+SPEC_DEV void sk_gather_segs(const float* __restrict__ part, const SKPlan& p, int m, const SKTileSegs (&seg)[NF],
+                             const int (&lane)[NF], const bool (&on)[NF], SKGather<NF, SB>& g) {
 #pragma unroll
   for (int f = 0; f < NF; ++f) {
-    int tile, lane;
-    sk_feature(p, n[f], tile, lane);
-    g.s[f] = sk_tile_segs(p, tile);
-    g.q[f] = part + (size_t)m * 128 + lane;
+    g.s[f] = seg[f];
+    g.q[f] = part + (size_t)m * 128 + lane[f];
     g.on[f] = on[f];
   }
 #pragma unroll
@@ -82,6 +82,19 @@ SPEC_DEV void sk_gather(const float* __restrict__ part, const SKPlan& p, int m, 
     for (int k = 0; k < SB; ++k)
       g.v[f][k] = on[f] && g.s[f].c0 + 1 + k <= g.s[f].c1 ? g.q[f][sk_slot(p, g.s[f].c0 + 1 + k, 0)] : 0.f;
   }
+}
+template <int NF, int SB>
+SPEC_DEV void sk_gather(const float* __restrict__ part, const SKPlan& p, int m, const int (&n)[NF],
+                        const bool (&on)[NF], SKGather<NF, SB>& g) {
+  SKTileSegs seg[NF];
+  int lane[NF];
+#pragma unroll
+  for (int f = 0; f < NF; ++f) {
+    int tile;
+    sk_feature(p, n[f], tile, lane[f]);
+    seg[f] = sk_tile_segs(p, tile);
+  }
+  sk_gather_segs<NF, SB>(part, p, m, seg, lane, on, g);
 }
 template <int NF, int SB>
 SPEC_DEV void sk_reduce(const SKPlan& p, const SKGather<NF, SB>& g, float (&out)[NF]) {
