@@ -269,29 +269,42 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
                    const T* __restrict__ hid_in, const T* __restrict__ gain, float* __restrict__ r,
                    T* __restrict__ out_a, T* __restrict__ out_b) {
   SPEC_TL(spec::kTLResnorm);
-  pdl_wait();
-  pdl_trigger();
   __shared__ float red[64];
   __shared__ float2 slot[kCL];
+  __shared__ SKTileSegs s_seg[kNormKeep * 1024 / 128 + 2];
   const int m = blockIdx.x / kCL, rk = blockIdx.x % kCL;
   const int n0 = rk * H / kCL, n1 = (rk + 1) * H / kCL;
   const T* h = (MODE == 0) ? hid_in + (size_t)row_src(ri, m) * H : nullptr;
   float* rr = r + (size_t)m * H;
   float ss = 0.f;
-  if (n1 - n0 <= kNormKeep * (int)blockDim.x) {
+  if (n1 - n0 <= kNormKeep * (int)blockDim.x && p.nmat == 1) {
     // at most kNormKeep features a thread: bases, partials and gains loaded at once,
-    // the row kept in registers across the cluster reduction
-    int nn[kNormKeep];
+    // the row kept in registers across the cluster reduction.  The segments of the
+    // block's tiles (from the plan) and the gains (weights) before the dependency wait.
+    const int tb = n0 >> 7;
+    for (int t = threadIdx.x; t <= ((n1 - 1) >> 7) - tb; t += blockDim.x) s_seg[t] = sk_tile_segs(p, tb + t);
+    int nn[kNormKeep], lane[kNormKeep];
     bool on[kNormKeep];
     float base[kNormKeep], sv[kNormKeep], gv[kNormKeep];
 #pragma unroll
     for (int u = 0; u < kNormKeep; ++u) {
       nn[u] = n0 + threadIdx.x + u * blockDim.x;
       on[u] = nn[u] < n1;
-      base[u] = !on[u] ? 0.f : (MODE == 0) ? ld(h + nn[u]) : (MODE == 1 ? rr[nn[u]] : 0.f);
+      lane[u] = nn[u] & 127;
       gv[u] = on[u] ? ld(gain + nn[u]) : 0.f;
     }
-    sk_sum_n<kNormKeep>(part, p, m, nn, on, sv);
+    pdl_wait();
+    pdl_trigger();
+    __syncthreads();
+    SKTileSegs seg[kNormKeep];
+#pragma unroll
+    for (int u = 0; u < kNormKeep; ++u) {
+      seg[u] = s_seg[on[u] ? (nn[u] >> 7) - tb : 0];
+      base[u] = !on[u] ? 0.f : (MODE == 0) ? ld(h + nn[u]) : (MODE == 1 ? rr[nn[u]] : 0.f);
+    }
+    SKGather<kNormKeep, kSegBatch> gat;
+    sk_gather_segs<kNormKeep, kSegBatch>(part, p, m, seg, lane, on, gat);
+    sk_reduce<kNormKeep, kSegBatch>(p, gat, sv);
 #pragma unroll
     for (int u = 0; u < kNormKeep; ++u) {
       sv[u] += base[u];
@@ -307,6 +320,8 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
       if (on[u]) st(out_b + (size_t)m * H + nn[u], sv[u] * rs * gv[u]);
     return;
   }
+  pdl_wait();
+  pdl_trigger();
   // two features a thread per round, their partials' loads in flight together
   for (int n = n0 + threadIdx.x; n < n1; n += 2 * blockDim.x) {
     const int nn[2] = {n, n + (int)blockDim.x};
