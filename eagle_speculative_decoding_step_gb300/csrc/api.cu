@@ -75,7 +75,7 @@ SKPlan make_plan(const int* rows, int nmat, int K, int M, int G) {
   // at least kMinIters iterations per CTA (a tiny GEMM -- one tile, long K -- would
   // otherwise leave one partial per CTA for its epilogue to add up), but every tile
   // keeps a CTA of its own
-  constexpr long long kMinIters = 8;
+  constexpr long long kMinIters = 4;
   p.G = (int)std::min<long long>(G, std::max<long long>(p.ntiles, (p.T + kMinIters - 1) / kMinIters));
   if (p.G < 1) p.G = 1;
   p.mpad = tc_mpad(M);

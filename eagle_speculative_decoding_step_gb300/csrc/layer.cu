@@ -187,12 +187,23 @@ template <typename TO>
 __global__ void epi_store_kernel(const float* __restrict__ part, SKPlan p, int M, int N, TO* __restrict__ out,
                                  int ld_out) {
   SPEC_TL(spec::kTLEpiStore);
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool live = idx < (long long)M * N;
+  const int m = live ? (int)(idx / N) : 0, n = live ? (int)(idx % N) : 0;
+  // the feature's tile segments from the plan before the dependency wait
+  SKTileSegs seg[1];
+  int lane[1], tile;
+  sk_feature(p, n, tile, lane[0]);
+  seg[0] = sk_tile_segs(p, tile);
   pdl_wait();
   pdl_trigger();
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long long)M * N) return;
-  const int m = (int)(idx / N), n = (int)(idx % N);
-  st(out + (size_t)m * ld_out + n, sk_sum(part, p, m, n));
+  if (!live) return;
+  const bool on[1] = {true};
+  SKGather<1, 16> gat;                        // up to 17 segments (one-tile GEMMs with a long K) at once
+  sk_gather_segs<1, 16>(part, p, m, seg, lane, on, gat);
+  float v[1];
+  sk_reduce<1, 16>(p, gat, v);
+  st(out + (size_t)m * ld_out + n, v[0]);
 }
 
 // q / k get the rotary embedding (pairs i, i + hd/2), v is copied; q goes to
@@ -202,37 +213,49 @@ __global__ void epi_qkv_kernel(const float* __restrict__ part, SKPlan p, RowInfo
                                const float2* __restrict__ cs, T* __restrict__ qbuf, spec_kv kv, int* __restrict__ work,
                                void* ws) {
   SPEC_TL(spec::kTLEpiQkv);
-  pdl_wait();
-  pdl_trigger();
-  if (work != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *work = 0;   // the attention's item counter
   const int half = hd / 2;
   const int nh = nq + 2 * nkv;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long long)ri.M * nh * half) return;
-  const int m = (int)(idx / (nh * half));
-  const int rem = (int)(idx % (nh * half));
+  const bool live = idx < (long long)ri.M * nh * half;
+  const int m = live ? (int)(idx / (nh * half)) : 0;
+  const int rem = live ? (int)(idx % (nh * half)) : 0;
   const int hh = rem / half, i = rem % half;
   const int n1 = hh * hd + i, n2 = n1 + half;
-  // the rotary pair and the row's cache entry are read while the partials load
-  float2 c = make_float2(1.f, 0.f);
-  if (hh < nq + nkv) c = cs[(size_t)m * half + i];
-  int b = 0, ci = 0;
-  if (hh >= nq) {
-    b = row_req(ri, m);
-    ci = ri.ctx_len[b] + row_kvidx(ri, m);
-  }
-  // both features of the pair lie in one tile (heads do not straddle tiles): its
-  // segments are worked out once
+  // Before the dependency wait: the pair's tile segments (both features lie in
+  // one tile -- heads do not straddle tiles -- so worked out once), and for a K / V
+  // head the row's cache slot.  Context lengths, cache indices and the block table
+  // are inputs of the call that no kernel of it writes, and this kernel starts only
+  // once every block of the QKV GEMM has passed its own wait, i.e. after the
+  // prologue (and all earlier launches) finished; they are read through L2.
   SKTileSegs seg[2];
   int lane[2], t1, t2;
   sk_feature(p, n1, t1, lane[0]);
   sk_feature(p, n2, t2, lane[1]);
   seg[0] = sk_tile_segs(p, t1);
   seg[1] = t2 == t1 ? seg[0] : sk_tile_segs(p, t2);
+  int b = 0, ci = 0;
+  long long slot = 0;
+  if (live && hh >= nq) {
+    b = row_req(ri, m);
+    ci = __ldcg(ri.ctx_len + b) + (ri.kv_idx ? __ldcg(ri.kv_idx + m) : ri.step);
+    const int blk = ci / kv.block_size;
+    slot = -1;
+    if (ci >= 0 && blk < kv.max_blocks) {
+      const long long s0 = (long long)__ldcg(kv.block_table + (long long)b * kv.max_blocks + blk) * kv.block_size +
+                           ci % kv.block_size;
+      if (s0 >= 0 && s0 < kv.num_slots) slot = s0;
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (work != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *work = 0;   // the attention's item counter
+  if (!live) return;
+  // the rotary pair (written by the prologue) is read while the partials load
+  float2 c = make_float2(1.f, 0.f);
+  if (hh < nq + nkv) c = cs[(size_t)m * half + i];
   const bool on[2] = {true, true};
   SKGather<2, kSegBatch> gat;
   sk_gather_segs<2, kSegBatch>(part, p, m, seg, lane, on, gat);
-  const long long slot = hh >= nq ? slot_of(kv, b, ci) : 0;
   float xv[2];
   sk_reduce<2, kSegBatch>(p, gat, xv);
   float x1 = xv[0], x2 = xv[1];
