@@ -90,6 +90,9 @@ struct EpiPartial {
   SPEC_DEV bool after(const Seg&, int, int) { return true; }
   SPEC_DEV bool segment(const Seg& s, uint32_t tb, int warp, int lane) {
     float* dst = P.part + sk_slot(P.p, c, s.idx) + warp * 32 + lane;
+    // the partials stay in L2 (evict-last) for the epilogue kernel that reduces them,
+    // through the weights streaming past (evict-first)
+    const uint64_t keep = policy_evict_last();
     // up to 64 accumulator columns in flight before one wait
     constexpr int CB = MPAD < 64 ? MPAD : 64;
 #pragma unroll
@@ -103,7 +106,9 @@ struct EpiPartial {
 #pragma unroll
       for (int q = 0; q < CB; ++q) {
         const int m = cb + q;
-        if (m < P.M) dst[(size_t)m * 128] = __uint_as_float(r[q]);
+        if (m < P.M)
+          asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(dst + (size_t)m * 128), "r"(r[q]), "l"(keep)
+                       : "memory");
       }
     }
     return true;
