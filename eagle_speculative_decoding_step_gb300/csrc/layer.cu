@@ -292,6 +292,9 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
                    const T* __restrict__ hid_in, const T* __restrict__ gain, float* __restrict__ r,
                    T* __restrict__ out_a, T* __restrict__ out_b) {
   SPEC_TL(spec::kTLResnorm);
+  // the next launch (a GEMM) may start and fill its ring with weight tiles once every
+  // block of this one has started, instead of after this kernel's dependency wait
+  pdl_trigger();
   __shared__ float red[64];
   __shared__ float2 slot[kCL];
   __shared__ SKTileSegs s_seg[kNormKeep * 1024 / 128 + 2];
@@ -317,8 +320,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
       gv[u] = on[u] ? ld(gain + nn[u]) : 0.f;
     }
     pdl_wait();
-    pdl_trigger();
-    __syncthreads();
+      __syncthreads();
     SKTileSegs seg[kNormKeep];
 #pragma unroll
     for (int u = 0; u < kNormKeep; ++u) {
@@ -344,7 +346,6 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(NormCL<kCL>::kThre
     return;
   }
   pdl_wait();
-  pdl_trigger();
   // two features a thread per round, their partials' loads in flight together
   for (int n = n0 + threadIdx.x; n < n1; n += 2 * blockDim.x) {
     const int nn[2] = {n, n + (int)blockDim.x};
@@ -378,6 +379,9 @@ template <typename T, int U>
 __global__ void __launch_bounds__(256) epi_swiglu_kernel(const float* __restrict__ part, SKPlan p, int M, int I,
                                                          T* __restrict__ act) {
   SPEC_TL(spec::kTLSwiglu);
+  // one feature a thread (small batches): the down projection may start and fill its
+  // ring once every block has started (measured better there, worse at four)
+  if (U == 1) pdl_trigger();
   // the block's 2U gate tiles and 2U up tiles: their segments once, into shared
   // memory, from the plan alone (before the dependency wait)
   __shared__ SKTileSegs s_seg[4 * U];
@@ -389,7 +393,7 @@ __global__ void __launch_bounds__(256) epi_swiglu_kernel(const float* __restrict
     s_seg[k] = sk_tile_segs(p, tile);
   }
   pdl_wait();
-  pdl_trigger();
+  if (U != 1) pdl_trigger();
   __syncthreads();
   const int m = blockIdx.y;
   SKTileSegs seg[2 * U];
