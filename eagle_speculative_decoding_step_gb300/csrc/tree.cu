@@ -62,7 +62,7 @@ __device__ __forceinline__ bool ranks_before(float sa, int ia, float sb, int ib)
   return sa > sb || (sa == sb && ia < ib);
 }
 
-__global__ void __launch_bounds__(256) tree_expand_kernel(TreeDims td, int d, const int32_t* __restrict__ ctx_len,
+__global__ void __launch_bounds__(1024) tree_expand_kernel(TreeDims td, int d, const int32_t* __restrict__ ctx_len,
                                                           const int32_t* __restrict__ root_tok,
                                                           const int32_t* __restrict__ ids,
                                                           const float* __restrict__ lp, void* state,
@@ -143,26 +143,36 @@ __global__ void __launch_bounds__(256) tree_expand_kernel(TreeDims td, int d, co
     }
     return;
   }
-  // 3b. final selection: the N best of the pool, numbered by (depth, score, creation)
+  // 3b. final selection: the N best of the pool, numbered by (depth, score, creation).
+  // A candidate's rank is counted by four threads (every fourth pool entry each);
+  // the order of the N selected by a warp each (every 32nd entry a lane).
   const int N = td.N;
-  for (int p = threadIdx.x; p < cnt; p += blockDim.x) {
-    const float sp = s_score[p];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  for (int base = 0; base < cnt; base += blockDim.x / 4) {
+    const int p = base + (int)threadIdx.x / 4, q = threadIdx.x & 3;
     int r = 0;
-    for (int u = 0; u < cnt; ++u) r += ranks_before(s_score[u], u, sp, p) ? 1 : 0;
-    s_map[p] = (r < N) ? 0 : -1;
+    if (p < cnt) {
+      const float sp = s_score[p];
+      for (int u = q; u < cnt; u += 4) r += ranks_before(s_score[u], u, sp, p) ? 1 : 0;
+    }
+    r += __shfl_xor_sync(0xffffffffu, r, 1);
+    r += __shfl_xor_sync(0xffffffffu, r, 2);
+    if (p < cnt && q == 0) s_map[p] = (r < N) ? 0 : -1;
   }
   __syncthreads();
-  for (int p = threadIdx.x; p < cnt; p += blockDim.x) {
-    if (s_map[p] < 0) continue;
+  for (int p = warp; p < cnt; p += nwarp) {
+    if (s_map[p] < 0) continue;                 // uniform in the warp
     const int dp = s_depth[p];
     const float sp = s_score[p];
     int r = 0;
-    for (int u = 0; u < cnt; ++u) {
+    for (int u = lane; u < cnt; u += 32) {
       if (s_map[u] < 0) continue;
       const int du = s_depth[u];
       r += (du < dp || (du == dp && ranks_before(s_score[u], u, sp, p))) ? 1 : 0;
     }
-    s_order[r] = p;    // final index r + 1
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    if (lane == 0) s_order[r] = p;    // final index r + 1
   }
   __syncthreads();
   // final index of every selected node; then one thread per node writes its
@@ -234,7 +244,7 @@ extern "C" spec_status spec_tree_expand(int32_t B, int32_t top_k, int32_t depth_
       return SPEC_ERR_ARG;
   }
   TreeDims td{top_k, draft_depth, total, P};
-  launch_pdl(tree_expand_kernel, dim3(B), dim3(256), 0, stream, td, depth_idx, ctx_len, root_tok, topk_ids, topk_logprob, tree_state,
+  launch_pdl(tree_expand_kernel, dim3(B), dim3(1024), 0, stream, td, depth_idx, ctx_len, root_tok, topk_ids, topk_logprob, tree_state,
                                             *io);
   return last_launch();
 }
