@@ -105,8 +105,9 @@ def _lib():
     global _LIB
     if _LIB is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError("libeaglespec.so is not built (run `python -m "
-                               "eagle_speculative_decoding_step_gb300.build`); there is no fallback")
+            raise RuntimeError("%s is not built (run `python -m eagle_speculative_decoding_step_gb300.build`%s); "
+                               "there is no fallback" % (os.path.basename(LIB_PATH),
+                                                         " -t" if "timeline" in LIB_PATH else ""))
         lib = ctypes.CDLL(LIB_PATH)
         for name, (res, args) in EXPORTS.items():
             f = getattr(lib, name)
