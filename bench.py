@@ -701,7 +701,7 @@ def run_timeline(args, w):
     with open(args.timeline, "w") as f:
         f.write("# Timeline: %s, one graph-replayed step (instrumented build)\n\n" % w.name)
         f.write(timeline.markdown(step) + "\n\nLaunch sequence (us from the step's first launch: start, end, "
-                "duration, kernel, blocks):\n\n```\n" + timeline.sequence(step) + "\n```\n")
+                "duration, tail, kernel, blocks):\n\n```\n" + timeline.sequence(step) + "\n```\n")
     print(timeline.markdown(step))
 
 

@@ -51,7 +51,9 @@ def launches(log):
         while i < len(sel):
             g = max(1, int(grid[sel[i]]))
             blk = sel[i:i + g]
-            out.append({"start": int(e[blk, 0].min()), "end": int(e[blk, 2].max()),
+            ends = e[blk, 2]
+            out.append({"start": int(e[blk, 0].min()), "end": int(ends.max()),
+                        "tail": int(ends.max() - np.median(ends)),
                         "name": NAMES[int(k)] if int(k) < len(NAMES) else "kernel %d" % k,
                         "blocks": len(blk), "grid": g})
             i += g
@@ -77,32 +79,35 @@ def attribute(step):
     for l in step:
         charged = max(0, l["end"] - max(prev, l["start"]))
         prev = max(prev, l["end"])
-        d = per.setdefault(l["name"], {"launches": 0, "dur_ns": 0, "charged_ns": 0})
+        d = per.setdefault(l["name"], {"launches": 0, "dur_ns": 0, "charged_ns": 0, "tail_ns": 0})
         d["launches"] += 1
         d["dur_ns"] += l["end"] - l["start"]
         d["charged_ns"] += charged
+        d["tail_ns"] += l.get("tail", 0)
     return per, (prev - t0)
 
 
 def markdown(step):
     """Table of one step's kernels, largest charged time first."""
     per, span = attribute(step)
-    lines = ["| kernel | launches | charged us | share | mean launch us (start to end) |",
-             "|---|---|---|---|---|"]
+    lines = ["| kernel | launches | charged us | share | mean launch us (start to end) | mean tail us |",
+             "|---|---|---|---|---|---|"]
     for name, d in sorted(per.items(), key=lambda x: -x[1]["charged_ns"]):
-        lines.append("| `%s` | %d | %.1f | %.1f %% | %.1f |" % (
+        lines.append("| `%s` | %d | %.1f | %.1f %% | %.1f | %.1f |" % (
             name, d["launches"], d["charged_ns"] / 1e3, 100.0 * d["charged_ns"] / max(span, 1),
-            d["dur_ns"] / d["launches"] / 1e3))
+            d["dur_ns"] / d["launches"] / 1e3, d["tail_ns"] / d["launches"] / 1e3))
     lines.append("")
-    lines.append("Step span (first launch start to last end): %.1f us, %d launches." % (span / 1e3, len(step)))
+    lines.append("Step span (first launch start to last end): %.1f us, %d launches.  Tail: a launch's last "
+                 "block end minus its median block end (for the one-block-per-SM GEMMs, how much the slowest "
+                 "SM's share lags)." % (span / 1e3, len(step)))
     return "\n".join(lines)
 
 
 def sequence(step):
-    """One line per launch: start, end (us from the step's first start), duration, name, blocks."""
+    """One line per launch: start, end (us from the step's first start), duration, tail, name, blocks."""
     if not step:
         return ""
     t0 = step[0]["start"]
-    return "\n".join("%9.1f %9.1f %8.1f  %-28s %d" % ((l["start"] - t0) / 1e3, (l["end"] - t0) / 1e3,
-                                                      (l["end"] - l["start"]) / 1e3, l["name"], l["blocks"])
-                     for l in step)
+    return "\n".join("%9.1f %9.1f %8.1f %6.1f  %-28s %d" % (
+        (l["start"] - t0) / 1e3, (l["end"] - t0) / 1e3, (l["end"] - l["start"]) / 1e3, l.get("tail", 0) / 1e3,
+        l["name"], l["blocks"]) for l in step)

@@ -25,6 +25,8 @@ def test_launches_group_blocks_by_grid_in_start_order():
     ls = tl.launches(_log(blocks))
     assert [(l["name"].split()[0], l["start"], l["end"], l["blocks"]) for l in ls] == [
         ("tc_kernel", 100, 520, 2), ("resnorm_kernel", 400, 700, 1), ("tc_kernel", 790, 1200, 2)]
+    # tail: last block end minus the median block end
+    assert [l["tail"] for l in ls] == [10, 0, 50]
 
 
 def test_attribution_splits_the_step_span_along_the_sequence():
